@@ -1,0 +1,301 @@
+/*
+ * Plain fp64 CPU oracle for scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path may call, link or
+ * load this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do. It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes (written straight from the definitions, no tiling, no
+ * online softmax, no reordering beyond the per-row loops below):
+ *
+ *   "Inside NVIDIA's cuDNN Graph API" (tradepoint.io), section 5
+ *   "SDPA (Flash Attention) with causal masking": the op is
+ *   O = softmax(attn_scale * Q K^T + causal mask) V, with the causal mask
+ *   aligned top-left (diagonal_alignment TOP_LEFT, right_bound 0), i.e.
+ *   query row i may attend to key j iff j <= i.  The same alignment is the
+ *   TransformerEngine PR #2964 note that the causal mask becomes
+ *   set_diagonal_band_right_bound(0).
+ *
+ *   cudnn-frontend PR #554, commit "dense backward" notes: the per-row
+ *   statistic is aten's logsumexp of the scaled scores, fp32, shape
+ *   (B, H, S); packed THD statistics are token-major (T, H).
+ *
+ *   The analytic backward of softmax attention (standard calculus, no page
+ *   prints it): D_i = sum_k dO[i,k] O[i,k]; dP_ij = dO_i . V_j;
+ *   dS_ij = P_ij (dP_ij - D_i); dQ_i = scale sum_j dS_ij K_j;
+ *   dK_j = scale sum_i dS_ij Q_i; dV_j = sum_i P_ij dO_i.
+ *
+ * Allowed key set of query row i (top-left alignment):
+ *   A_i = { j : 0 <= j < n_kv  and  (not causal  or  j <= i) }
+ * which is always the prefix j < n_allowed(i).  A row whose set is empty is
+ * "dead": O_i = 0, LSE_i = -inf, and it contributes nothing to any gradient
+ * (cudnn-frontend PR #554, FP8 d512 notes on fully-masked rows and the
+ * zero-length-KV THD test).
+ *
+ * All arrays are fp64.  Each attention problem is one (batch, head) or one
+ * (sequence, head) slice, addressed by a base pointer and a row stride in
+ * elements, so dense BHSD and packed THD both reduce to it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static int n_allowed(int i, int n_kv, int causal)
+{
+    if (!causal) return n_kv;
+    return (i + 1 < n_kv) ? i + 1 : n_kv;
+}
+
+static double dot(const double *a, const double *b, int d)
+{
+    double s = 0.0;
+    for (int t = 0; t < d; ++t) s += a[t] * b[t];
+    return s;
+}
+
+/* One query row: fills p[0..na) with the softmax probabilities, returns LSE.
+ * s_ij = scale * q.k_j;  m = max_j s_ij;  LSE = m + ln sum_j exp(s_ij - m);
+ * P_ij = exp(s_ij - LSE). */
+static double row_probs(const double *q, const double *k, int64_t k_rs, int na,
+                        int d, double scale, double *p)
+{
+    if (na == 0) return -INFINITY;
+    double m = -INFINITY;
+    for (int j = 0; j < na; ++j) {
+        p[j] = scale * dot(q, k + (int64_t)j * k_rs, d);
+        if (p[j] > m) m = p[j];
+    }
+    double sum = 0.0;
+    for (int j = 0; j < na; ++j) sum += exp(p[j] - m);
+    double lse = m + log(sum);
+    for (int j = 0; j < na; ++j) p[j] = exp(p[j] - lse);
+    return lse;
+}
+
+/* O_i = sum_j P_ij V_j */
+static void row_output(const double *p, const double *v, int64_t v_rs, int na,
+                       int d, double *o)
+{
+    for (int t = 0; t < d; ++t) o[t] = 0.0;
+    for (int j = 0; j < na; ++j) {
+        const double *vj = v + (int64_t)j * v_rs;
+        for (int t = 0; t < d; ++t) o[t] += p[j] * vj[t];
+    }
+}
+
+/* Forward of one problem, rows listed in `rows` (or all rows if rows==NULL).
+ * Outputs go to o + r*o_rs and lse + r*lse_rs where r is the position in the
+ * row list (or the row index itself when rows==NULL). */
+static void fwd_problem(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
+                        const double *v, int64_t v_rs, double *o, int64_t o_rs,
+                        double *lse, int64_t lse_rs, int n_q, int n_kv, int d,
+                        double scale, int causal, const int32_t *rows, int n_rows)
+{
+    int count = rows ? n_rows : n_q;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(n_kv > 0 ? n_kv : 1));
+#pragma omp for schedule(dynamic, 4)
+        for (int r = 0; r < count; ++r) {
+            int i = rows ? rows[r] : r;
+            int na = n_allowed(i, n_kv, causal);
+            double l = row_probs(q + (int64_t)i * q_rs, k, k_rs, na, d, scale, p);
+            row_output(p, v, v_rs, na, d, o + (int64_t)r * o_rs);
+            if (lse) lse[(int64_t)r * lse_rs] = l;
+        }
+        free(p);
+    }
+}
+
+/* Backward of one problem.  Pass 1 (independent rows i): LSE_i, D_i and dQ_i.
+ * Pass 2 (independent key rows j): dK_j and dV_j, re-deriving P_ij and dS_ij
+ * from the pass-1 LSE_i and D_i.  Either pass can be restricted to a list of
+ * rows; the statistics of pass 1 are always computed for every row because
+ * pass 2 needs all of them. */
+static void bwd_problem(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
+                        const double *v, int64_t v_rs, const double *dout, int64_t do_rs,
+                        double *dq, int64_t dq_rs, double *dk, int64_t dk_rs,
+                        double *dv, int64_t dv_rs, int n_q, int n_kv, int d,
+                        double scale, int causal,
+                        const int32_t *q_rows, int n_q_rows,
+                        const int32_t *kv_rows, int n_kv_rows)
+{
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(n_q > 0 ? n_q : 1));
+    double *D = (double *)malloc(sizeof(double) * (size_t)(n_q > 0 ? n_q : 1));
+    /* dq output slot of row i, or -1 when dQ_i is not requested */
+    int32_t *dq_slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_q > 0 ? n_q : 1));
+    for (int i = 0; i < n_q; ++i) dq_slot[i] = q_rows ? -1 : i;
+    if (q_rows)
+        for (int r = 0; r < n_q_rows; ++r) dq_slot[q_rows[r]] = r;
+
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(n_kv > 0 ? n_kv : 1));
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int i = 0; i < n_q; ++i) {
+            int na = n_allowed(i, n_kv, causal);
+            const double *qi = q + (int64_t)i * q_rs;
+            const double *doi = dout + (int64_t)i * do_rs;
+            lse[i] = row_probs(qi, k, k_rs, na, d, scale, p);
+            row_output(p, v, v_rs, na, d, o);
+            D[i] = dot(doi, o, d);
+            int slot = dq_slot[i];
+            if (slot < 0) continue;
+            double *dqi = dq + (int64_t)slot * dq_rs;
+            for (int t = 0; t < d; ++t) dqi[t] = 0.0;
+            for (int j = 0; j < na; ++j) {
+                const double *kj = k + (int64_t)j * k_rs;
+                double dp = dot(doi, v + (int64_t)j * v_rs, d);
+                double ds = p[j] * (dp - D[i]);
+                for (int t = 0; t < d; ++t) dqi[t] += scale * ds * kj[t];
+            }
+        }
+        free(p);
+        free(o);
+    }
+
+    int count = kv_rows ? n_kv_rows : n_kv;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int r = 0; r < count; ++r) {
+        int j = kv_rows ? kv_rows[r] : r;
+        const double *kj = k + (int64_t)j * k_rs;
+        const double *vj = v + (int64_t)j * v_rs;
+        double *dkj = dk + (int64_t)r * dk_rs;
+        double *dvj = dv + (int64_t)r * dv_rs;
+        for (int t = 0; t < d; ++t) { dkj[t] = 0.0; dvj[t] = 0.0; }
+        for (int i = 0; i < n_q; ++i) {
+            if (j >= n_allowed(i, n_kv, causal)) continue;
+            const double *qi = q + (int64_t)i * q_rs;
+            const double *doi = dout + (int64_t)i * do_rs;
+            double pij = exp(scale * dot(qi, kj, d) - lse[i]);
+            double dp = dot(doi, vj, d);
+            double ds = pij * (dp - D[i]);
+            for (int t = 0; t < d; ++t) {
+                dvj[t] += pij * doi[t];
+                dkj[t] += scale * ds * qi[t];
+            }
+        }
+    }
+    free(lse);
+    free(D);
+    free(dq_slot);
+}
+
+/* ------------------------------------------------------------------ */
+/* Exported entry points                                                */
+/* ------------------------------------------------------------------ */
+
+/* One problem, explicit row strides (elements). */
+void oracle_attn_fwd(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
+                     const double *v, int64_t v_rs, double *o, int64_t o_rs,
+                     double *lse, int64_t lse_rs, int n_q, int n_kv, int d,
+                     double scale, int causal)
+{
+    fwd_problem(q, q_rs, k, k_rs, v, v_rs, o, o_rs, lse, lse_rs, n_q, n_kv, d,
+                scale, causal, NULL, 0);
+}
+
+/* Selected rows of one problem; outputs packed [n_rows, d] and [n_rows]. */
+void oracle_attn_fwd_rows(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
+                          const double *v, int64_t v_rs, double *o, double *lse,
+                          int n_q, int n_kv, int d, double scale, int causal,
+                          const int32_t *rows, int n_rows)
+{
+    (void)n_q;
+    fwd_problem(q, q_rs, k, k_rs, v, v_rs, o, d, lse, 1, n_q, n_kv, d, scale,
+                causal, rows, n_rows);
+}
+
+void oracle_attn_bwd(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
+                     const double *v, int64_t v_rs, const double *dout, int64_t do_rs,
+                     double *dq, int64_t dq_rs, double *dk, int64_t dk_rs,
+                     double *dv, int64_t dv_rs, int n_q, int n_kv, int d,
+                     double scale, int causal)
+{
+    bwd_problem(q, q_rs, k, k_rs, v, v_rs, dout, do_rs, dq, dq_rs, dk, dk_rs, dv,
+                dv_rs, n_q, n_kv, d, scale, causal, NULL, 0, NULL, 0);
+}
+
+/* Selected dQ rows and dK/dV rows of one problem; outputs packed. */
+void oracle_attn_bwd_rows(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
+                          const double *v, int64_t v_rs, const double *dout, int64_t do_rs,
+                          double *dq, double *dk, double *dv, int n_q, int n_kv, int d,
+                          double scale, int causal, const int32_t *q_rows, int n_q_rows,
+                          const int32_t *kv_rows, int n_kv_rows)
+{
+    bwd_problem(q, q_rs, k, k_rs, v, v_rs, dout, do_rs, dq, d, dk, d, dv, d, n_q,
+                n_kv, d, scale, causal, q_rows, n_q_rows, kv_rows, n_kv_rows);
+}
+
+/* Dense BHSD: q,o [b,h,s_q,d]; k,v [b,h,s_kv,d]; lse [b,h,s_q]. */
+void oracle_sdpa_fwd(const double *q, const double *k, const double *v, double *o,
+                     double *lse, int b, int h, int s_q, int s_kv, int d,
+                     double scale, int causal)
+{
+    for (int64_t bh = 0; bh < (int64_t)b * h; ++bh)
+        fwd_problem(q + bh * s_q * d, d, k + bh * s_kv * d, d, v + bh * s_kv * d, d,
+                    o + bh * s_q * d, d, lse + bh * s_q, 1, s_q, s_kv, d, scale,
+                    causal, NULL, 0);
+}
+
+void oracle_sdpa_bwd(const double *q, const double *k, const double *v,
+                     const double *dout, double *dq, double *dk, double *dv, int b,
+                     int h, int s_q, int s_kv, int d, double scale, int causal)
+{
+    for (int64_t bh = 0; bh < (int64_t)b * h; ++bh)
+        bwd_problem(q + bh * s_q * d, d, k + bh * s_kv * d, d, v + bh * s_kv * d, d,
+                    dout + bh * s_q * d, d, dq + bh * s_q * d, d, dk + bh * s_kv * d,
+                    d, dv + bh * s_kv * d, d, s_q, s_kv, d, scale, causal, NULL, 0,
+                    NULL, 0);
+}
+
+/* Packed THD: q,o [total_q,h,d]; k,v [total_kv,h,d]; lse [total_q,h];
+ * sequence n owns query tokens [cu_q[n], cu_q[n+1]) and key tokens
+ * [cu_kv[n], cu_kv[n+1]); the mask is applied per sequence. */
+void oracle_sdpa_varlen_fwd(const double *q, const double *k, const double *v,
+                            double *o, double *lse, const int32_t *cu_q,
+                            const int32_t *cu_kv, int num_seqs, int h, int d,
+                            double scale, int causal)
+{
+    int64_t rs = (int64_t)h * d;
+    for (int n = 0; n < num_seqs; ++n) {
+        int nq = cu_q[n + 1] - cu_q[n], nkv = cu_kv[n + 1] - cu_kv[n];
+        for (int hh = 0; hh < h; ++hh) {
+            int64_t qo = (int64_t)cu_q[n] * rs + (int64_t)hh * d;
+            int64_t ko = (int64_t)cu_kv[n] * rs + (int64_t)hh * d;
+            fwd_problem(q + qo, rs, k + ko, rs, v + ko, rs, o + qo, rs,
+                        lse + (int64_t)cu_q[n] * h + hh, h, nq, nkv, d, scale,
+                        causal, NULL, 0);
+        }
+    }
+}
+
+void oracle_sdpa_varlen_bwd(const double *q, const double *k, const double *v,
+                            const double *dout, double *dq, double *dk, double *dv,
+                            const int32_t *cu_q, const int32_t *cu_kv, int num_seqs,
+                            int h, int d, double scale, int causal)
+{
+    int64_t rs = (int64_t)h * d;
+    for (int n = 0; n < num_seqs; ++n) {
+        int nq = cu_q[n + 1] - cu_q[n], nkv = cu_kv[n + 1] - cu_kv[n];
+        for (int hh = 0; hh < h; ++hh) {
+            int64_t qo = (int64_t)cu_q[n] * rs + (int64_t)hh * d;
+            int64_t ko = (int64_t)cu_kv[n] * rs + (int64_t)hh * d;
+            bwd_problem(q + qo, rs, k + ko, rs, v + ko, rs, dout + qo, rs, dq + qo,
+                        rs, dk + ko, rs, dv + ko, rs, nq, nkv, d, scale, causal,
+                        NULL, 0, NULL, 0);
+        }
+    }
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
