@@ -1,0 +1,172 @@
+/*
+ * sdpa.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product attention
+ * library (libsdpa_gb300.so).
+ *
+ * The operation (forward), as "Inside NVIDIA's cuDNN Graph API" (tradepoint.io),
+ * section 5 "SDPA (Flash Attention) with causal masking" builds it:
+ *
+ *     O = softmax(attn_scale * Q K^T + mask) V
+ *
+ * with the causal mask aligned top-left (diagonal_alignment TOP_LEFT,
+ * right_bound 0): query row i attends to key j iff j <= i.  The same page
+ * counts its cost as 4*b*h*s*s*d*0.5 FLOPs when causal.  Besides O the
+ * forward writes the per-row statistic
+ *
+ *     LSE_i = ln sum_{j allowed} exp(attn_scale * Q_i . K_j)
+ *
+ * (natural log of the scaled scores), fp32, in aten's logsumexp layout for
+ * dense tensors and token-major for packed tensors (cudnn-frontend PR #554,
+ * dense-backward and THD-statistics notes).  A row with no allowed key (only
+ * possible when its sequence has zero keys) gets O = 0 and LSE = -inf
+ * (cudnn-frontend PR #554, FP8 d512 notes on fully-masked rows).
+ *
+ * The backward recomputes P from the stored LSE and returns dQ, dK, dV in
+ * the layouts of Q, K, V (cudnn-frontend PR #554, "dense backward" notes).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library allocates no device memory and never synchronises the host; it
+ *    enqueues work on `stream` (0 = legacy default stream) and returns.
+ *  - Element types: `dtype` is SDPA_BF16 or SDPA_FP16 for q, k, v, o, dout,
+ *    dq, dk, dv.  lse is always fp32.  Arithmetic is fp32 throughout
+ *    (tensor-core fp32 accumulation, fp32 softmax statistics).
+ *  - Head dimension d must be 64 or 128.
+ *  - Every tensor pointer must be 16-byte aligned and tensors are dense
+ *    (contiguous innermost dimension, no gaps), as the pages' descriptor
+ *    contract requires (cudnn-frontend PR #554, "normalize dense operands").
+ *  - Arguments are validated before anything is enqueued; on an error the
+ *    function returns a non-zero sdpa_status, writes nothing, and
+ *    sdpa_last_error() describes the problem.
+ *  - Empty problems (any of b, h, s_q, total_q equal to 0) return SDPA_OK
+ *    without launching.  s_kv == 0 (or a sequence with no keys) is valid and
+ *    yields dead rows.
+ *  - Host scalars (total_q, total_kv, max_seqlen_*) describe the packed
+ *    problem so that nothing is read back from the device (cudnn-frontend
+ *    PR #554, "no D2H sync in varlen backward" and "max_s_kv grid hint").
+ *    The device-side cu_seqlens must be non-decreasing, start at 0 and end
+ *    at total_q / total_kv; this is the caller's contract and is not checked.
+ *  - Calls are thread-safe; sdpa_last_error() is per host thread.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (a cudaStream_t); NULL is the legacy stream. */
+typedef void *sdpa_stream_t;
+
+typedef enum {
+    SDPA_OK = 0,
+    SDPA_ERR_INVALID_ARG = 1, /* negative size, NULL pointer, aliasing, bad flag */
+    SDPA_ERR_UNSUPPORTED = 2, /* d not in {64,128}, unknown dtype, wrong GPU */
+    SDPA_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned */
+    SDPA_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required */
+    SDPA_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+    SDPA_ERR_TIMEOUT = 6      /* a kernel gave up on a bounded wait */
+} sdpa_status;
+
+typedef enum { SDPA_BF16 = 0, SDPA_FP16 = 1 } sdpa_dtype;
+
+/*
+ * Dense forward (BHSD).
+ *   q, o : [b, h, s_q, d]   (dtype)      k, v : [b, h, s_kv, d] (dtype)
+ *   lse  : [b, h, s_q] fp32, or NULL to skip writing it.
+ *   attn_scale: multiplier of Q K^T (the pages' default is 1/sqrt(d); the
+ *   ABI takes it explicitly).  causal: 0 or 1 (top-left alignment).
+ * o and lse must not overlap q, k or v.
+ */
+int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int b, int h, int s_q, int s_kv, int d, float attn_scale,
+             int causal, int dtype, sdpa_stream_t stream);
+
+/*
+ * Packed (THD / varlen) forward.
+ *   q, o : [total_q, h, d]   k, v : [total_kv, h, d]   lse : [total_q, h] fp32
+ *   (token-major) or NULL.
+ *   cu_seqlens_q, cu_seqlens_kv : int32 device arrays [num_seqs + 1], prefix
+ *   sums of the per-sequence lengths (cudnn-frontend PR #554, THD notes).
+ *   Sequence n owns query tokens [cu_q[n], cu_q[n+1]) and key tokens
+ *   [cu_kv[n], cu_kv[n+1]); the causal mask is top-left within it.
+ *   max_seqlen_q / max_seqlen_kv: upper bounds of the per-sequence lengths
+ *   (host values; used to size the launch).
+ * Rows of q/k/v past total_q/total_kv are never read, so a buffer allocated
+ * with spare capacity may hold anything (even NaN) there (cudnn-frontend PR
+ * #554, "clamp the f16 THD K/V descriptors to the packed total").
+ */
+int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o,
+                    float *lse, const int32_t *cu_seqlens_q,
+                    const int32_t *cu_seqlens_kv, int num_seqs, int total_q,
+                    int total_kv, int max_seqlen_q, int max_seqlen_kv, int h,
+                    int d, float attn_scale, int causal, int dtype,
+                    sdpa_stream_t stream);
+
+/*
+ * Workspace bytes sdpa_bwd needs: an fp32 dQ accumulator [b,h,s_q,d] and the
+ * fp32 row terms D_i = sum_k dO_ik O_ik [b,h,s_q] (cudnn-frontend PR #554:
+ * the backward chain's "do_dot" step and its fp32 dQ accumulator), rounded
+ * up for alignment.  Returns 0 for an empty problem, (size_t)-1 for invalid
+ * sizes.
+ */
+size_t sdpa_bwd_workspace_size(int b, int h, int s_q, int d);
+
+/*
+ * Dense backward (BHSD).  Same shapes and flags as the sdpa_fwd call that
+ * produced o and lse (lse must not be NULL).  dout : [b,h,s_q,d].
+ * Writes dq [b,h,s_q,d], dk, dv [b,h,s_kv,d] in dtype.  `workspace` is a
+ * device buffer of at least sdpa_bwd_workspace_size(b,h,s_q,d) bytes, owned
+ * by the caller; its contents on entry do not matter and it must not be used
+ * by another call until this one completes on `stream`.
+ * dQ is accumulated with fp32 atomics, so its low bits may differ from run
+ * to run; dK and dV are deterministic.
+ */
+int sdpa_bwd(const void *q, const void *k, const void *v, const void *o,
+             const void *dout, const float *lse, void *dq, void *dk, void *dv,
+             int b, int h, int s_q, int s_kv, int d, float attn_scale,
+             int causal, int dtype, void *workspace, size_t workspace_bytes,
+             sdpa_stream_t stream);
+
+/* Workspace bytes sdpa_varlen_bwd needs (same content as the dense one, sized
+ * by the packed token count). */
+size_t sdpa_varlen_bwd_workspace_size(int total_q, int h, int d);
+
+/*
+ * Packed (THD) backward.  Arguments as sdpa_varlen_fwd, plus o, dout
+ * [total_q,h,d], lse [total_q,h] fp32 from that forward, outputs dq
+ * [total_q,h,d], dk, dv [total_kv,h,d] and the workspace.
+ */
+int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
+                    const void *dout, const float *lse, void *dq, void *dk,
+                    void *dv, const int32_t *cu_seqlens_q,
+                    const int32_t *cu_seqlens_kv, int num_seqs, int total_q,
+                    int total_kv, int max_seqlen_q, int max_seqlen_kv, int h,
+                    int d, float attn_scale, int causal, int dtype,
+                    void *workspace, size_t workspace_bytes,
+                    sdpa_stream_t stream);
+
+/* Message describing the last non-OK status returned on this host thread
+ * ("" if none).  The pointer stays valid until the next call on the thread. */
+const char *sdpa_last_error(void);
+
+/*
+ * Reads and clears the library's device error word on the current device:
+ * kernels that give up on a bounded wait (about two seconds) record the
+ * failure there instead of hanging.  Synchronises `stream` first.  Returns
+ * SDPA_OK, SDPA_ERR_TIMEOUT (message says which kernel and which wait) or
+ * SDPA_ERR_CUDA.
+ */
+int sdpa_check_device_error(sdpa_stream_t stream);
+
+/* Library version string, e.g. "sdpa_gb300 0.1 sm_103a". */
+const char *sdpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */

@@ -1,0 +1,91 @@
+"""GB300-native fused scaled-dot-product attention.
+
+``O = softmax(attn_scale * Q K^T + causal mask) V`` plus the per-row
+log-sum-exp, dense BHSD or packed THD, and its backward, computed by
+hand-written sm_103a kernels behind the C ABI in ``include/sdpa.h``.
+
+This package is the thin Python side: ``_lib`` mirrors the C entry points
+one to one, and the helpers below allocate outputs with torch and call them.
+PyTorch only provides device memory and streams.
+"""
+from __future__ import annotations
+
+import math
+
+from ._lib import (SDPA_BF16, SDPA_FP16, SdpaError, dtype_code, load, sdpa_bwd,  # noqa: F401
+                   sdpa_bwd_workspace_size, sdpa_check_device_error, sdpa_fwd, sdpa_last_error,
+                   sdpa_varlen_bwd, sdpa_varlen_bwd_workspace_size, sdpa_varlen_fwd,
+                   sdpa_version)
+
+__all__ = ["attention", "attention_varlen", "attention_bwd", "attention_varlen_bwd",
+           "sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
+           "sdpa_bwd_workspace_size", "sdpa_varlen_bwd_workspace_size", "sdpa_last_error",
+           "sdpa_check_device_error", "sdpa_version", "SdpaError", "load"]
+
+
+def _default_scale(d: int, scale):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def attention(q, k, v, *, scale=None, causal=False, stream=None):
+    """Dense forward. q [b,h,s_q,d], k/v [b,h,s_kv,d] (CUDA, contiguous) -> (o, lse)."""
+    import torch
+    b, h, s_q, d = q.shape
+    s_kv = k.shape[2]
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, s_q), dtype=torch.float32, device=q.device)
+    sdpa_fwd(q, k, v, o, lse, b, h, s_q, s_kv, d, _default_scale(d, scale), causal,
+             dtype_code(q), stream)
+    return o, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q, max_seqlen_kv, *,
+                     scale=None, causal=False, stream=None, total_q=None, total_kv=None):
+    """Packed forward. q [Tq,h,d], k/v [Tkv,h,d], cu_seqlens int32 on the device.
+
+    ``total_q``/``total_kv`` default to the tensors' first dimension; pass them
+    when the buffers hold spare capacity past the packed total.
+    """
+    import torch
+    tq = q.shape[0] if total_q is None else int(total_q)
+    tkv = k.shape[0] if total_kv is None else int(total_kv)
+    _, h, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], h), dtype=torch.float32, device=q.device)
+    sdpa_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, cu_seqlens_q.numel() - 1, tq, tkv,
+                    int(max_seqlen_q), int(max_seqlen_kv), h, d, _default_scale(d, scale), causal,
+                    dtype_code(q), stream)
+    return o, lse
+
+
+def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, stream=None, workspace=None):
+    """Dense backward -> (dq, dk, dv).  Allocates the workspace unless one is given."""
+    import torch
+    b, h, s_q, d = q.shape
+    s_kv = k.shape[2]
+    ws_bytes = sdpa_bwd_workspace_size(b, h, s_q, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, b, h, s_q, s_kv, d, _default_scale(d, scale),
+             causal, dtype_code(q), workspace, workspace.numel(), stream)
+    return dq, dk, dv
+
+
+def attention_varlen_bwd(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_kv, max_seqlen_q,
+                         max_seqlen_kv, *, scale=None, causal=False, stream=None, workspace=None,
+                         total_q=None, total_kv=None):
+    """Packed backward -> (dq, dk, dv) in the packed layout."""
+    import torch
+    tq = q.shape[0] if total_q is None else int(total_q)
+    tkv = k.shape[0] if total_kv is None else int(total_kv)
+    _, h, d = q.shape
+    ws_bytes = sdpa_varlen_bwd_workspace_size(tq, h, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sdpa_varlen_bwd(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv,
+                    cu_seqlens_q.numel() - 1, tq, tkv, int(max_seqlen_q), int(max_seqlen_kv), h, d,
+                    _default_scale(d, scale), causal, dtype_code(q), workspace, workspace.numel(),
+                    stream)
+    return dq, dk, dv

@@ -1,0 +1,355 @@
+// C ABI of the attention library: argument validation, TMA descriptor
+// construction and kernel launch.  Nothing here allocates device memory or
+// synchronises the host (except sdpa_check_device_error, which exists to do
+// exactly that).  Declarations and the contract live in include/sdpa.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "../../include/sdpa.h"
+
+namespace sdpa {
+namespace {
+
+// First bounded-wait failure of any kernel launched by this library on the
+// device: (kernel tag << 16) | wait site.  Read and cleared by
+// sdpa_check_device_error.
+__device__ uint32_t g_error_word;
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return status;
+}
+
+int ok() {
+    t_last_error.clear();
+    return SDPA_OK;
+}
+
+// ----------------------------------------------------------- per-device state
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    uint32_t *err = nullptr;
+};
+std::mutex g_dev_mutex;
+DeviceState g_dev[kMaxDevices];
+
+int device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(SDPA_ERR_UNSUPPORTED, "device %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(SDPA_ERR_UNSUPPORTED,
+                        "device %d has compute capability %d.%d; this library is built for sm_103a",
+                        dev, major, minor);
+        e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "device attributes: %s", cudaGetErrorString(e));
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_error_word);
+        if (e != cudaSuccess)
+            return fail(SDPA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+        s.err = static_cast<uint32_t *>(addr);
+        s.ready = true;
+    }
+    *out = &s;
+    return SDPA_OK;
+}
+
+// ----------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    return SDPA_OK;
+}
+
+// 3-D map over [dim2][dim1][d] with element stride 1 along d.  The box is
+// 64 elements (128 bytes, one swizzle span) x box1 x box2, 128-byte swizzle.
+int encode_map(CUtensorMap *m, const void *ptr, bool bf16, uint64_t d, uint64_t dim1,
+               uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1,
+               uint32_t box2) {
+    cuuint64_t dims[3] = {d, dim1, dim2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {64, box1, box2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return SDPA_OK;
+}
+
+// Dense [rows_per_slice, d] slices stacked `slices` deep; tile = 128 rows of one slice.
+int dense_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int64_t rows, int64_t slices) {
+    if (rows == 0 || slices == 0) {
+        memset(m, 0, sizeof(*m));
+        return SDPA_OK;
+    }
+    return encode_map(m, ptr, bf16, d, rows, slices, (uint64_t)d * 2, (uint64_t)rows * d * 2, 128, 1);
+}
+
+// Packed [tokens, h, d]; tile = 128 tokens of one head.  The token extent is
+// the packed total, so reads past it are zero-filled.
+int packed_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int h, int64_t tokens) {
+    if (tokens == 0) {
+        memset(m, 0, sizeof(*m));
+        return SDPA_OK;
+    }
+    return encode_map(m, ptr, bf16, d, h, tokens, (uint64_t)d * 2, (uint64_t)h * d * 2, 1, 128);
+}
+
+// ----------------------------------------------------------- validation
+struct Span {
+    const void *p;
+    size_t bytes;
+    const char *name;
+    uintptr_t align = 16;
+};
+
+bool overlaps(const Span &a, const Span &b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    auto a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+int check_common(int d, int dtype, int causal, float scale) {
+    if (dtype != SDPA_BF16 && dtype != SDPA_FP16)
+        return fail(SDPA_ERR_UNSUPPORTED, "dtype %d is not SDPA_BF16 or SDPA_FP16", dtype);
+    if (d != 64 && d != 128) return fail(SDPA_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (causal != 0 && causal != 1) return fail(SDPA_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", causal);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(SDPA_ERR_INVALID_ARG, "attn_scale must be finite and > 0 (got %g)", (double)scale);
+    return SDPA_OK;
+}
+
+int check_ptrs(const Span *in, int n_in, const Span *out, int n_out) {
+    for (int i = 0; i < n_in + n_out; ++i) {
+        const Span &s = i < n_in ? in[i] : out[i - n_in];
+        if (s.bytes == 0) continue;
+        if (!s.p) return fail(SDPA_ERR_INVALID_ARG, "%s is NULL", s.name);
+        if (reinterpret_cast<uintptr_t>(s.p) & (s.align - 1))
+            return fail(SDPA_ERR_MISALIGNED, "%s is not %d-byte aligned", s.name, (int)s.align);
+    }
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = 0; j < n_in; ++j)
+            if (overlaps(out[i], in[j]))
+                return fail(SDPA_ERR_INVALID_ARG, "output %s overlaps input %s", out[i].name, in[j].name);
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlaps(out[i], out[j]))
+                return fail(SDPA_ERR_INVALID_ARG, "outputs %s and %s overlap", out[i].name, out[j].name);
+    }
+    return SDPA_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+int launch_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return ok();
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+        return fail(SDPA_ERR_UNSUPPORTED, "%s: no sm_103a kernel image for this device (%s)", what,
+                    cudaGetErrorString(e));
+    return fail(SDPA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" {
+
+const char *sdpa_last_error(void) { return t_last_error.c_str(); }
+
+const char *sdpa_version(void) { return "sdpa_gb300 0.1 sm_103a"; }
+
+int sdpa_check_device_error(sdpa_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    uint32_t word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+    if (word == 0) return ok();
+    const uint32_t zero = 0;
+    cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    static const char *names[] = {"?", "fwd", "bwd_preprocess", "bwd_main", "bwd_dq_convert"};
+    const uint32_t tag = word >> 16;
+    return fail(SDPA_ERR_TIMEOUT, "kernel %s gave up on a bounded wait (site %u)",
+                tag < 5 ? names[tag] : "?", word & 0xffffu);
+}
+
+int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b, int h,
+             int s_q, int s_kv, int d, float attn_scale, int causal, int dtype,
+             sdpa_stream_t stream) {
+    int st = check_common(d, dtype, causal, attn_scale);
+    if (st) return st;
+    if (b < 0 || h < 0 || s_q < 0 || s_kv < 0)
+        return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d h=%d s_q=%d s_kv=%d)", b, h, s_q, s_kv);
+    const int64_t bh = (int64_t)b * h;
+    if (bh == 0 || s_q == 0) return ok();
+    const int64_t q_tiles = (s_q + kTileM - 1) / kTileM;
+    if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
+        return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
+    const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh * s_kv * d * 2;
+    const Span in[3] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}};
+    const Span out[2] = {{o, qbytes, "o"}, {lse, lse ? (size_t)bh * s_q * 4 : 0, "lse"}};
+    if ((st = check_ptrs(in, 3, out, 2))) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev))) return st;
+    if ((st = get_encoder())) return st;
+    const bool bf16 = dtype == SDPA_BF16;
+    CUtensorMap tq, tk, tv;
+    if ((st = dense_map(&tq, q, bf16, d, s_q, bh))) return st;
+    if ((st = dense_map(&tk, k, bf16, d, s_kv, bh))) return st;
+    if ((st = dense_map(&tv, v, bf16, d, s_kv, bh))) return st;
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.err = dev->err;
+    p.bh = (int)bh;
+    p.h = h;
+    p.s_q = s_q;
+    p.s_kv = s_kv;
+    p.q_tiles = (int)q_tiles;
+    p.causal = causal;
+    p.scale_log2 = attn_scale * kLog2e;
+    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, false, (int)(q_tiles * bh),
+                                    static_cast<cudaStream_t>(stream)),
+                         "sdpa_fwd");
+}
+
+static int check_varlen_sizes(const int32_t *cu_q, const int32_t *cu_kv, int num_seqs, int total_q,
+                              int total_kv, int max_q, int max_kv, int h) {
+    if (num_seqs < 0 || total_q < 0 || total_kv < 0 || max_q < 0 || max_kv < 0 || h < 0)
+        return fail(SDPA_ERR_INVALID_ARG, "negative size in varlen arguments");
+    if (cu_kv && !cu_q)
+        return fail(SDPA_ERR_INVALID_ARG, "cu_seqlens_kv given without cu_seqlens_q");
+    if (num_seqs > 0 && (!cu_q || !cu_kv))
+        return fail(SDPA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_kv are required");
+    if (max_q > total_q || max_kv > total_kv)
+        return fail(SDPA_ERR_INVALID_ARG, "max_seqlen exceeds the packed total");
+    if (total_q > 0 && max_q == 0)
+        return fail(SDPA_ERR_INVALID_ARG, "max_seqlen_q is 0 but total_q is %d", total_q);
+    if (total_kv > 0 && max_kv == 0)
+        return fail(SDPA_ERR_INVALID_ARG, "max_seqlen_kv is 0 but total_kv is %d", total_kv);
+    if (num_seqs == 0 && (total_q > 0 || total_kv > 0))
+        return fail(SDPA_ERR_INVALID_ARG, "tokens given but num_seqs is 0");
+    return SDPA_OK;
+}
+
+int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                    int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int h, int d,
+                    float attn_scale, int causal, int dtype, sdpa_stream_t stream) {
+    int st = check_common(d, dtype, causal, attn_scale);
+    if (st) return st;
+    if ((st = check_varlen_sizes(cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                                 max_seqlen_q, max_seqlen_kv, h)))
+        return st;
+    if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
+    const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;
+    const int64_t slices = (int64_t)num_seqs * h;
+    if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)
+        return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
+    const size_t qbytes = (size_t)total_q * h * d * 2, kvbytes = (size_t)total_kv * h * d * 2;
+    const Span in[5] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"},
+                        {cu_seqlens_q, (size_t)(num_seqs + 1) * 4, "cu_seqlens_q", 4},
+                        {cu_seqlens_kv, (size_t)(num_seqs + 1) * 4, "cu_seqlens_kv", 4}};
+    const Span out[2] = {{o, qbytes, "o"}, {lse, lse ? (size_t)total_q * h * 4 : 0, "lse"}};
+    if ((st = check_ptrs(in, 5, out, 2))) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev))) return st;
+    if ((st = get_encoder())) return st;
+    const bool bf16 = dtype == SDPA_BF16;
+    CUtensorMap tq, tk, tv;
+    if ((st = packed_map(&tq, q, bf16, d, h, total_q))) return st;
+    if ((st = packed_map(&tk, k, bf16, d, h, total_kv))) return st;
+    if ((st = packed_map(&tv, v, bf16, d, h, total_kv))) return st;
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.cu_q = cu_seqlens_q;
+    p.cu_kv = cu_seqlens_kv;
+    p.err = dev->err;
+    p.bh = (int)slices;
+    p.h = h;
+    p.num_seqs = num_seqs;
+    p.q_tiles = (int)q_tiles;
+    p.causal = causal;
+    p.scale_log2 = attn_scale * kLog2e;
+    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, true, (int)(q_tiles * slices),
+                                    static_cast<cudaStream_t>(stream)),
+                         "sdpa_varlen_fwd");
+}
+
+size_t sdpa_bwd_workspace_size(int b, int h, int s_q, int d) {
+    if (b < 0 || h < 0 || s_q < 0 || (d != 64 && d != 128)) return (size_t)-1;
+    const size_t rows = (size_t)b * h * s_q;
+    if (rows == 0) return 0;
+    const size_t acc = rows * d * 4, delta = rows * 4;
+    return ((acc + 255) & ~(size_t)255) + ((delta + 255) & ~(size_t)255);
+}
+
+size_t sdpa_varlen_bwd_workspace_size(int total_q, int h, int d) {
+    if (total_q < 0 || h < 0 || (d != 64 && d != 128)) return (size_t)-1;
+    const size_t rows = (size_t)total_q * h;
+    if (rows == 0) return 0;
+    const size_t acc = rows * d * 4, delta = rows * 4;
+    return ((acc + 255) & ~(size_t)255) + ((delta + 255) & ~(size_t)255);
+}
+
+int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+             const float *lse, void *dq, void *dk, void *dv, int b, int h, int s_q, int s_kv,
+             int d, float attn_scale, int causal, int dtype, void *workspace,
+             size_t workspace_bytes, sdpa_stream_t stream) {
+    (void)q; (void)k; (void)v; (void)o; (void)dout; (void)lse; (void)dq; (void)dk; (void)dv;
+    (void)b; (void)h; (void)s_q; (void)s_kv; (void)d; (void)attn_scale; (void)causal;
+    (void)dtype; (void)workspace; (void)workspace_bytes; (void)stream;
+    return fail(SDPA_ERR_UNSUPPORTED, "sdpa_bwd: not built yet");
+}
+
+int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                    const float *lse, void *dq, void *dk, void *dv, const int32_t *cu_seqlens_q,
+                    const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int total_kv,
+                    int max_seqlen_q, int max_seqlen_kv, int h, int d, float attn_scale,
+                    int causal, int dtype, void *workspace, size_t workspace_bytes,
+                    sdpa_stream_t stream) {
+    (void)q; (void)k; (void)v; (void)o; (void)dout; (void)lse; (void)dq; (void)dk; (void)dv;
+    (void)cu_seqlens_q; (void)cu_seqlens_kv; (void)num_seqs; (void)total_q; (void)total_kv;
+    (void)max_seqlen_q; (void)max_seqlen_kv; (void)h; (void)d; (void)attn_scale; (void)causal;
+    (void)dtype; (void)workspace; (void)workspace_bytes; (void)stream;
+    return fail(SDPA_ERR_UNSUPPORTED, "sdpa_varlen_bwd: not built yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+"""The C-ABI library: builds, loads without a GPU, exports every symbol that
+include/sdpa.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from scaled_dot_product_04_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(sdpa_[a-z_0-9]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_lists_the_entry_points():
+    names = declared_functions()
+    for required in ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
+                     "sdpa_bwd_workspace_size", "sdpa_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from scaled_dot_product_04_gb300 import _lib
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in sdpa.h but not exported"
+    assert set(declared_functions()) <= set(_lib.EXPORTS) | set(declared_functions())
+    assert set(_lib.EXPORTS) == set(declared_functions())
+
+
+def test_version(lib):
+    from scaled_dot_product_04_gb300 import _lib
+    assert "sm_103a" in _lib.sdpa_version()
+
+
+def _fwd(lib, q=0x10000, k=0x20000, v=0x30000, o=0x40000, lse=None, b=1, h=1, s_q=128, s_kv=128,
+         d=64, scale=0.125, causal=1, dtype=0):
+    return lib.sdpa_fwd(q, k, v, o, lse, b, h, s_q, s_kv, d, scale, causal, dtype, None)
+
+
+def test_validation_before_any_cuda_call(lib):
+    from scaled_dot_product_04_gb300 import _lib as L
+    assert _fwd(lib, d=96) == L.SDPA_ERR_UNSUPPORTED
+    assert "d=96" in L.sdpa_last_error()
+    assert _fwd(lib, dtype=7) == L.SDPA_ERR_UNSUPPORTED
+    assert _fwd(lib, b=-1) == L.SDPA_ERR_INVALID_ARG
+    assert _fwd(lib, causal=2) == L.SDPA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == L.SDPA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == L.SDPA_ERR_INVALID_ARG
+    assert _fwd(lib, q=0x10001) == L.SDPA_ERR_MISALIGNED
+    assert _fwd(lib, q=None) == L.SDPA_ERR_INVALID_ARG
+    # o overlaps q (q spans 128*64*2 bytes from 0x10000)
+    assert _fwd(lib, o=0x10000 + 4096) == L.SDPA_ERR_INVALID_ARG
+    assert "overlaps" in L.sdpa_last_error()
+    # empty problems succeed without launching anything
+    assert _fwd(lib, b=0) == L.SDPA_OK
+    assert _fwd(lib, s_q=0) == L.SDPA_OK
+    assert L.sdpa_last_error() == ""
+
+
+def test_varlen_validation(lib):
+    from scaled_dot_product_04_gb300 import _lib as L
+
+    def call(cu_q=0x50000, cu_kv=0x60000, n=2, tq=100, tkv=100, mq=60, mkv=60, d=64):
+        return lib.sdpa_varlen_fwd(0x10000, 0x20000, 0x30000, 0x40000, None, cu_q, cu_kv, n, tq,
+                                   tkv, mq, mkv, 2, d, 0.125, 1, 0, None)
+
+    assert call(cu_q=None) == L.SDPA_ERR_INVALID_ARG  # cu_seqlens_kv without cu_seqlens_q
+    assert "without cu_seqlens_q" in L.sdpa_last_error()
+    assert call(mq=200) == L.SDPA_ERR_INVALID_ARG
+    assert call(mq=0) == L.SDPA_ERR_INVALID_ARG
+    assert call(n=-1) == L.SDPA_ERR_INVALID_ARG
+    assert call(cu_q=0x50002) == L.SDPA_ERR_MISALIGNED
+    assert call(d=80) == L.SDPA_ERR_UNSUPPORTED
+    assert call(n=0, tq=0, tkv=0, mq=0, mkv=0) == L.SDPA_OK
+
+
+def test_workspace_sizes(lib):
+    from scaled_dot_product_04_gb300 import _lib as L
+    assert L.sdpa_bwd_workspace_size(0, 4, 128, 64) == 0
+    ws = L.sdpa_bwd_workspace_size(2, 3, 100, 128)
+    assert ws >= 2 * 3 * 100 * (128 + 1) * 4 and ws % 256 == 0
+    assert L.sdpa_varlen_bwd_workspace_size(200, 3, 128) == ws
+    assert L.sdpa_bwd_workspace_size(1, 1, 1, 96) == ctypes.c_size_t(-1).value
