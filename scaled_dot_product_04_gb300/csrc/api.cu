@@ -329,14 +329,70 @@ size_t sdpa_varlen_bwd_workspace_size(int total_q, int h, int d) {
     return ((acc + 255) & ~(size_t)255) + ((delta + 255) & ~(size_t)255);
 }
 
+static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
 int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
              const float *lse, void *dq, void *dk, void *dv, int b, int h, int s_q, int s_kv,
              int d, float attn_scale, int causal, int dtype, void *workspace,
              size_t workspace_bytes, sdpa_stream_t stream) {
-    (void)q; (void)k; (void)v; (void)o; (void)dout; (void)lse; (void)dq; (void)dk; (void)dv;
-    (void)b; (void)h; (void)s_q; (void)s_kv; (void)d; (void)attn_scale; (void)causal;
-    (void)dtype; (void)workspace; (void)workspace_bytes; (void)stream;
-    return fail(SDPA_ERR_UNSUPPORTED, "sdpa_bwd: not built yet");
+    int st = check_common(d, dtype, causal, attn_scale);
+    if (st) return st;
+    if (b < 0 || h < 0 || s_q < 0 || s_kv < 0)
+        return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d h=%d s_q=%d s_kv=%d)", b, h, s_q, s_kv);
+    const int64_t bh = (int64_t)b * h;
+    if (bh == 0) return ok();
+    const int64_t kv_tiles = (s_kv + kTileN - 1) / kTileN;
+    if (bh > INT32_MAX || kv_tiles * bh > INT32_MAX || (int64_t)s_q * bh > INT32_MAX)
+        return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
+    const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh * s_kv * d * 2;
+    const size_t need = sdpa_bwd_workspace_size(b, h, s_q, d);
+    const Span in[6] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}, {o, qbytes, "o"},
+                        {dout, qbytes, "dout"}, {lse, (size_t)bh * s_q * 4, "lse"}};
+    const Span out[4] = {{dq, qbytes, "dq"}, {dk, kvbytes, "dk"}, {dv, kvbytes, "dv"},
+                         {workspace, need, "workspace"}};
+    if ((st = check_ptrs(in, 6, out, 4))) return st;
+    if (need > 0 && workspace_bytes < need)
+        return fail(SDPA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev))) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (s_q == 0) {
+        // no query: the key/value gradients are zero
+        if (kvbytes) {
+            cudaError_t e = cudaMemsetAsync(dk, 0, kvbytes, cs);
+            if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kvbytes, cs);
+            if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+        }
+        return ok();
+    }
+    if ((st = get_encoder())) return st;
+    const bool bf16 = dtype == SDPA_BF16;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((st = dense_map(&tq, q, bf16, d, s_q, bh))) return st;
+    if ((st = dense_map(&tk, k, bf16, d, s_kv, bh))) return st;
+    if ((st = dense_map(&tv, v, bf16, d, s_kv, bh))) return st;
+    if ((st = dense_map(&tdo, dout, bf16, d, s_q, bh))) return st;
+    BwdParams p{};
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dq_acc = static_cast<float *>(workspace);
+    p.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                        round256((size_t)bh * s_q * d * 4));
+    p.err = dev->err;
+    p.bh = (int)bh;
+    p.h = h;
+    p.s_q = s_q;
+    p.s_kv = s_kv;
+    p.kv_tiles = (int)kv_tiles;
+    p.total_q = (int)(bh * s_q);
+    p.causal = causal;
+    p.scale = attn_scale;
+    p.scale_log2 = attn_scale * kLog2e;
+    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, false, cs), "sdpa_bwd");
 }
 
 int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -345,11 +401,65 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
                     int max_seqlen_q, int max_seqlen_kv, int h, int d, float attn_scale,
                     int causal, int dtype, void *workspace, size_t workspace_bytes,
                     sdpa_stream_t stream) {
-    (void)q; (void)k; (void)v; (void)o; (void)dout; (void)lse; (void)dq; (void)dk; (void)dv;
-    (void)cu_seqlens_q; (void)cu_seqlens_kv; (void)num_seqs; (void)total_q; (void)total_kv;
-    (void)max_seqlen_q; (void)max_seqlen_kv; (void)h; (void)d; (void)attn_scale; (void)causal;
-    (void)dtype; (void)workspace; (void)workspace_bytes; (void)stream;
-    return fail(SDPA_ERR_UNSUPPORTED, "sdpa_varlen_bwd: not built yet");
+    int st = check_common(d, dtype, causal, attn_scale);
+    if (st) return st;
+    if ((st = check_varlen_sizes(cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                                 max_seqlen_q, max_seqlen_kv, h)))
+        return st;
+    if (h == 0 || num_seqs == 0 || (total_q == 0 && total_kv == 0)) return ok();
+    const int64_t kv_tiles = (max_seqlen_kv + kTileN - 1) / kTileN;
+    const int64_t slices = (int64_t)num_seqs * h;
+    if (slices > INT32_MAX || kv_tiles * slices > INT32_MAX || (int64_t)total_q * h > INT32_MAX)
+        return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
+    const size_t qbytes = (size_t)total_q * h * d * 2, kvbytes = (size_t)total_kv * h * d * 2;
+    const size_t need = sdpa_varlen_bwd_workspace_size(total_q, h, d);
+    const Span in[8] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}, {o, qbytes, "o"},
+                        {dout, qbytes, "dout"}, {lse, (size_t)total_q * h * 4, "lse"},
+                        {cu_seqlens_q, (size_t)(num_seqs + 1) * 4, "cu_seqlens_q", 4},
+                        {cu_seqlens_kv, (size_t)(num_seqs + 1) * 4, "cu_seqlens_kv", 4}};
+    const Span out[4] = {{dq, qbytes, "dq"}, {dk, kvbytes, "dk"}, {dv, kvbytes, "dv"},
+                         {workspace, need, "workspace"}};
+    if ((st = check_ptrs(in, 8, out, 4))) return st;
+    if (need > 0 && workspace_bytes < need)
+        return fail(SDPA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev))) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (total_q == 0) {
+        cudaError_t e = cudaMemsetAsync(dk, 0, kvbytes, cs);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kvbytes, cs);
+        if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+        return ok();
+    }
+    if ((st = get_encoder())) return st;
+    const bool bf16 = dtype == SDPA_BF16;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((st = packed_map(&tq, q, bf16, d, h, total_q))) return st;
+    if ((st = packed_map(&tk, k, bf16, d, h, total_kv))) return st;
+    if ((st = packed_map(&tv, v, bf16, d, h, total_kv))) return st;
+    if ((st = packed_map(&tdo, dout, bf16, d, h, total_q))) return st;
+    BwdParams p{};
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dq_acc = static_cast<float *>(workspace);
+    p.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                        round256((size_t)total_q * h * d * 4));
+    p.cu_q = cu_seqlens_q;
+    p.cu_kv = cu_seqlens_kv;
+    p.err = dev->err;
+    p.bh = (int)slices;
+    p.h = h;
+    p.num_seqs = num_seqs;
+    p.kv_tiles = (int)kv_tiles;
+    p.total_q = total_q;
+    p.causal = causal;
+    p.scale = attn_scale;
+    p.scale_log2 = attn_scale * kLog2e;
+    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, true, cs), "sdpa_varlen_bwd");
 }
 
 }  // extern "C"

@@ -1,0 +1,602 @@
+// Attention backward for sm_103a: dQ, dK, dV from dO, O and the forward's
+// LSE, recomputing P instead of storing it.
+//
+// The chain follows the backward structure cudnn-frontend PR #554 describes
+// for its SM80 kernels ("do_dot", main kernel, "dQ cast"), rebuilt for
+// tcgen05/TMEM:
+//   bwd_preprocess   D_i = sum_k dO_ik O_ik (fp32) and zeroing of the fp32 dQ
+//                    accumulator (the PR's fp32 dq accumulator);
+//   bwd_main         one CTA per (slice, 128-key tile), walking the query
+//                    tiles that can see those keys;
+//   bwd_dq_convert   fp32 accumulator -> dQ in the I/O dtype and Q's layout.
+//
+// Math per (key tile, query tile), all in the transposed orientation so the
+// key tile's rows are TMEM lanes:
+//   S^T  = K Q^T                         (tcgen05, K-major operands)
+//   P^T  = exp2(S^T * scale*log2e - LSE*log2e), masked        (registers)
+//   dP^T = V dO^T
+//   dV  += P^T dO                        (A = P^T straight from TMEM)
+//   dS^T = P^T o (dP^T - D) * scale      (bf16, written once to shared memory)
+//   dK  += dS^T Q                        (A = dS^T, K-major view)
+//   dQ_t = dS K                          (A = the same bytes, M-major view)
+//   dQacc[rows of the query tile] += dQ_t  (fp32 reductions into global memory)
+// scale is folded into dS once, so dK and dQ need no further multiply.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sdpa {
+namespace {
+
+constexpr float kLog2eF = 1.4426950408889634f;
+
+SDPA_DEV bool warp_wait_b(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
+    bool ok = mbar_wait(bar, parity, w, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// -------------------------------------------------------------------- layouts
+// Row r of a problem slice in the I/O tensors and in the fp32 buffers:
+//   dense  : I/O element offset (slice*S + r)*d, stats offset slice*S + r
+//   packed : I/O element offset ((tok0 + r)*h + head)*d, stats (tok0 + r)*h + head
+// The dQ accumulator is head-major in both cases: [slices or heads][rows][d],
+// so a query tile of one head is contiguous.
+struct RowMap {
+    int64_t io0, io_rs;      // I/O tensors (elements)
+    int64_t st0, st_rs;      // LSE / D
+    int64_t acc0;            // dQ accumulator row 0 (elements, row stride d)
+};
+
+// ------------------------------------------------------------------ preprocess
+// One warp handles 32/(d/8) rows at a time; each lane reads 8 elements of O
+// and dO with 16-byte loads.
+template <int D, bool kBf16, bool kPacked>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const BwdParams p, int64_t rows, int64_t acc_elems) {
+    constexpr int kLanesPerRow = D / 8;
+    constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+    const int64_t warp_global = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t warps_total = (gridDim.x * (int64_t)blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
+    const uint16_t *o = static_cast<const uint16_t *>(p.o);
+    const uint16_t *dout = static_cast<const uint16_t *>(p.dout);
+    for (int64_t r0 = warp_global * kRowsPerWarp; r0 < rows; r0 += warps_total * kRowsPerWarp) {
+        const int64_t r = r0 + sub;  // row in the I/O order (dense: slice*S+i, packed: t*h+head)
+        float acc = 0.f;
+        if (r < rows) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(o + r * D + part * 8);
+            const uint4 b = *reinterpret_cast<const uint4 *>(dout + r * D + part * 8);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 fa = unpack2<kBf16>(av[i]), fb = unpack2<kBf16>(bv[i]);
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
+            }
+        }
+#pragma unroll
+        for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (r < rows && part == 0) p.delta[r] = acc;  // stats layout == I/O row order
+    }
+    // zero the fp32 dQ accumulator
+    float4 *acc4 = reinterpret_cast<float4 *>(p.dq_acc);
+    const int64_t n4 = acc_elems / 4;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+         i += gridDim.x * (int64_t)blockDim.x)
+        acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------ dq convert
+template <int D, bool kBf16, bool kPacked>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BwdParams p, int64_t rows) {
+    // thread handles 8 consecutive elements of one row of dQ (I/O order)
+    constexpr int kPerRow = D / 8;
+    const int64_t total = rows * kPerRow;
+    uint16_t *dq = static_cast<uint16_t *>(p.dq);
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += gridDim.x * (int64_t)blockDim.x) {
+        const int64_t r = idx / kPerRow;
+        const int part = (int)(idx % kPerRow);
+        int64_t acc_row;
+        if constexpr (kPacked) {
+            const int64_t t = r / p.h, head = r % p.h;
+            acc_row = head * (int64_t)p.total_q + t;
+        } else {
+            acc_row = r;
+        }
+        const float4 *src = reinterpret_cast<const float4 *>(p.dq_acc + acc_row * D + part * 8);
+        const float4 a = src[0], b = src[1];
+        uint4 out;
+        out.x = pack2<kBf16>(a.x, a.y);
+        out.y = pack2<kBf16>(a.z, a.w);
+        out.z = pack2<kBf16>(b.x, b.y);
+        out.w = pack2<kBf16>(b.z, b.w);
+        *reinterpret_cast<uint4 *>(dq + r * D + part * 8) = out;
+    }
+}
+
+// ------------------------------------------------------------------ main
+template <int D>
+struct BwdLayout {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kK = 0;
+    static constexpr int kV = kK + kTileBytes;
+    static constexpr int kQ = kV + kTileBytes;               // 2 stages
+    static constexpr int kDO = kQ + 2 * kTileBytes;          // 2 stages
+    static constexpr int kDS = kDO + 2 * kTileBytes;         // 128 keys x 128 queries bf16
+    static constexpr int kStats = kDS + 2 * kChunkBytes;     // 2 stages x (lse2[128], D[128])
+    static constexpr int kBar = kStats + 2 * 2 * 128 * 4;
+    // barriers
+    static constexpr int bKVFull = 0;
+    static constexpr int bQFull = 1;       // 2
+    static constexpr int bDOFull = 3;      // 2
+    static constexpr int bStatsFull = 5;   // 2
+    static constexpr int bStageEmpty = 7;  // 2
+    static constexpr int bSFull = 9;
+    static constexpr int bDPFull = 10;
+    static constexpr int bPReady = 11;
+    static constexpr int bDSReady = 12;
+    static constexpr int bDVDone = 13;
+    static constexpr int bDQFull = 14;
+    static constexpr int bDQFree = 15;
+    static constexpr int bDSFree = 16;
+    static constexpr int bMmaIdle = 17;
+    static constexpr int kNumBars = 18;
+    static constexpr int kMisc = kBar + kNumBars * 8;
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColDV = 0;
+    static constexpr uint32_t kColDK = D;
+    static constexpr uint32_t kColS = 2 * D;
+    static constexpr uint32_t kColDP = 2 * D + 128;
+    static constexpr bool kDQAliasDP = (D == 128);  // no spare columns at d = 128
+    static constexpr uint32_t kColDQ = kDQAliasDP ? kColDP : 2 * D + 256;
+};
+
+constexpr int kBwdThreads = 320;  // warps: 0 TMA, 1 MMA, 2-5 compute, 6-9 dQ epilogue
+
+template <int D, bool kBf16, bool kPacked>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = smem_u32(smem);
+
+    // ---------------------------------------------------------------- work unit
+    // Key tiles in ascending order: under the causal mask the first key tiles
+    // see the most query tiles, so the heaviest units start first.
+    const int kt = blockIdx.x / p.bh;
+    const int slice = blockIdx.x % p.bh;
+    int Lq, Lkv, tok_q0 = 0, tok_kv0 = 0, head = 0;
+    RowMap qm, km;
+    if constexpr (!kPacked) {
+        Lq = p.s_q;
+        Lkv = p.s_kv;
+        qm = {(int64_t)slice * p.s_q * D, D, (int64_t)slice * p.s_q, 1, (int64_t)slice * p.s_q * D};
+        km = {(int64_t)slice * p.s_kv * D, D, 0, 0, 0};
+    } else {
+        const int n = slice / p.h;
+        head = slice % p.h;
+        tok_q0 = p.cu_q[n];
+        tok_kv0 = p.cu_kv[n];
+        Lq = p.cu_q[n + 1] - tok_q0;
+        Lkv = p.cu_kv[n + 1] - tok_kv0;
+        qm = {((int64_t)tok_q0 * p.h + head) * D, (int64_t)p.h * D, (int64_t)tok_q0 * p.h + head,
+              p.h, ((int64_t)head * p.total_q + tok_q0) * D};
+        km = {((int64_t)tok_kv0 * p.h + head) * D, (int64_t)p.h * D, 0, 0, 0};
+    }
+    const int k0 = kt * kTileN;
+    if (k0 >= Lkv) return;  // packed: this sequence has fewer key tiles
+    const int q_tiles = (Lq + kTileM - 1) / kTileM;
+    const int qt_begin = p.causal ? k0 / kTileM : 0;
+    const int n_q = max(0, q_tiles - qt_begin);
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+
+    if (n_q == 0) {
+        // No query sees these keys: dK = dV = 0.
+        if (threadIdx.x < kTileN) {
+            const int j = k0 + threadIdx.x;
+            if (j < Lkv) {
+                uint4 *a = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.dk) + km.io0 + j * km.io_rs);
+                uint4 *b = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.dv) + km.io0 + j * km.io_rs);
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) a[i] = b[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    if ((sbase & 1023u) != 0) {
+        // The swizzled operand tiles need a 1024-byte aligned base.
+        if (threadIdx.x == 0) atomicCAS(p.err, 0u, (kTagBwdMain << 16) | 0xfffu);
+        return;
+    }
+    auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+    float *stats = reinterpret_cast<float *>(smem + L::kStats);  // [stage][2][128]
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::bKVFull), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(L::bQFull + s), 1);
+            mbar_init(bar(L::bDOFull + s), 1);
+            mbar_init(bar(L::bStatsFull + s), 32);
+            mbar_init(bar(L::bStageEmpty + s), 1);
+        }
+        mbar_init(bar(L::bSFull), 1);
+        mbar_init(bar(L::bDPFull), 1);
+        mbar_init(bar(L::bPReady), 128);
+        mbar_init(bar(L::bDSReady), 128);
+        mbar_init(bar(L::bDVDone), 1);
+        mbar_init(bar(L::bDQFull), 1);
+        mbar_init(bar(L::bDQFree), 128);
+        mbar_init(bar(L::bDSFree), 1);
+        mbar_init(bar(L::bMmaIdle), 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::kMisc, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const WaitCtx wc{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.err, kTagBwdMain};
+
+    if (warp == 0) {
+        // ============================================================ producer
+        const int ky = kPacked ? head : k0;
+        const int kz = kPacked ? tok_kv0 + k0 : slice;
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            mbar_arrive_expect_tx(bar(L::bKVFull), 2 * L::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c) {
+                tma_load_3d(sbase + L::kK + c * L::kChunkBytes, &tm_k, bar(L::bKVFull), c * 64, ky, kz);
+                tma_load_3d(sbase + L::kV + c * L::kChunkBytes, &tm_v, bar(L::bKVFull), c * 64, ky, kz);
+            }
+        }
+        int issued = 0;
+        for (int i = 0; i < n_q; ++i) {
+            const int st = i & 1, use = i >> 1;
+            if (use > 0 && !warp_wait_b(bar(L::bStageEmpty + st), (use - 1) & 1, wc, 1)) break;
+            const int q0 = (qt_begin + i) * kTileM;
+            if (lane == 0) {
+                const int qy = kPacked ? head : q0;
+                const int qz = kPacked ? tok_q0 + q0 : slice;
+                mbar_arrive_expect_tx(bar(L::bQFull + st), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(sbase + L::kQ + st * L::kTileBytes + c * L::kChunkBytes, &tm_q,
+                                bar(L::bQFull + st), c * 64, qy, qz);
+                mbar_arrive_expect_tx(bar(L::bDOFull + st), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(sbase + L::kDO + st * L::kTileBytes + c * L::kChunkBytes, &tm_do,
+                                bar(L::bDOFull + st), c * 64, qy, qz);
+            }
+            // Row statistics of the query tile: LSE*log2(e) and D.  Rows past
+            // the sequence get +inf / 0 so their P (and so dS) is exactly 0.
+            float *lse2 = stats + st * 256;
+            float *dd = lse2 + 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = u * 32 + lane;
+                const int q = q0 + r;
+                float a = INFINITY, b = 0.f;
+                if (q < Lq) {
+                    const int64_t idx = qm.st0 + (int64_t)q * qm.st_rs;
+                    a = p.lse[idx] * kLog2eF;
+                    b = p.delta[idx];
+                }
+                lse2[r] = a;
+                dd[r] = b;
+            }
+            mbar_arrive(bar(L::bStatsFull + st));
+            issued = i + 1;
+        }
+        if (lane == 0) {
+            mbar_wait_drain(bar(L::bKVFull), 0);
+            for (int i = max(0, issued - 2); i < issued; ++i) {
+                mbar_wait_drain(bar(L::bQFull + (i & 1)), (i >> 1) & 1);
+                mbar_wait_drain(bar(L::bDOFull + (i & 1)), (i >> 1) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_sq = make_idesc_f16(128, 128, kBf16, false, false);
+            constexpr uint32_t id_mn = make_idesc_f16(128, D, kBf16, false, true);
+            constexpr uint32_t id_dq = make_idesc_f16(128, D, kBf16, true, true);
+            const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
+            // X^T = A B^T over the head dim (both K-major), 128 x 128
+            auto issue_kmajor = [&](uint32_t a_s, uint32_t b_s, uint32_t col) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
+                    mma_ss(tmem + col, smem_desc_sw128(a_s + off, 16, 1024),
+                           smem_desc_sw128(b_s + off, 16, 1024), id_sq, k > 0);
+                }
+            };
+            bool ok = mbar_wait(bar(L::bKVFull), 0, wc, 2) && mbar_wait(bar(L::bQFull), 0, wc, 3);
+            if (ok) {
+                tc_fence_after();
+                issue_kmajor(sK, sbase + L::kQ, L::kColS);  // S^T_0
+                mma_commit(bar(L::bSFull));
+                ok = mbar_wait(bar(L::bDOFull), 0, wc, 4);
+            }
+            if (ok) {
+                tc_fence_after();
+                issue_kmajor(sV, sbase + L::kDO, L::kColDP);  // dP^T_0
+                mma_commit(bar(L::bDPFull));
+            }
+            for (int i = 0; ok && i < n_q; ++i) {
+                const int st = i & 1;
+                const uint32_t sQ = sbase + L::kQ + st * L::kTileBytes;
+                const uint32_t sDO = sbase + L::kDO + st * L::kTileBytes;
+                // dV += P^T dO  (P^T bf16 in the S columns)
+                ok = mbar_wait(bar(L::bPReady), i & 1, wc, 5);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k)
+                    mma_ts(tmem + L::kColDV, tmem + L::kColS + k * 8,
+                           smem_desc_sw128(sDO + k * 2048, L::kChunkBytes, 1024), id_mn,
+                           (i > 0 || k > 0) ? 1u : 0u);
+                mma_commit(bar(L::bDVDone));
+                // S^T_{i+1}, once the dV product has finished reading P^T_i
+                if (i + 1 < n_q) {
+                    const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
+                    ok = mbar_wait(bar(L::bQFull + st1), use1 & 1, wc, 6) &&
+                         mbar_wait(bar(L::bDVDone), i & 1, wc, 7);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_kmajor(sK, sbase + L::kQ + st1 * L::kTileBytes, L::kColS);
+                    mma_commit(bar(L::bSFull));
+                }
+                // dK += dS^T Q ; dQ_i = dS K
+                ok = mbar_wait(bar(L::bDSReady), i & 1, wc, 8);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k) {
+                    const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
+                    mma_ss(tmem + L::kColDK, smem_desc_sw128(sDS + off, 16, 1024),
+                           smem_desc_sw128(sQ + k * 2048, L::kChunkBytes, 1024), id_mn,
+                           (i > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(L::bStageEmpty + st));
+                if (!L::kDQAliasDP && i > 0) {
+                    ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k)
+                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
+                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
+                mma_commit(bar(L::bDQFull));
+                mma_commit(bar(L::bDSFree));
+                // dP^T_{i+1}
+                if (i + 1 < n_q) {
+                    const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
+                    ok = mbar_wait(bar(L::bDOFull + st1), use1 & 1, wc, 10);
+                    if (ok && L::kDQAliasDP) ok = mbar_wait(bar(L::bDQFree), i & 1, wc, 11);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_kmajor(sV, sbase + L::kDO + st1 * L::kTileBytes, L::kColDP);
+                    mma_commit(bar(L::bDPFull));
+                }
+            }
+            mma_commit(bar(L::bMmaIdle));
+            mbar_wait_drain(bar(L::bMmaIdle), 0);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ============================================================ compute
+        const int quad = warp & 3;
+        const int j = quad * 32 + lane;  // key row of the tile == TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+        const int key = k0 + j;
+        const bool key_ok = key < Lkv;
+        const float sl2 = p.scale_log2;
+        const float scale = p.scale;
+        uint8_t *ds_row = smem + L::kDS + j * 128;
+        bool ok = true;
+        for (int i = 0; i < n_q; ++i) {
+            const int st = i & 1;
+            const int q0 = (qt_begin + i) * kTileM;
+            const float *lse2 = stats + st * 256;
+            const float *dd = lse2 + 128;
+            ok = warp_wait_b(bar(L::bSFull), i & 1, wc, 12) &&
+                 warp_wait_b(bar(L::bStatsFull + st), (i >> 1) & 1, wc, 13);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + L::kColS + c * 32, s + c * 32);
+            tmem_ld_wait_regs<128>(s);
+            // visible iff key < Lkv and (not causal or query >= key); query rows
+            // past Lq carry lse2 = +inf and vanish on their own.
+            int lo = 0;  // first visible column
+            if (p.causal) lo = key - q0;
+            if (!key_ok) lo = 128;
+            // P^T in place of S^T, then packed to bf16/fp16 pairs in s[0..64):
+            // the packed copy feeds both the dV product (via TMEM) and dS.
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x = fmaf(__uint_as_float(s[c + e]), sl2, -lv[e]);
+                    s[c + e] = __float_as_uint((c + e >= lo) ? ex2_approx(x) : 0.f);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                s[c] = pack2<kBf16>(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+            tmem_st32(t_lane + L::kColS, s);
+            tmem_st32(t_lane + L::kColS + 32, s + 32);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(L::bPReady));
+
+            // dS^T = P^T o (dP^T - D) * scale  ->  shared memory (bf16, SW128)
+            ok = warp_wait_b(bar(L::bDPFull), i & 1, wc, 14);
+            if (ok && i > 0) ok = warp_wait_b(bar(L::bDSFree), (i - 1) & 1, wc, 15);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t dp[32];
+                tmem_ld32(t_lane + L::kColDP + c * 32, dp);
+                tmem_ld_wait_regs<32>(dp);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dd + c * 32 + e);
+                    const float2 p01 = unpack2<kBf16>(s[(c * 32 + e) / 2]);
+                    const float2 p23 = unpack2<kBf16>(s[(c * 32 + e) / 2 + 1]);
+                    const float g0 = p01.x * (__uint_as_float(dp[e]) - d4.x) * scale;
+                    const float g1 = p01.y * (__uint_as_float(dp[e + 1]) - d4.y) * scale;
+                    const float g2 = p23.x * (__uint_as_float(dp[e + 2]) - d4.z) * scale;
+                    const float g3 = p23.y * (__uint_as_float(dp[e + 3]) - d4.w) * scale;
+                    w[e / 2] = pack2<kBf16>(g0, g1);
+                    w[e / 2 + 1] = pack2<kBf16>(g2, g3);
+                }
+                // queries [32c, 32c+32): 128-byte chunk c/2, 16-byte units (c%2)*4 .. +3
+                uint8_t *chunk = ds_row + (c >> 1) * L::kChunkBytes;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int unit = (c & 1) * 4 + u;
+                    *reinterpret_cast<uint4 *>(chunk + ((unit ^ (j & 7)) << 4)) =
+                        make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(L::bDSReady));
+        }
+        // dK, dV epilogue
+        if (ok) ok = warp_wait_b(bar(L::bMmaIdle), 0, wc, 16);
+        if (ok) {
+            tc_fence_after();
+            uint16_t *dv_row = static_cast<uint16_t *>(p.dv) + km.io0 + (int64_t)key * km.io_rs;
+            uint16_t *dk_row = static_cast<uint16_t *>(p.dk) + km.io0 + (int64_t)key * km.io_rs;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
+                uint16_t *dst_row = which == 0 ? dv_row : dk_row;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_lane + col + c * 32, r);
+                    tmem_ld_wait_regs<32>(r);
+                    if (key_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(
+                                pack2<kBf16>(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
+                                pack2<kBf16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                pack2<kBf16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                pack2<kBf16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+                    }
+                }
+            }
+        }
+    } else {
+        // ============================================================ dQ epilogue
+        const int quad = warp & 3;
+        const int qr = quad * 32 + lane;  // query row of the tile == TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+        for (int i = 0; i < n_q; ++i) {
+            if (!warp_wait_b(bar(L::bDQFull), i & 1, wc, 17)) break;
+            tc_fence_after();
+            uint32_t r[D];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(t_lane + L::kColDQ + c * 32, r + c * 32);
+            tmem_ld_wait_regs<D>(r);
+            tc_fence_before();
+            mbar_arrive(bar(L::bDQFree));
+            const int q = (qt_begin + i) * kTileM + qr;
+            if (q < Lq) {
+                float *dst = p.dq_acc + qm.acc0 + (int64_t)q * D;
+#pragma unroll
+                for (int c = 0; c < D; c += 4) {
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c),
+                                 "f"(__uint_as_float(r[c])), "f"(__uint_as_float(r[c + 1])),
+                                 "f"(__uint_as_float(r[c + 2])), "f"(__uint_as_float(r[c + 3]))
+                                 : "memory");
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+template <int D, bool kBf16, bool kPacked>
+cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream) {
+    using L = BwdLayout<D>;
+    const int64_t rows = kPacked ? (int64_t)p.total_q * p.h : (int64_t)p.bh * p.s_q;
+    const int64_t acc_elems = rows * D;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int small_grid = sms * 8;
+    bwd_preprocess_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(p, rows, acc_elems);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = bwd_main_kernel<D, kBf16, kPacked>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p.kv_tiles * p.bh;
+    kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dq_convert_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(p, rows);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, const BwdParams &p, int d, bool bf16, bool packed,
+                       cudaStream_t stream) {
+#define SDPA_BWD_CASE(D_, BF_, PK_)                                            \
+    if (d == D_ && bf16 == BF_ && packed == PK_)                               \
+        return launch_bwd_t<D_, BF_, PK_>(tq, tk, tv, tdo, p, stream);
+    SDPA_BWD_CASE(64, true, false)
+    SDPA_BWD_CASE(64, true, true)
+    SDPA_BWD_CASE(64, false, false)
+    SDPA_BWD_CASE(64, false, true)
+    SDPA_BWD_CASE(128, true, false)
+    SDPA_BWD_CASE(128, true, true)
+    SDPA_BWD_CASE(128, false, false)
+    SDPA_BWD_CASE(128, false, true)
+#undef SDPA_BWD_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sdpa
