@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the fused attention hot path on GB300.
+
+One step = one full pass of the path over the long-context causal workload
+(b=1, h=32, s=16384, d=128, bf16, Q and K scaled by 2): the forward kernel
+(O and LSE) followed by the backward chain (preprocess, main, dQ convert)
+that produces dQ, dK, dV.  FLOPs per step follow the pages' count
+4*b*h*s*s*d*0.5 for the causal forward ("Inside NVIDIA's cuDNN Graph API",
+section 5) and 2.5x that for the backward (five s x s x d products against
+the forward's two), 3.5x in total.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints one JSON line on rank 0.  For N > 1 each rank runs an independent
+replica of the workload on its own GPU (the path has no cross-GPU exchange),
+so the scaling is weak; the time is the maximum over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on
+a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SDPA fwd/bwd TFLOP/s (causal-halved FLOPs), % of GB300 BF16 tensor peak"
+WORKLOAD = "c5_b1h32s16384d128_causal_qk2"
+BWD_FACTOR = 2.5          # backward FLOPs per forward FLOP
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+REF_PREFIX = 2048         # tokens of one head per oracle sample
+
+# DRAM bytes per launch of the dominant kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel and the
+# library version the capture was taken with.  None until captured.
+TRAFFIC = {}
+
+
+def fwd_flops(w) -> float:
+    return 4.0 * w.b * w.h * w.s * w.s * w.d * (0.5 if w.causal else 1.0)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="dense workload name from sdpa_inputs.WORKLOADS (profiling runs); the "
+                         "reported metric is quoted on the default")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle CPU-baseline leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms during the timed region."""
+
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.5)  # let the first samples arrive before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 10:
+                continue
+            if self.uuid and parts[1] != self.uuid:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({name for r in inside for name, v in zip(self.REASONS, r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------- oracle legs
+def oracle_sample_rate(w, t, min_s: float, max_s: float, heads=None):
+    """Time the fp64 oracle (fwd + bwd) on causal prefixes of single heads.
+
+    Each sample is head h of the workload's own inputs cut to its first
+    REF_PREFIX tokens, a self-contained causal problem with the same
+    arithmetic per score.  Returns (TFLOP/s, seconds, samples, threads).
+    """
+    import oracle
+    L = min(REF_PREFIX, w.s)
+    flops = 4.0 * L * L * w.d * 0.5 * (1.0 + BWD_FACTOR)
+    done, spent, h = 0, 0.0, 0
+    order = heads if heads is not None else range(10 ** 9)
+    for h in order:
+        hh = h % w.h
+        q = t["q"][0:1, hh:hh + 1, :L]
+        k = t["k"][0:1, hh:hh + 1, :L]
+        v = t["v"][0:1, hh:hh + 1, :L]
+        do = t["do"][0:1, hh:hh + 1, :L]
+        t0 = time.perf_counter()
+        oracle.sdpa_fwd(q, k, v, w.scale, w.causal)
+        oracle.sdpa_bwd(q, k, v, do, w.scale, w.causal)
+        spent += time.perf_counter() - t0
+        done += 1
+        if heads is None and (spent >= min_s or spent + spent / done > max_s):
+            break
+    return flops * done / spent / 1e12, spent, done, oracle.num_threads()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import sdpa_inputs
+    import oracle
+    oracle.build()
+    w = sdpa_inputs.WORKLOADS[args.workload]
+    t = sdpa_inputs.make(w)
+    oracle_sample_rate(w, t, 0, 0, heads=range(args.warmup))
+    rate, spent, n, threads = oracle_sample_rate(w, t, 0, 0, heads=range(args.steps))
+    L = min(REF_PREFIX, w.s)
+    sample = (f"per step: one head of {w.name} (heads in turn) cut to its first {L} tokens, "
+              f"causal fp64 forward + backward")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": spent / n * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample_prefix_tokens": L},
+        "cpu_baseline": {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import sdpa_inputs
+    import scaled_dot_product_04_gb300 as sdpa
+    sdpa.load()
+
+    w = sdpa_inputs.WORKLOADS[args.workload]
+    if w.layout != "bhsd":
+        raise SystemExit(f"bench.py times dense workloads; {w.name} is packed")
+    t = sdpa_inputs.make(w)
+    b, h, s, d = w.b, w.h, w.s, w.d
+    scale, causal = w.scale, int(w.causal)
+    q, k, v, do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((b, h, s), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(sdpa.sdpa_bwd_workspace_size(b, h, s, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    f_fwd = fwd_flops(w)
+    f_step = f_fwd * (1.0 + BWD_FACTOR)
+
+    def step(ev_f=None, ev_b=None):
+        if ev_f:
+            sdpa.sdpa_set_kernel_timer(*ev_f)
+        sdpa.sdpa_fwd(q, k, v, o, lse, b, h, s, s, d, scale, causal, 0, stream)
+        if ev_b:
+            sdpa.sdpa_set_kernel_timer(*ev_b)
+        sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, b, h, s, s, d, scale, causal, 0, ws,
+                      ws.numel(), stream)
+        sdpa.sdpa_set_kernel_timer(None, None)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    sdpa.sdpa_check_device_error(stream)
+
+    def new_ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    ev = [(new_ev(), new_ev(), (new_ev(), new_ev()), (new_ev(), new_ev()))
+          for _ in range(args.steps)]
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flush between steps, outside the events
+        ev[i][0].record(stream)
+        step(ev[i][2], ev[i][3])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    sdpa.sdpa_check_device_error(stream)
+
+    step_ms = [a.elapsed_time(bb) for a, bb, _, _ in ev]
+    fwd_ms = [f[0].elapsed_time(f[1]) for _, _, f, _ in ev]
+    bwd_ms = [g[0].elapsed_time(g[1]) for _, _, _, g in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    value = world * f_step * args.steps / (total_ms * 1e-3) / 1e12
+    clocks = sampler.summary(t0, t1)
+
+    # ------------------------------------------------------------ end to end
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t[x].pin_memory() for x in ("q", "k", "v", "do"))
+        ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+                             for x in (o, dq, dk, dv))
+        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            step()
+            for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 10))
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        a, z = new_ev(), new_ev()
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        z.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(z) / n_e2e
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+        d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+        e2e = {"value": world * f_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    # ------------------------------------------------------------ roofline
+    peaks, peak_src = read_peaks()
+    mean_f, mean_b = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    kern = "bwd_main" if sum(bwd_ms) >= sum(fwd_ms) else "fwd"
+    k_flops = f_fwd * BWD_FACTOR if kern == "bwd_main" else f_fwd
+    k_ms = mean_b if kern == "bwd_main" else mean_f
+    achieved = k_flops / (k_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops_sustained"])
+    version = sdpa.sdpa_version()
+    tr = TRAFFIC.get((kern, version))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": tr, "kernel": kern,
+                "peak_source": f"{peak_src} sustained bf16 (MEASURED_PEAKS.json)"
+                if peak_src == "measured" else "fallback sustained bf16"}
+    burst = float(peaks["bf16_tflops"])
+    phases = {
+        "fwd_kernel": {"ms": mean_f, "tflops": f_fwd / (mean_f * 1e-3) / 1e12,
+                       "frac_sustained": f_fwd / (mean_f * 1e-3) / 1e12 / peak,
+                       "frac_burst": f_fwd / (mean_f * 1e-3) / 1e12 / burst},
+        "bwd_main_kernel": {"ms": mean_b,
+                            "tflops": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12,
+                            "frac_sustained": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12 / peak,
+                            "frac_burst": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12 / burst},
+        "bwd_pre_and_convert_ms": statistics.mean(
+            sm - fm - bm for sm, fm, bm in zip(step_ms, fwd_ms, bwd_ms)),
+    }
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, spent, n, threads = oracle_sample_rate(w, t, min_s=10.0, max_s=30.0)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} heads of {w.name}, each cut to its first "
+                         f"{min(REF_PREFIX, w.s)} tokens, causal fp64 fwd + bwd, {spent:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16" + (", Q and K x2)" if w.qk_mult != 1 else ")"),
+            "config": {"workload": w.name, "b": b, "h": h, "s_q": s, "s_kv": s, "d": d,
+                       "causal": bool(causal), "layout": "bhsd",
+                       "step": "fwd (O, LSE) + bwd (dQ, dK, dV)",
+                       "flops_per_step": f_step, "pct_of_peak": 100.0 * value / world / peak,
+                       "l2": "a 512 MiB buffer (> L2) is written between timed steps; "
+                             "inputs+outputs total %d MiB" % ((4 * q.numel() + 2 * k.numel() * 2)
+                                                              * 2 >> 20),
+                       "parallelism": f"replicas x{world}"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": 4 * args.steps,
+            "roofline": roofline, "phases": phases, "cpu_baseline": cpu,
+            "library": version,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -162,6 +162,17 @@ const char *sdpa_last_error(void);
  */
 int sdpa_check_device_error(sdpa_stream_t stream);
 
+/*
+ * Measurement hook (no counterpart on the pages).  While both events are
+ * non-NULL, every later call on this host thread records `start_event` on
+ * its stream immediately before launching its main kernel (the forward
+ * kernel, or the backward's main kernel) and `stop_event` immediately after,
+ * so a caller can time that kernel alone with cudaEventElapsedTime.  The
+ * events are cudaEvent_t handles owned by the caller; pass NULL, NULL to
+ * stop.  Recording adds no synchronisation.
+ */
+void sdpa_set_kernel_timer(void *start_event, void *stop_event);
+
 /* Library version string, e.g. "sdpa_gb300 0.1 sm_103a". */
 const char *sdpa_version(void);
 

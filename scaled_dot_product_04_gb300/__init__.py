@@ -14,13 +14,14 @@ import math
 
 from ._lib import (SDPA_BF16, SDPA_FP16, SdpaError, dtype_code, load, sdpa_bwd,  # noqa: F401
                    sdpa_bwd_workspace_size, sdpa_check_device_error, sdpa_fwd, sdpa_last_error,
-                   sdpa_varlen_bwd, sdpa_varlen_bwd_workspace_size, sdpa_varlen_fwd,
-                   sdpa_version)
+                   sdpa_set_kernel_timer, sdpa_varlen_bwd, sdpa_varlen_bwd_workspace_size,
+                   sdpa_varlen_fwd, sdpa_version)
 
 __all__ = ["attention", "attention_varlen", "attention_bwd", "attention_varlen_bwd",
            "sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
            "sdpa_bwd_workspace_size", "sdpa_varlen_bwd_workspace_size", "sdpa_last_error",
-           "sdpa_check_device_error", "sdpa_version", "SdpaError", "load"]
+           "sdpa_check_device_error", "sdpa_set_kernel_timer", "sdpa_version", "SdpaError",
+           "load"]
 
 
 def _default_scale(d: int, scale):

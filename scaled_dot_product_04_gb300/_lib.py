@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
 # Exported symbols, in the order include/sdpa.h declares them.
 EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd",
            "sdpa_varlen_bwd_workspace_size", "sdpa_varlen_bwd", "sdpa_last_error",
-           "sdpa_check_device_error", "sdpa_version")
+           "sdpa_check_device_error", "sdpa_set_kernel_timer", "sdpa_version")
 
 
 class SdpaError(RuntimeError):
@@ -77,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sdpa_last_error.restype = ctypes.c_char_p
         lib.sdpa_check_device_error.argtypes = [_P]
         lib.sdpa_version.restype = ctypes.c_char_p
+        lib.sdpa_set_kernel_timer.argtypes = [_P, _P]
+        lib.sdpa_set_kernel_timer.restype = None
         for name in ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
                      "sdpa_check_device_error"):
             getattr(lib, name).restype = _I
@@ -160,6 +162,17 @@ def sdpa_last_error() -> str:
 
 def sdpa_check_device_error(stream=None) -> None:
     _check(load().sdpa_check_device_error(_stream(stream)))
+
+
+def sdpa_set_kernel_timer(start_event=None, stop_event=None) -> None:
+    """Record torch.cuda.Event pairs around the main kernel of later calls on this thread."""
+    def handle(ev):
+        if ev is None:
+            return None
+        if not ev.cuda_event:  # torch creates the CUDA event lazily
+            ev.record()
+        return ev.cuda_event
+    load().sdpa_set_kernel_timer(handle(start_event), handle(stop_event))
 
 
 def sdpa_version() -> str:

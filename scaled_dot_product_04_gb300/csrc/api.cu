@@ -23,6 +23,7 @@ namespace {
 __device__ uint32_t g_error_word;
 
 thread_local std::string t_last_error;
+thread_local KernelTimer t_timer;
 
 int fail(int status, const char *fmt, ...) {
     char buf[512];
@@ -194,6 +195,12 @@ const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
 const char *sdpa_version(void) { return "sdpa_gb300 0.1 sm_103a"; }
 
+void sdpa_set_kernel_timer(void *start_event, void *stop_event) {
+    t_timer.start = static_cast<cudaEvent_t>(start_event);
+    t_timer.stop = static_cast<cudaEvent_t>(stop_event);
+    if (!t_timer.start || !t_timer.stop) t_timer = KernelTimer{};
+}
+
 int sdpa_check_device_error(sdpa_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
@@ -245,7 +252,7 @@ int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     p.causal = causal;
     p.scale_log2 = attn_scale * kLog2e;
     return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, false, (int)(q_tiles * bh),
-                                    static_cast<cudaStream_t>(stream)),
+                                    static_cast<cudaStream_t>(stream), t_timer),
                          "sdpa_fwd");
 }
 
@@ -309,7 +316,7 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
     p.causal = causal;
     p.scale_log2 = attn_scale * kLog2e;
     return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, true, (int)(q_tiles * slices),
-                                    static_cast<cudaStream_t>(stream)),
+                                    static_cast<cudaStream_t>(stream), t_timer),
                          "sdpa_varlen_fwd");
 }
 
@@ -392,7 +399,7 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     p.causal = causal;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, false, cs), "sdpa_bwd");
+    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
 }
 
 int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -459,7 +466,7 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     p.causal = causal;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, true, cs), "sdpa_varlen_bwd");
+    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
 }
 
 }  // extern "C"

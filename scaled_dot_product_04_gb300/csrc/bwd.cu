@@ -557,7 +557,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool kBf16, bool kPacked>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream) {
+                         const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream,
+                         const KernelTimer &timer) {
     using L = BwdLayout<D>;
     const int64_t rows = kPacked ? (int64_t)p.total_q * p.h : (int64_t)p.bh * p.s_q;
     const int64_t acc_elems = rows * D;
@@ -572,8 +573,10 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.kv_tiles * p.bh;
+    if (timer.start) cudaEventRecord(timer.start, stream);
     kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, p);
     e = cudaGetLastError();
+    if (timer.stop) cudaEventRecord(timer.stop, stream);
     if (e != cudaSuccess) return e;
     bwd_dq_convert_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(p, rows);
     return cudaGetLastError();
@@ -583,10 +586,10 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdParams &p, int d, bool bf16, bool packed,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const KernelTimer &timer) {
 #define SDPA_BWD_CASE(D_, BF_, PK_)                                            \
     if (d == D_ && bf16 == BF_ && packed == PK_)                               \
-        return launch_bwd_t<D_, BF_, PK_>(tq, tk, tv, tdo, p, stream);
+        return launch_bwd_t<D_, BF_, PK_>(tq, tk, tv, tdo, p, stream, timer);
     SDPA_BWD_CASE(64, true, false)
     SDPA_BWD_CASE(64, true, true)
     SDPA_BWD_CASE(64, false, false)

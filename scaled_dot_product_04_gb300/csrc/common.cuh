@@ -56,11 +56,17 @@ struct BwdParams {
 };
 
 // Host launchers (one translation unit each).
+// Optional measurement events recorded on `stream` right before and right
+// after the main kernel of a call (both null = none).
+struct KernelTimer {
+    cudaEvent_t start = nullptr, stop = nullptr;
+};
+
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
-                       cudaStream_t stream);
+                       cudaStream_t stream, const KernelTimer &timer);
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdParams &p, int d, bool bf16, bool packed,
-                       cudaStream_t stream);
+                       cudaStream_t stream, const KernelTimer &timer);
 
 }  // namespace sdpa

@@ -375,24 +375,28 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int D, bool kBf16, bool kPacked>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const FwdParams &p, int grid, cudaStream_t stream) {
+                         const FwdParams &p, int grid, cudaStream_t stream,
+                         const KernelTimer &timer) {
     using L = FwdLayout<D>;
     auto kern = fwd_kernel<D, kBf16, kPacked>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);
     if (e != cudaSuccess) return e;
+    if (timer.start) cudaEventRecord(timer.start, stream);
     kern<<<grid, 192, L::kSmemAlloc, stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (timer.stop) cudaEventRecord(timer.stop, stream);
+    return e;
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const KernelTimer &timer) {
 #define SDPA_FWD_CASE(D_, BF_, PK_)                                            \
     if (d == D_ && bf16 == BF_ && packed == PK_)                               \
-        return launch_fwd_t<D_, BF_, PK_>(tq, tk, tv, p, grid, stream);
+        return launch_fwd_t<D_, BF_, PK_>(tq, tk, tv, p, grid, stream, timer);
     SDPA_FWD_CASE(64, true, false)
     SDPA_FWD_CASE(64, true, true)
     SDPA_FWD_CASE(64, false, false)
