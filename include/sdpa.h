@@ -149,6 +149,38 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
                     void *workspace, size_t workspace_bytes,
                     sdpa_stream_t stream);
 
+/*
+ * Dense backward that allocates nothing and takes no workspace (the pages
+ * have no counterpart of this entry point).
+ *
+ * For callers that cannot allocate device memory themselves: plug-in or
+ * callback code running inside another runtime that owns every device
+ * allocation and hands out no workspace, or a latency-critical loop where a
+ * cudaMalloc, which may synchronise the device, is not allowed.  Arguments
+ * and results are those of sdpa_bwd without workspace/workspace_bytes; the
+ * caller still passes every input and output buffer.
+ *
+ * The scratch that sdpa_bwd keeps in its workspace comes instead from a
+ * 32 MiB array inside the library's device image, which every GPU that
+ * loads the library holds until the process exits.  Problems whose
+ * sdpa_bwd_workspace_size exceeds 32 MiB (about b*h*s_q*(d+1)*4 bytes: up
+ * to 65,027 rows of b*h*s_q at d = 128) are rejected with
+ * SDPA_ERR_WORKSPACE before anything is launched.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array, so calls whose work can overlap on the
+ *    GPU (other streams, other host threads) race on it and give wrong
+ *    gradients; serialise them.  Each call rewrites the part of the array it
+ *    uses before reading it, so leftovers of an earlier call do no harm.
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int sdpa_bwd_noalloc(const void *q, const void *k, const void *v,
+                     const void *o, const void *dout, const float *lse,
+                     void *dq, void *dk, void *dv, int b, int h, int s_q,
+                     int s_kv, int d, float attn_scale, int causal, int dtype,
+                     sdpa_stream_t stream);
+
 /* Message describing the last non-OK status returned on this host thread
  * ("" if none).  The pointer stays valid until the next call on the thread. */
 const char *sdpa_last_error(void);

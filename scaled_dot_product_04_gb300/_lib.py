@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
 
 # Exported symbols, in the order include/sdpa.h declares them.
 EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd",
-           "sdpa_varlen_bwd_workspace_size", "sdpa_varlen_bwd", "sdpa_last_error",
+           "sdpa_varlen_bwd_workspace_size", "sdpa_varlen_bwd", "sdpa_bwd_noalloc",
+           "sdpa_last_error",
            "sdpa_check_device_error", "sdpa_set_kernel_timer", "sdpa_version")
 
 
@@ -74,13 +75,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                  _I, _P, _Z, _P]
         lib.sdpa_varlen_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I,
                                         _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]
+        lib.sdpa_bwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                         _F, _I, _I, _P]
         lib.sdpa_last_error.restype = ctypes.c_char_p
         lib.sdpa_check_device_error.argtypes = [_P]
         lib.sdpa_version.restype = ctypes.c_char_p
         lib.sdpa_set_kernel_timer.argtypes = [_P, _P]
         lib.sdpa_set_kernel_timer.restype = None
         for name in ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
-                     "sdpa_check_device_error"):
+                     "sdpa_bwd_noalloc", "sdpa_check_device_error"):
             getattr(lib, name).restype = _I
         _lib = lib
         return lib
@@ -154,6 +157,14 @@ def sdpa_varlen_bwd(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_
                                   _ptr(cu_seqlens_kv), num_seqs, total_q, total_kv, max_seqlen_q,
                                   max_seqlen_kv, h, d, float(attn_scale), int(causal), int(dtype),
                                   _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def sdpa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, b, h, s_q, s_kv, d, attn_scale, causal,
+                     dtype, stream=None):
+    """Dense backward without a workspace (the library's built-in scratch array)."""
+    _check(load().sdpa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), b, h, s_q, s_kv, d,
+                                   float(attn_scale), int(causal), int(dtype), _stream(stream)))
 
 
 def sdpa_last_error() -> str:

@@ -185,6 +185,11 @@ int launch_status(cudaError_t e, const char *what) {
 }
 
 }  // namespace
+
+// Lets other translation units of the library set the message that
+// sdpa_last_error() returns on this thread.
+int report_error(int status, const char *message) { return fail(status, "%s", message); }
+
 }  // namespace sdpa
 
 using namespace sdpa;
