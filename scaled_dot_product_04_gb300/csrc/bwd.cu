@@ -134,7 +134,8 @@ struct BwdLayout {
     static constexpr int bQFull = 1;       // 2
     static constexpr int bDOFull = 3;      // 2
     static constexpr int bStatsFull = 5;   // 2
-    static constexpr int bStageEmpty = 7;  // 2
+    static constexpr int bQEmpty = 7;      // 2: Q (and row stats) stage, freed after dK
+    static constexpr int bDOEmpty = 18;    // 2: dO stage, freed after dV
     static constexpr int bSFull = 9;
     static constexpr int bDPFull = 10;
     static constexpr int bPReady = 11;
@@ -144,7 +145,7 @@ struct BwdLayout {
     static constexpr int bDQFree = 15;
     static constexpr int bDSFree = 16;
     static constexpr int bMmaIdle = 17;
-    static constexpr int kNumBars = 18;
+    static constexpr int kNumBars = 20;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
@@ -228,7 +229,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(L::bQFull + s), 1);
             mbar_init(bar(L::bDOFull + s), 1);
             mbar_init(bar(L::bStatsFull + s), 32);
-            mbar_init(bar(L::bStageEmpty + s), 1);
+            mbar_init(bar(L::bQEmpty + s), 1);
+            mbar_init(bar(L::bDOEmpty + s), 1);
         }
         mbar_init(bar(L::bSFull), 1);
         mbar_init(bar(L::bDPFull), 1);
@@ -268,24 +270,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(sbase + L::kV + c * L::kChunkBytes, &tm_v, bar(L::bKVFull), c * 64, ky, kz);
             }
         }
-        int issued = 0;
+        int issued = 0, issued_do = 0;
         for (int i = 0; i < n_q; ++i) {
             const int st = i & 1, use = i >> 1;
-            if (use > 0 && !warp_wait_b(bar(L::bStageEmpty + st), (use - 1) & 1, wc, 1)) break;
             const int q0 = (qt_begin + i) * kTileM;
+            const int qy = kPacked ? head : q0;
+            const int qz = kPacked ? tok_q0 + q0 : slice;
+            // dO's stage frees after dV, Q's only after dK: load dO first.
+            if (use > 0 && !warp_wait_b(bar(L::bDOEmpty + st), (use - 1) & 1, wc, 1)) break;
             if (lane == 0) {
-                const int qy = kPacked ? head : q0;
-                const int qz = kPacked ? tok_q0 + q0 : slice;
-                mbar_arrive_expect_tx(bar(L::bQFull + st), L::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kQ + st * L::kTileBytes + c * L::kChunkBytes, &tm_q,
-                                bar(L::bQFull + st), c * 64, qy, qz);
                 mbar_arrive_expect_tx(bar(L::bDOFull + st), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kDO + st * L::kTileBytes + c * L::kChunkBytes, &tm_do,
                                 bar(L::bDOFull + st), c * 64, qy, qz);
+            }
+            if (use > 0 && !warp_wait_b(bar(L::bQEmpty + st), (use - 1) & 1, wc, 18)) {
+                issued_do = i + 1;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(L::bQFull + st), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(sbase + L::kQ + st * L::kTileBytes + c * L::kChunkBytes, &tm_q,
+                                bar(L::bQFull + st), c * 64, qy, qz);
             }
             // Row statistics of the query tile: LSE*log2(e) and D.  Rows past
             // the sequence get +inf / 0 so their P (and so dS) is exactly 0.
@@ -305,14 +314,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 dd[r] = b;
             }
             mbar_arrive(bar(L::bStatsFull + st));
-            issued = i + 1;
+            issued = issued_do = i + 1;
         }
         if (lane == 0) {
             mbar_wait_drain(bar(L::bKVFull), 0);
-            for (int i = max(0, issued - 2); i < issued; ++i) {
+            for (int i = max(0, issued - 2); i < issued; ++i)
                 mbar_wait_drain(bar(L::bQFull + (i & 1)), (i >> 1) & 1);
+            for (int i = max(0, issued_do - 2); i < issued_do; ++i)
                 mbar_wait_drain(bar(L::bDOFull + (i & 1)), (i >> 1) & 1);
-            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -357,6 +366,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            smem_desc_sw128(sDO + k * 2048, L::kChunkBytes, 1024), id_mn,
                            (i > 0 || k > 0) ? 1u : 0u);
                 mma_commit(bar(L::bDVDone));
+                mma_commit(bar(L::bDOEmpty + st));
                 // S^T_{i+1}, once the dV product has finished reading P^T_i
                 if (i + 1 < n_q) {
                     const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
@@ -367,10 +377,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     issue_kmajor(sK, sbase + L::kQ + st1 * L::kTileBytes, L::kColS);
                     mma_commit(bar(L::bSFull));
                 }
-                // dK += dS^T Q ; dQ_i = dS K
+                // dQ_i = dS K first, so the epilogue's read of dQ_i overlaps
+                // dK += dS^T Q and frees the dP columns before dP^T_{i+1}.
                 ok = mbar_wait(bar(L::bDSReady), i & 1, wc, 8);
+                if (ok && !L::kDQAliasDP && i > 0) ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
                 if (!ok) break;
                 tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k)
+                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
+                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
+                mma_commit(bar(L::bDQFull));
 #pragma unroll
                 for (int k = 0; k < 128 / 16; ++k) {
                     const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
@@ -378,17 +395,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            smem_desc_sw128(sQ + k * 2048, L::kChunkBytes, 1024), id_mn,
                            (i > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(L::bStageEmpty + st));
-                if (!L::kDQAliasDP && i > 0) {
-                    ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int k = 0; k < 128 / 16; ++k)
-                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
-                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
-                mma_commit(bar(L::bDQFull));
+                mma_commit(bar(L::bQEmpty + st));
                 mma_commit(bar(L::bDSFree));
                 // dP^T_{i+1}
                 if (i + 1 < n_q) {

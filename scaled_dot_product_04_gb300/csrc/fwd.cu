@@ -39,7 +39,9 @@ struct FwdLayout {
     static constexpr int kChunks = D / 64;                // 128-byte swizzle columns per row
     static constexpr int kChunkBytes = kTileM * 128;      // 16 KiB: 128 rows x 64 elements
     static constexpr int kTileBytes = kChunks * kChunkBytes;
-    static constexpr int kStages = (D == 128) ? 2 : 4;
+    // K and V have rings of their own: a K stage is released once S = Q K^T
+    // has read it, a V stage once O += P V has, so the next loads start early.
+    static constexpr int kStages = (D == 128) ? 3 : 5;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kTileBytes;
     static constexpr int kV = kK + kStages * kTileBytes;
@@ -47,8 +49,9 @@ struct FwdLayout {
     static constexpr int bQFull = 0;
     static constexpr int bKFull = 1;
     static constexpr int bVFull = bKFull + kStages;
-    static constexpr int bKVEmpty = bVFull + kStages;
-    static constexpr int bSFull = bKVEmpty + kStages;  // two
+    static constexpr int bKEmpty = bVFull + kStages;
+    static constexpr int bVEmpty = bKEmpty + kStages;
+    static constexpr int bSFull = bVEmpty + kStages;  // two
     static constexpr int bPReady = bSFull + 2;
     static constexpr int bPVDone = bPReady + 1;
     static constexpr int bMmaIdle = bPVDone + 1;
@@ -143,7 +146,8 @@ __global__ void __launch_bounds__(192, 1)
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(bar(L::bKFull + s), 1);
             mbar_init(bar(L::bVFull + s), 1);
-            mbar_init(bar(L::bKVEmpty + s), 1);
+            mbar_init(bar(L::bKEmpty + s), 1);
+            mbar_init(bar(L::bVEmpty + s), 1);
         }
         mbar_init(bar(L::bSFull + 0), 1);
         mbar_init(bar(L::bSFull + 1), 1);
@@ -176,10 +180,10 @@ __global__ void __launch_bounds__(192, 1)
             for (int c = 0; c < L::kChunks; ++c)
                 tma_load_3d(sbase + L::kQ + c * L::kChunkBytes, &tm_q, bar(L::bQFull), c * 64, qy,
                             qz);
-            int issued = 0;
+            int issued = 0, issued_k = 0;
             for (int j = 0; j < n_kv; ++j) {
                 const int st = j % L::kStages, use = j / L::kStages;
-                if (use > 0 && !mbar_wait(bar(L::bKVEmpty + st), (use - 1) & 1, wc, 1)) break;
+                if (use > 0 && !mbar_wait(bar(L::bKEmpty + st), (use - 1) & 1, wc, 1)) break;
                 const int ky = kPacked ? head : j * kTileN;
                 const int kz = kPacked ? tok_kv0 + j * kTileN : slice;
                 const uint32_t ks = sbase + L::kK + st * L::kTileBytes;
@@ -188,19 +192,22 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(ks + c * L::kChunkBytes, &tm_k, bar(L::bKFull + st), c * 64, ky, kz);
+                if (use > 0 && !mbar_wait(bar(L::bVEmpty + st), (use - 1) & 1, wc, 11)) {
+                    issued_k = j + 1;
+                    break;
+                }
                 mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(vs + c * L::kChunkBytes, &tm_v, bar(L::bVFull + st), c * 64, ky, kz);
-                issued = j + 1;
+                issued = issued_k = j + 1;
             }
             // Every load issued must land before the CTA may exit.
             mbar_wait_drain(bar(L::bQFull), 0);
-            for (int j = max(0, issued - L::kStages); j < issued; ++j) {
-                const int st = j % L::kStages, use = j / L::kStages;
-                mbar_wait_drain(bar(L::bKFull + st), use & 1);
-                mbar_wait_drain(bar(L::bVFull + st), use & 1);
-            }
+            for (int j = max(0, issued_k - L::kStages); j < issued_k; ++j)
+                mbar_wait_drain(bar(L::bKFull + j % L::kStages), (j / L::kStages) & 1);
+            for (int j = max(0, issued - L::kStages); j < issued; ++j)
+                mbar_wait_drain(bar(L::bVFull + j % L::kStages), (j / L::kStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -236,6 +243,7 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
                 issue_s(0, 0);
                 mma_commit(bar(L::bSFull + 0));
+                mma_commit(bar(L::bKEmpty + 0));
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (j + 1 < n_kv) {
@@ -248,6 +256,7 @@ __global__ void __launch_bounds__(192, 1)
                     tc_fence_after();
                     issue_s(st1, ((j + 1) & 1) * 128);
                     mma_commit(bar(L::bSFull + ((j + 1) & 1)));
+                    mma_commit(bar(L::bKEmpty + st1));
                 }
                 ok = mbar_wait(bar(L::bPReady), j & 1, wc, 6) &&
                      mbar_wait(bar(L::bVFull + j % L::kStages), (j / L::kStages) & 1, wc, 7);
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
                 issue_pv(j % L::kStages, (j & 1) * 128, j > 0);
                 mma_commit(bar(L::bPVDone));
-                mma_commit(bar(L::bKVEmpty + j % L::kStages));
+                mma_commit(bar(L::bVEmpty + j % L::kStages));
             }
             // Let every MMA issued above retire before TMEM is released.
             mma_commit(bar(L::bMmaIdle));
@@ -290,9 +299,16 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c = 0; c < kTileN; ++c)
                     if (c >= lim) s[c] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max: four independent chains of 3-input max
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+            for (int c = 0; c < kTileN; c += 8) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mx4[u] = fmax3(mx4[u], __uint_as_float(s[c + 2 * u]),
+                                   __uint_as_float(s[c + 2 * u + 1]));
+            }
+            const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
             const float m_tile = mx * sl2;
             float alpha = 1.f;
             bool rescale = false;
@@ -303,16 +319,24 @@ __global__ void __launch_bounds__(192, 1)
                 l *= alpha;
             }
             const float base = (m_used == -INFINITY) ? 0.f : m_used;
-            float rs0 = 0.f, rs1 = 0.f;
+            const uint64_t sl2_2 = f2_pack(sl2, sl2), nbase_2 = f2_pack(-base, -base);
+            // P = exp2(s * scale*log2e - base), pairs packed in place into s[0..64)
+            uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int i = 0; i < kTileN / 2; ++i) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), sl2, -base));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), sl2, -base));
-                rs0 += p0;
-                rs1 += p1;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                 sl2_2, nbase_2),
+                          x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
                 s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
             }
-            l += rs0 + rs1;
+            {
+                float a0, a1;
+                f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), a0, a1);
+                l += a0 + a1;
+            }
             tmem_st32(t_lane + cs, s);
             tmem_st32(t_lane + cs + 32, s + 32);
 

@@ -233,6 +233,32 @@ SDPA_DEV float lg2_approx(float x) {
     return y;
 }
 
+// Packed fp32 pair arithmetic (two lanes per instruction on sm_100+).
+SDPA_DEV uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+SDPA_DEV void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// (lo, hi) * (a.lo, a.hi) + (b.lo, b.hi)
+SDPA_DEV uint64_t f2_fma(uint64_t x, uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(a), "l"(b));
+    return r;
+}
+SDPA_DEV uint64_t f2_add(uint64_t x, uint64_t y) {
+    uint64_t r;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    return r;
+}
+SDPA_DEV float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 template <bool kBf16>
 SDPA_DEV uint32_t pack2(float lo, float hi) {
     uint32_t r;
