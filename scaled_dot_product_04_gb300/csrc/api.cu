@@ -131,6 +131,20 @@ int packed_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int h, int64_t
     return encode_map(m, ptr, bf16, d, h, tokens, (uint64_t)d * 2, (uint64_t)h * d * 2, 1, 128);
 }
 
+// fp32 dQ accumulator [rows][d] as a 2-D map with 32 x 32 boxes (128-byte rows,
+// 128-byte swizzle) for TMA reduce-add.
+int acc_map(CUtensorMap *m, float *acc, int d, int64_t rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled (dQ accumulator) failed (%d)", (int)r);
+    return SDPA_OK;
+}
+
 // ----------------------------------------------------------- validation
 struct Span {
     const void *p;
@@ -384,6 +398,8 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     if ((st = dense_map(&tk, k, bf16, d, s_kv, bh))) return st;
     if ((st = dense_map(&tv, v, bf16, d, s_kv, bh))) return st;
     if ((st = dense_map(&tdo, dout, bf16, d, s_q, bh))) return st;
+    CUtensorMap tdq;
+    if ((st = acc_map(&tdq, static_cast<float *>(workspace), d, bh * s_q))) return st;
     BwdParams p{};
     p.o = o;
     p.dout = dout;
@@ -404,7 +420,7 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     p.causal = causal;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
+    return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
 }
 
 int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -450,6 +466,8 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     if ((st = packed_map(&tk, k, bf16, d, h, total_kv))) return st;
     if ((st = packed_map(&tv, v, bf16, d, h, total_kv))) return st;
     if ((st = packed_map(&tdo, dout, bf16, d, h, total_q))) return st;
+    CUtensorMap tdq;
+    if ((st = acc_map(&tdq, static_cast<float *>(workspace), d, (int64_t)total_q * h))) return st;
     BwdParams p{};
     p.o = o;
     p.dout = dout;
@@ -471,7 +489,7 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     p.causal = causal;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_bwd(tq, tk, tv, tdo, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
+    return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
 }
 
 }  // extern "C"

@@ -124,10 +124,15 @@ struct BwdLayout {
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kK = 0;
     static constexpr int kV = kK + kTileBytes;
+    // dO is read by dP^T_i and dV_i only, and dO_{i+1} is not needed before
+    // dP^T_{i+1}, so one buffer suffices at d = 128 and frees room for the
+    // dQ staging boxes.
+    static constexpr int kDOStages = (D == 128) ? 1 : 2;
     static constexpr int kQ = kV + kTileBytes;               // 2 stages
-    static constexpr int kDO = kQ + 2 * kTileBytes;          // 2 stages
-    static constexpr int kDS = kDO + 2 * kTileBytes;         // 128 keys x 128 queries bf16
-    static constexpr int kStats = kDS + 2 * kChunkBytes;     // 2 stages x (lse2[128], D[128])
+    static constexpr int kDO = kQ + 2 * kTileBytes;          // kDOStages stages
+    static constexpr int kDS = kDO + kDOStages * kTileBytes; // 128 keys x 128 queries bf16
+    static constexpr int kDQStage = kDS + 2 * kChunkBytes;   // 4 warps x 2 boxes x 4 KiB fp32
+    static constexpr int kStats = kDQStage + 4 * 2 * 4096;   // 2 stages x (lse2[128], D[128])
     static constexpr int kBar = kStats + 2 * 2 * 128 * 4;
     // barriers
     static constexpr int bKVFull = 0;
@@ -135,7 +140,7 @@ struct BwdLayout {
     static constexpr int bDOFull = 3;      // 2
     static constexpr int bStatsFull = 5;   // 2
     static constexpr int bQEmpty = 7;      // 2: Q (and row stats) stage, freed after dK
-    static constexpr int bDOEmpty = 18;    // 2: dO stage, freed after dV
+    static constexpr int bDOEmpty = 18;    // kDOStages: dO stage, freed after dV
     static constexpr int bSFull = 9;
     static constexpr int bDPFull = 10;
     static constexpr int bPReady = 11;
@@ -163,7 +168,7 @@ template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(L::bDOFull + s), 1);
             mbar_init(bar(L::bStatsFull + s), 32);
             mbar_init(bar(L::bQEmpty + s), 1);
-            mbar_init(bar(L::bDOEmpty + s), 1);
+            if (s < L::kDOStages) mbar_init(bar(L::bDOEmpty + s), 1);
         }
         mbar_init(bar(L::bSFull), 1);
         mbar_init(bar(L::bDPFull), 1);
@@ -273,22 +278,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int issued = 0, issued_do = 0;
         for (int i = 0; i < n_q; ++i) {
             const int st = i & 1, use = i >> 1;
+            const int dst = i % L::kDOStages, duse = i / L::kDOStages;
             const int q0 = (qt_begin + i) * kTileM;
             const int qy = kPacked ? head : q0;
             const int qz = kPacked ? tok_q0 + q0 : slice;
-            // dO's stage frees after dV, Q's only after dK: load dO first.
-            if (use > 0 && !warp_wait_b(bar(L::bDOEmpty + st), (use - 1) & 1, wc, 1)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(L::bDOFull + st), L::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kDO + st * L::kTileBytes + c * L::kChunkBytes, &tm_do,
-                                bar(L::bDOFull + st), c * 64, qy, qz);
-            }
-            if (use > 0 && !warp_wait_b(bar(L::bQEmpty + st), (use - 1) & 1, wc, 18)) {
-                issued_do = i + 1;
-                break;
-            }
+            // Q_i (freed by dK_{i-2}) is needed first, by S^T_i; dO_i (freed by
+            // dV_{i-kDOStages}) only by dP^T_i.
+            if (use > 0 && !warp_wait_b(bar(L::bQEmpty + st), (use - 1) & 1, wc, 18)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(L::bQFull + st), L::kTileBytes);
 #pragma unroll
@@ -296,6 +292,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_load_3d(sbase + L::kQ + st * L::kTileBytes + c * L::kChunkBytes, &tm_q,
                                 bar(L::bQFull + st), c * 64, qy, qz);
             }
+            issued = i + 1;
             // Row statistics of the query tile: LSE*log2(e) and D.  Rows past
             // the sequence get +inf / 0 so their P (and so dS) is exactly 0.
             float *lse2 = stats + st * 256;
@@ -314,14 +311,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 dd[r] = b;
             }
             mbar_arrive(bar(L::bStatsFull + st));
-            issued = issued_do = i + 1;
+            if (duse > 0 && !warp_wait_b(bar(L::bDOEmpty + dst), (duse - 1) & 1, wc, 1)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(L::bDOFull + dst), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(sbase + L::kDO + dst * L::kTileBytes + c * L::kChunkBytes, &tm_do,
+                                bar(L::bDOFull + dst), c * 64, qy, qz);
+            }
+            issued_do = i + 1;
         }
         if (lane == 0) {
             mbar_wait_drain(bar(L::bKVFull), 0);
             for (int i = max(0, issued - 2); i < issued; ++i)
                 mbar_wait_drain(bar(L::bQFull + (i & 1)), (i >> 1) & 1);
-            for (int i = max(0, issued_do - 2); i < issued_do; ++i)
-                mbar_wait_drain(bar(L::bDOFull + (i & 1)), (i >> 1) & 1);
+            for (int i = max(0, issued_do - L::kDOStages); i < issued_do; ++i)
+                mbar_wait_drain(bar(L::bDOFull + i % L::kDOStages), (i / L::kDOStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -355,7 +360,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int i = 0; ok && i < n_q; ++i) {
                 const int st = i & 1;
                 const uint32_t sQ = sbase + L::kQ + st * L::kTileBytes;
-                const uint32_t sDO = sbase + L::kDO + st * L::kTileBytes;
+                const int dst = i % L::kDOStages;
+                const uint32_t sDO = sbase + L::kDO + dst * L::kTileBytes;
                 // dV += P^T dO  (P^T bf16 in the S columns)
                 ok = mbar_wait(bar(L::bPReady), i & 1, wc, 5);
                 if (!ok) break;
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            smem_desc_sw128(sDO + k * 2048, L::kChunkBytes, 1024), id_mn,
                            (i > 0 || k > 0) ? 1u : 0u);
                 mma_commit(bar(L::bDVDone));
-                mma_commit(bar(L::bDOEmpty + st));
+                mma_commit(bar(L::bDOEmpty + dst));
                 // S^T_{i+1}, once the dV product has finished reading P^T_i
                 if (i + 1 < n_q) {
                     const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
@@ -377,17 +383,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     issue_kmajor(sK, sbase + L::kQ + st1 * L::kTileBytes, L::kColS);
                     mma_commit(bar(L::bSFull));
                 }
-                // dQ_i = dS K first, so the epilogue's read of dQ_i overlaps
-                // dK += dS^T Q and frees the dP columns before dP^T_{i+1}.
+                // dK += dS^T Q (last reader of Q_i), then dQ_i = dS K
                 ok = mbar_wait(bar(L::bDSReady), i & 1, wc, 8);
-                if (ok && !L::kDQAliasDP && i > 0) ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 128 / 16; ++k)
-                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
-                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
-                mma_commit(bar(L::bDQFull));
 #pragma unroll
                 for (int k = 0; k < 128 / 16; ++k) {
                     const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
@@ -396,15 +395,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            (i > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(L::bQEmpty + st));
+                if (!L::kDQAliasDP && i > 0) {
+                    ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k)
+                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
+                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
+                mma_commit(bar(L::bDQFull));
                 mma_commit(bar(L::bDSFree));
                 // dP^T_{i+1}
                 if (i + 1 < n_q) {
-                    const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
-                    ok = mbar_wait(bar(L::bDOFull + st1), use1 & 1, wc, 10);
+                    const int dst1 = (i + 1) % L::kDOStages, duse1 = (i + 1) / L::kDOStages;
+                    ok = mbar_wait(bar(L::bDOFull + dst1), duse1 & 1, wc, 10);
                     if (ok && L::kDQAliasDP) ok = mbar_wait(bar(L::bDQFree), i & 1, wc, 11);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_kmajor(sV, sbase + L::kDO + st1 * L::kTileBytes, L::kColDP);
+                    issue_kmajor(sV, sbase + L::kDO + dst1 * L::kTileBytes, L::kColDP);
                     mma_commit(bar(L::bDPFull));
                 }
             }
@@ -528,9 +537,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else {
         // ============================================================ dQ epilogue
+        // Each warp owns 32 query rows (its TMEM lane quadrant).  dQ_i leaves
+        // TMEM at once (freeing the columns), then goes out in 32 x 32 fp32
+        // boxes: staged in shared memory with the 128-byte swizzle and added
+        // into the fp32 accumulator by TMA reduce-add through tm_dq, two
+        // boxes in flight per warp.  Rows past the sequence carry exact zeros
+        // (their P is 0); rows past the accumulator are dropped by the map.
         const int quad = warp & 3;
-        const int qr = quad * 32 + lane;  // query row of the tile == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t stage = sbase + L::kDQStage + quad * 8192;
+        uint8_t *stage_ptr = smem + L::kDQStage + quad * 8192;
+        const int acc_row0 = (int)(qm.acc0 / D);
+        int boxes = 0;
         for (int i = 0; i < n_q; ++i) {
             if (!warp_wait_b(bar(L::bDQFull), i & 1, wc, 17)) break;
             tc_fence_after();
@@ -540,18 +558,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld_wait_regs<D>(r);
             tc_fence_before();
             mbar_arrive(bar(L::bDQFree));
-            const int q = (qt_begin + i) * kTileM + qr;
-            if (q < Lq) {
-                float *dst = p.dq_acc + qm.acc0 + (int64_t)q * D;
+            const int qrow0 = (qt_begin + i) * kTileM + quad * 32;
+            if (qrow0 >= Lq) continue;  // no live row in this warp's quarter
 #pragma unroll
-                for (int c = 0; c < D; c += 4) {
-                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c),
-                                 "f"(__uint_as_float(r[c])), "f"(__uint_as_float(r[c + 1])),
-                                 "f"(__uint_as_float(r[c + 2])), "f"(__uint_as_float(r[c + 3]))
-                                 : "memory");
+            for (int c = 0; c < D / 32; ++c, ++boxes) {
+                const int slot = boxes & 1;
+                if (boxes >= 2) {
+                    if (lane == 0) bulk_wait_read<1>();  // the slot's previous box has been read
+                    __syncwarp();
+                }
+                uint8_t *row = stage_ptr + slot * 4096 + lane * 128;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<uint4 *>(row + ((u ^ (lane & 7)) << 4)) =
+                        make_uint4(r[c * 32 + 4 * u], r[c * 32 + 4 * u + 1], r[c * 32 + 4 * u + 2],
+                                   r[c * 32 + 4 * u + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_2d(&tm_dq, stage + slot * 4096, c * 32, acc_row0 + qrow0);
+                    bulk_commit();
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -564,8 +595,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool kBf16, bool kPacked>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo, const BwdParams &p, cudaStream_t stream,
-                         const KernelTimer &timer) {
+                         const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &p,
+                         cudaStream_t stream, const KernelTimer &timer) {
     using L = BwdLayout<D>;
     const int64_t rows = kPacked ? (int64_t)p.total_q * p.h : (int64_t)p.bh * p.s_q;
     const int64_t acc_elems = rows * D;
@@ -581,7 +612,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     if (e != cudaSuccess) return e;
     const int grid = p.kv_tiles * p.bh;
     if (timer.start) cudaEventRecord(timer.start, stream);
-    kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, p);
+    kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
     if (timer.stop) cudaEventRecord(timer.stop, stream);
     if (e != cudaSuccess) return e;
@@ -592,11 +623,11 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const BwdParams &p, int d, bool bf16, bool packed,
-                       cudaStream_t stream, const KernelTimer &timer) {
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &p, int d,
+                       bool bf16, bool packed, cudaStream_t stream, const KernelTimer &timer) {
 #define SDPA_BWD_CASE(D_, BF_, PK_)                                            \
     if (d == D_ && bf16 == BF_ && packed == PK_)                               \
-        return launch_bwd_t<D_, BF_, PK_>(tq, tk, tv, tdo, p, stream, timer);
+        return launch_bwd_t<D_, BF_, PK_>(tq, tk, tv, tdo, tdq, p, stream, timer);
     SDPA_BWD_CASE(64, true, false)
     SDPA_BWD_CASE(64, true, true)
     SDPA_BWD_CASE(64, false, false)

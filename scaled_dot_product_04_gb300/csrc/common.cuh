@@ -65,8 +65,9 @@ struct KernelTimer {
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
                        cudaStream_t stream, const KernelTimer &timer);
+// tdq: 2-D fp32 map over the dQ accumulator [rows][d], box 32 x 32, 128-byte swizzle.
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const BwdParams &p, int d, bool bf16, bool packed,
-                       cudaStream_t stream, const KernelTimer &timer);
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &p, int d,
+                       bool bf16, bool packed, cudaStream_t stream, const KernelTimer &timer);
 
 }  // namespace sdpa

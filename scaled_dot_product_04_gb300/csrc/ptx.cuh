@@ -112,6 +112,25 @@ SDPA_DEV void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int 
         : "memory");
 }
 
+// Element-wise add of a shared-memory box into global memory through a 2-D
+// tensor map (out-of-bounds parts of the box are dropped), tracked as a bulk
+// async-group of the issuing thread.
+SDPA_DEV void tma_reduce_add_2d(const CUtensorMap *m, uint32_t src, int c0, int c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(m)),
+        "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+}
+SDPA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+SDPA_DEV void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+SDPA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tcgen05
 // TMEM allocation: executed by one whole warp.  The allocated base address is
 // written to shared memory at `dst_smem`.
