@@ -2,6 +2,7 @@
 // construction and kernel launch.  Nothing here allocates device memory or
 // synchronises the host (except sdpa_check_device_error, which exists to do
 // exactly that).  Declarations and the contract live in include/sdpa.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -268,9 +269,10 @@ int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     p.s_q = s_q;
     p.s_kv = s_kv;
     p.q_tiles = (int)q_tiles;
+    p.n_units = (int)(q_tiles * bh);
     p.causal = causal;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, false, (int)(q_tiles * bh),
+    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, false, std::min(p.n_units, dev->sm_count),
                                     static_cast<cudaStream_t>(stream), t_timer),
                          "sdpa_fwd");
 }
@@ -332,9 +334,10 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
     p.h = h;
     p.num_seqs = num_seqs;
     p.q_tiles = (int)q_tiles;
+    p.n_units = (int)(q_tiles * slices);
     p.causal = causal;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, true, (int)(q_tiles * slices),
+    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, true, std::min(p.n_units, dev->sm_count),
                                     static_cast<cudaStream_t>(stream), t_timer),
                          "sdpa_varlen_fwd");
 }

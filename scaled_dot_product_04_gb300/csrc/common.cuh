@@ -33,6 +33,7 @@ struct FwdParams {
     int s_q, s_kv;               // dense lengths
     int num_seqs;                // packed
     int q_tiles;                 // dense: ceil(s_q/128); packed: ceil(max_seqlen_q/128)
+    int n_units;                 // q_tiles * bh (units a persistent CTA may visit)
     int causal;
     float scale_log2;            // attn_scale * log2(e)
 };

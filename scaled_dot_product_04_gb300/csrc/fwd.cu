@@ -10,17 +10,25 @@
 // or multiplied; only diagonal and ragged-tail tiles pay for masking
 // (cudnn-frontend PR #554, SM80 backward notes on PARTIAL/GATE tile bounds).
 //
-// One CTA owns one 128-row query tile of one (batch, head) or (sequence,
-// head) and streams the key/value tiles it may see:
-//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages;
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into TMEM (two S
-//               buffers so S_{j+1} overlaps the softmax of S_j), then
-//               O += P_j V_j with P_j read straight from TMEM;
+// Persistent schedule (cudnn-frontend PR #554, "Thd persistent grid" and the
+// LPT scheduler notes): the grid is capped at one CTA per SM; CTA c walks
+// the units c, c + grid, c + 2*grid, ... of a list ordered latest query tile
+// first, which under the causal mask is heaviest first.  A unit is one
+// 128-row query tile of one (batch, head) or (sequence, head).  Packed
+// sequences are found from cu_seqlens on the device (cached in shared
+// memory); a unit past its sequence's end costs a few instructions.
+//
+// Roles inside a CTA:
+//   warp 0      TMA producer: Q of each unit, then K_j / V_j into two rings;
+//   warp 1      MMA issuer (one thread): S_t = Q K_t^T into TMEM (two S
+//               buffers, alternating over the CTA's running tile count t),
+//               then O += P_t V_t with P_t read straight from TMEM;
 //   warps 2..5  softmax: thread r owns query row r (= TMEM lane r); it reads
-//               S_j, applies the mask, keeps the fp32 running max/sum,
-//               writes P_j (bf16/fp16) back into the S_j columns, rescales O
-//               in TMEM when the running max grows by more than 2^8, and
-//               finally normalises O and writes O and LSE to global memory.
+//               S_t, applies the mask, keeps the fp32 running max/sum, writes
+//               P_t (bf16/fp16) back into the S_t columns, rescales O in TMEM
+//               when the running max grows by more than 2^8, and finally
+//               normalises O and writes O and LSE -- while the MMA warp
+//               already runs the next unit's first products.
 // TMEM columns: S buffers at 0 and 128, O at 256 (d columns).
 //
 // Packed layout: the Q/K/V tensor maps span exactly total_q / total_kv
@@ -41,20 +49,30 @@ struct FwdLayout {
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     // K and V have rings of their own: a K stage is released once S = Q K^T
     // has read it, a V stage once O += P V has, so the next loads start early.
-    static constexpr int kStages = (D == 128) ? 3 : 5;
+    static constexpr int kKStages = (D == 128) ? 3 : 5;
+    static constexpr int kVStages = (D == 128) ? 3 : 4;
+    // cu_seqlens entries cached in shared memory (longer lists are read from
+    // global memory); at d = 128 only the room left by the rings is used.
+    static constexpr int kCuCap = (D == 128) ? 192 : 2048;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kTileBytes;
-    static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kBar = kV + kStages * kTileBytes;
+    static constexpr int kV = kK + kKStages * kTileBytes;
+    static constexpr int kCu = kV + kVStages * kTileBytes;  // int32 cu_q[kCuCap], cu_kv[kCuCap]
+    static constexpr int kBar = kCu + 2 * kCuCap * 4;
     static constexpr int bQFull = 0;
-    static constexpr int bKFull = 1;
-    static constexpr int bVFull = bKFull + kStages;
-    static constexpr int bKEmpty = bVFull + kStages;
-    static constexpr int bVEmpty = bKEmpty + kStages;
-    static constexpr int bSFull = bVEmpty + kStages;  // two
-    static constexpr int bPReady = bSFull + 2;
-    static constexpr int bPVDone = bPReady + 1;
-    static constexpr int bMmaIdle = bPVDone + 1;
+    static constexpr int bQEmpty = 1;
+    static constexpr int bKFull = 2;
+    static constexpr int bKEmpty = bKFull + kKStages;
+    static constexpr int bVFull = bKEmpty + kKStages;
+    static constexpr int bVEmpty = bVFull + kVStages;
+    static constexpr int bSFull = bVEmpty + kVStages;  // two
+    // P_t ready / P_t V_t retired: two barriers each, indexed by t & 1, so no
+    // waiter can ever be two phases away from the barrier it polls.
+    static constexpr int bPReady = bSFull + 2;   // two
+    static constexpr int bPVDone = bPReady + 2;  // two
+    static constexpr int bOFull = bPVDone + 2;   // a unit's last P V retired
+    static constexpr int bOFree = bOFull + 1;    // the epilogue has read O
+    static constexpr int bMmaIdle = bOFree + 1;
     static constexpr int kNumBars = bMmaIdle + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;  // u32[0] TMEM base, u32[1] abort flag
     static constexpr int kBytes = kMisc + 16;
@@ -73,86 +91,106 @@ SDPA_DEV bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_
     return __all_sync(0xffffffffu, ok);
 }
 
+// k-th unit of CTA `first` out of `step`: a boustrophedon walk over the
+// heaviest-first list (c, 2G-1-c, 2G+c, 4G-1-c, ...), which evens out the
+// per-CTA sums of a decreasing cost list better than plain striding.
+SDPA_DEV int unit_of(int k, int first, int step) {
+    return k * step + ((k & 1) ? step - 1 - first : first);
+}
+
+// One work unit: a 128-row query tile of one slice.
+struct Unit {
+    int slice, head, Lq, Lkv, tok_q0, tok_kv0, row0, n_kv;
+    bool live;  // the tile holds at least one query row
+    int64_t o_row0, o_rs, lse_row0, lse_rs;
+};
+
+template <int D, bool kPacked>
+SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int *cu_kv) {
+    Unit U;
+    const int qt = p.q_tiles - 1 - u / p.bh;  // latest (heaviest) query tiles first
+    U.slice = u % p.bh;
+    if constexpr (!kPacked) {
+        U.head = 0;
+        U.tok_q0 = U.tok_kv0 = 0;
+        U.Lq = p.s_q;
+        U.Lkv = p.s_kv;
+        U.o_row0 = (int64_t)U.slice * p.s_q * D;
+        U.o_rs = D;
+        U.lse_row0 = (int64_t)U.slice * p.s_q;
+        U.lse_rs = 1;
+    } else {
+        const int n = U.slice / p.h;
+        U.head = U.slice % p.h;
+        U.tok_q0 = cu_q[n];
+        U.tok_kv0 = cu_kv[n];
+        U.Lq = cu_q[n + 1] - U.tok_q0;
+        U.Lkv = cu_kv[n + 1] - U.tok_kv0;
+        U.o_row0 = ((int64_t)U.tok_q0 * p.h + U.head) * D;
+        U.o_rs = (int64_t)p.h * D;
+        U.lse_row0 = (int64_t)U.tok_q0 * p.h + U.head;
+        U.lse_rs = p.h;
+    }
+    U.row0 = qt * kTileM;
+    U.live = U.row0 < U.Lq;
+    int n_kv = (U.Lkv + kTileN - 1) / kTileN;
+    if (p.causal) {
+        const int q_last = min(U.row0 + kTileM - 1, U.Lq - 1);
+        n_kv = min(n_kv, q_last / kTileN + 1);
+    }
+    U.n_kv = U.live ? max(n_kv, 0) : 0;
+    return U;
+}
+
 template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(192, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     using L = FwdLayout<D>;
+    using io_t = uint16_t;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (sbase - raw_base);
-
-    // ---------------------------------------------------------------- work unit
-    // Units are ordered by query tile, latest (heaviest under the causal mask)
-    // first, so the longest tiles start in the first wave.
-    const int unit = blockIdx.x;
-    const int qt = p.q_tiles - 1 - unit / p.bh;
-    const int slice = unit % p.bh;  // dense: b*h index.  packed: seq*h + head
-    int Lq, Lkv, tok_q0 = 0, tok_kv0 = 0, head = 0;
-    int64_t o_row0, o_rs, lse_row0, lse_rs;
-    if constexpr (!kPacked) {
-        Lq = p.s_q;
-        Lkv = p.s_kv;
-        o_row0 = (int64_t)slice * p.s_q * D;
-        o_rs = D;
-        lse_row0 = (int64_t)slice * p.s_q;
-        lse_rs = 1;
-    } else {
-        const int n = slice / p.h;
-        head = slice % p.h;
-        tok_q0 = p.cu_q[n];
-        tok_kv0 = p.cu_kv[n];
-        Lq = p.cu_q[n + 1] - tok_q0;
-        Lkv = p.cu_kv[n + 1] - tok_kv0;
-        o_row0 = ((int64_t)tok_q0 * p.h + head) * D;
-        o_rs = (int64_t)p.h * D;
-        lse_row0 = (int64_t)tok_q0 * p.h + head;
-        lse_rs = p.h;
-    }
-    const int row0 = qt * kTileM;
-    if (row0 >= Lq) return;  // packed: this sequence has fewer query tiles
-
-    int n_kv = (Lkv + kTileN - 1) / kTileN;
-    if (p.causal) {
-        const int q_last = min(row0 + kTileM - 1, Lq - 1);
-        n_kv = min(n_kv, q_last / kTileN + 1);
-    }
-
-    using io_t = uint16_t;
-    io_t *const o_base = reinterpret_cast<io_t *>(p.o) + o_row0;
-
-    if (n_kv == 0) {
-        // No key is visible to any row of this tile: O = 0, LSE = -inf.
-        if (threadIdx.x < kTileM) {
-            const int r = row0 + threadIdx.x;
-            if (r < Lq) {
-                uint4 *dst = reinterpret_cast<uint4 *>(o_base + (int64_t)r * o_rs);
-#pragma unroll
-                for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-                if (p.lse) p.lse[lse_row0 + (int64_t)r * lse_rs] = -INFINITY;
-            }
-        }
-        return;
-    }
-
     auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
 
+    // cu_seqlens of packed inputs, cached when they fit
+    int *cu_q_s = reinterpret_cast<int *>(smem + L::kCu);
+    int *cu_kv_s = cu_q_s + L::kCuCap;
+    const int *cu_q = p.cu_q, *cu_kv = p.cu_kv;
+    if constexpr (kPacked) {
+        if (p.num_seqs + 1 <= L::kCuCap) {
+            for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) {
+                cu_q_s[i] = p.cu_q[i];
+                cu_kv_s[i] = p.cu_kv[i];
+            }
+            cu_q = cu_q_s;
+            cu_kv = cu_kv_s;
+        }
+    }
+
     if (threadIdx.x == 0) {
         mbar_init(bar(L::bQFull), 1);
-        for (int s = 0; s < L::kStages; ++s) {
+        mbar_init(bar(L::bQEmpty), 1);
+        for (int s = 0; s < L::kKStages; ++s) {
             mbar_init(bar(L::bKFull + s), 1);
-            mbar_init(bar(L::bVFull + s), 1);
             mbar_init(bar(L::bKEmpty + s), 1);
+        }
+        for (int s = 0; s < L::kVStages; ++s) {
+            mbar_init(bar(L::bVFull + s), 1);
             mbar_init(bar(L::bVEmpty + s), 1);
         }
         mbar_init(bar(L::bSFull + 0), 1);
         mbar_init(bar(L::bSFull + 1), 1);
-        mbar_init(bar(L::bPReady), kTileM);
-        mbar_init(bar(L::bPVDone), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::bPReady + b), kTileM);
+            mbar_init(bar(L::bPVDone + b), 1);
+        }
+        mbar_init(bar(L::bOFull), 1);
+        mbar_init(bar(L::bOFree), kTileM);
         mbar_init(bar(L::bMmaIdle), 1);
         misc[1] = 0u;
         fence_mbar_init();
@@ -166,6 +204,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const WaitCtx wc{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.err, kTagFwd};
+    const int first = blockIdx.x, step = gridDim.x, n_units = p.n_units;
 
     if (warp == 0) {
         // ============================================================ producer
@@ -173,41 +212,66 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            const int qy = kPacked ? head : row0;
-            const int qz = kPacked ? tok_q0 + row0 : slice;
-            mbar_arrive_expect_tx(bar(L::bQFull), L::kTileBytes);
-#pragma unroll
-            for (int c = 0; c < L::kChunks; ++c)
-                tma_load_3d(sbase + L::kQ + c * L::kChunkBytes, &tm_q, bar(L::bQFull), c * 64, qy,
-                            qz);
-            int issued = 0, issued_k = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j % L::kStages, use = j / L::kStages;
-                if (use > 0 && !mbar_wait(bar(L::bKEmpty + st), (use - 1) & 1, wc, 1)) break;
-                const int ky = kPacked ? head : j * kTileN;
-                const int kz = kPacked ? tok_kv0 + j * kTileN : slice;
-                const uint32_t ks = sbase + L::kK + st * L::kTileBytes;
-                const uint32_t vs = sbase + L::kV + st * L::kTileBytes;
-                mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTileBytes);
+            // V_x is issued one tile after K_x, so a wait for a free V stage
+            // never holds back the K load that the next S product needs first.
+            int k_it = 0, v_it = 0, units = 0;
+            int pv_y = 0, pv_z = 0;
+            bool v_pending = false, ok = true;
+            auto issue_v = [&](int y, int z) -> bool {
+                const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
+                if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) return false;
+                mbar_arrive_expect_tx(bar(L::bVFull + vs), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(ks + c * L::kChunkBytes, &tm_k, bar(L::bKFull + st), c * 64, ky, kz);
-                if (use > 0 && !mbar_wait(bar(L::bVEmpty + st), (use - 1) & 1, wc, 11)) {
-                    issued_k = j + 1;
-                    break;
+                    tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
+                                bar(L::bVFull + vs), c * 64, y, z);
+                ++v_it;
+                return true;
+            };
+            for (int k = 0; ok; ++k) {
+                const int u = unit_of(k, first, step);
+                if (u >= n_units) break;
+                const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv);
+                if (U.n_kv == 0) continue;
+                // the previous unit's last V goes out before waiting for Q's slot
+                if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
+                v_pending = false;
+                if (units > 0 && !mbar_wait(bar(L::bQEmpty), (units - 1) & 1, wc, 1)) break;
+                const int qy = kPacked ? U.head : U.row0;
+                const int qz = kPacked ? U.tok_q0 + U.row0 : U.slice;
+                mbar_arrive_expect_tx(bar(L::bQFull), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(sbase + L::kQ + c * L::kChunkBytes, &tm_q, bar(L::bQFull), c * 64,
+                                qy, qz);
+                ++units;
+                for (int j = 0; j < U.n_kv; ++j) {
+                    const int ky = kPacked ? U.head : j * kTileN;
+                    const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.slice;
+                    const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
+                    if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(L::bKFull + ks), L::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
+                                    bar(L::bKFull + ks), c * 64, ky, kz);
+                    ++k_it;
+                    if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
+                    pv_y = ky;
+                    pv_z = kz;
+                    v_pending = true;
                 }
-                mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(vs + c * L::kChunkBytes, &tm_v, bar(L::bVFull + st), c * 64, ky, kz);
-                issued = issued_k = j + 1;
             }
+            if (ok && v_pending) issue_v(pv_y, pv_z);
             // Every load issued must land before the CTA may exit.
-            mbar_wait_drain(bar(L::bQFull), 0);
-            for (int j = max(0, issued_k - L::kStages); j < issued_k; ++j)
-                mbar_wait_drain(bar(L::bKFull + j % L::kStages), (j / L::kStages) & 1);
-            for (int j = max(0, issued - L::kStages); j < issued; ++j)
-                mbar_wait_drain(bar(L::bVFull + j % L::kStages), (j / L::kStages) & 1);
+            if (units > 0) mbar_wait_drain(bar(L::bQFull), (units - 1) & 1);
+            for (int i = max(0, k_it - L::kKStages); i < k_it; ++i)
+                mbar_wait_drain(bar(L::bKFull + i % L::kKStages), (i / L::kKStages) & 1);
+            for (int i = max(0, v_it - L::kVStages); i < v_it; ++i)
+                mbar_wait_drain(bar(L::bVFull + i % L::kVStages), (i / L::kVStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -216,55 +280,71 @@ __global__ void __launch_bounds__(192, 1)
             constexpr uint32_t idesc_s = make_idesc_f16(kTileM, kTileN, kBf16, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(kTileM, D, kBf16, false, true);
             // S = Q K^T: both operands K-major (head dim contiguous), 16 per step.
-            auto issue_s = [&](int st, uint32_t col) {
+            auto issue_s = [&](int ks, uint32_t col) {
                 const uint32_t qs = sbase + L::kQ;
-                const uint32_t ks = sbase + L::kK + st * L::kTileBytes;
+                const uint32_t kb = sbase + L::kK + ks * L::kTileBytes;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
                     mma_ss(tmem + col, smem_desc_sw128(qs + off, 16, 1024),
-                           smem_desc_sw128(ks + off, 16, 1024), idesc_s, k > 0);
+                           smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
                 }
             };
             // O += P V: P from TMEM (two bf16 per column, 8 columns per 16 keys),
             // V MN-major (head dim contiguous); 64-wide head-dim halves are
             // 16 KiB apart (leading offset), 8-key groups 1 KiB apart.
-            auto issue_pv = [&](int st, uint32_t pcol, bool acc) {
-                const uint32_t vs = sbase + L::kV + st * L::kTileBytes;
+            auto issue_pv = [&](int vs, uint32_t pcol, bool acc) {
+                const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
 #pragma unroll
                 for (int k = 0; k < kTileN / 16; ++k) {
                     mma_ts(tmem + L::kColO, tmem + pcol + k * 8,
-                           smem_desc_sw128(vs + k * 2048, L::kChunkBytes, 1024), idesc_o,
+                           smem_desc_sw128(vb + k * 2048, L::kChunkBytes, 1024), idesc_o,
                            (acc || k > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(bar(L::bQFull), 0, wc, 2) && mbar_wait(bar(L::bKFull), 0, wc, 3);
-            if (ok) {
+            // S_x goes to S buffer x&1, which held P_{x-2}: it waits for that
+            // P V product (barrier x&1 again, phase (x-2)>>1).  Every P V phase
+            // is waited here in order, so the waits stay within one phase.
+            auto issue_s_tile = [&](int x) -> bool {
+                if (!mbar_wait(bar(L::bKFull + x % L::kKStages), (x / L::kKStages) & 1, wc, 5))
+                    return false;
+                if (x >= 2 && !mbar_wait(bar(L::bPVDone + (x & 1)), ((x - 2) >> 1) & 1, wc, 6))
+                    return false;
                 tc_fence_after();
-                issue_s(0, 0);
-                mma_commit(bar(L::bSFull + 0));
-                mma_commit(bar(L::bKEmpty + 0));
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) {
-                    const int st1 = (j + 1) % L::kStages, use1 = (j + 1) / L::kStages;
-                    ok = mbar_wait(bar(L::bKFull + st1), use1 & 1, wc, 4);
-                    // S_{j+1} reuses the columns that held P_{j-1}: wait until the
-                    // P_{j-1} V_{j-1} product that reads them has retired.
-                    if (ok && j >= 1) ok = mbar_wait(bar(L::bPVDone), (j - 1) & 1, wc, 5);
+                issue_s(x % L::kKStages, (x & 1) * 128);
+                mma_commit(bar(L::bSFull + (x & 1)));
+                mma_commit(bar(L::bKEmpty + x % L::kKStages));
+                return true;
+            };
+            int t = 0, units = 0;  // tiles and live units processed by this CTA
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int u = unit_of(k, first, step);
+                if (u >= n_units) break;
+                const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv);
+                if (U.n_kv == 0) continue;
+                ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) && issue_s_tile(t);
+                if (!ok) break;
+                if (U.n_kv == 1) mma_commit(bar(L::bQEmpty));
+                for (int j = 0; j < U.n_kv; ++j, ++t) {
+                    if (j + 1 < U.n_kv) {
+                        if (!(ok = issue_s_tile(t + 1))) break;
+                        if (j + 2 == U.n_kv) mma_commit(bar(L::bQEmpty));  // last reader of Q
+                    }
+                    ok = mbar_wait(bar(L::bPReady + (t & 1)), (t >> 1) & 1, wc, 9) &&
+                         mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 10);
+                    // The unit's first P V overwrites O: the previous unit's
+                    // epilogue must have read it out.
+                    if (ok && j == 0 && units > 0) ok = mbar_wait(bar(L::bOFree), (units - 1) & 1, wc, 11);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(st1, ((j + 1) & 1) * 128);
-                    mma_commit(bar(L::bSFull + ((j + 1) & 1)));
-                    mma_commit(bar(L::bKEmpty + st1));
+                    issue_pv(t % L::kVStages, (t & 1) * 128, j > 0);
+                    mma_commit(bar(L::bPVDone + (t & 1)));
+                    mma_commit(bar(L::bVEmpty + t % L::kVStages));
                 }
-                ok = mbar_wait(bar(L::bPReady), j & 1, wc, 6) &&
-                     mbar_wait(bar(L::bVFull + j % L::kStages), (j / L::kStages) & 1, wc, 7);
                 if (!ok) break;
-                tc_fence_after();
-                issue_pv(j % L::kStages, (j & 1) * 128, j > 0);
-                mma_commit(bar(L::bPVDone));
-                mma_commit(bar(L::bVEmpty + j % L::kStages));
+                mma_commit(bar(L::bOFull));
+                ++units;
             }
             // Let every MMA issued above retire before TMEM is released.
             mma_commit(bar(L::bMmaIdle));
@@ -276,101 +356,123 @@ __global__ void __launch_bounds__(192, 1)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row of the tile == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-        const int q_idx = row0 + r;
         const float sl2 = p.scale_log2;
-        float m_used = -INFINITY;  // running max actually used as exponent base (log2 units)
-        float l = 0.f;             // running sum of P
+        int t = 0, units = 0;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const uint32_t cs = (j & 1) * 128;
-            ok = warp_wait(bar(L::bSFull + (j & 1)), (j >> 1) & 1, wc, 8);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t s[kTileN];
+        for (int k = 0; ok; ++k) {
+            const int u = unit_of(k, first, step);
+            if (u >= n_units) break;
+            const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv);
+            if (!U.live) continue;
+            const int q_idx = U.row0 + r;
+            const bool row_ok = q_idx < U.Lq;
+            io_t *orow = reinterpret_cast<io_t *>(p.o) + U.o_row0 + (int64_t)q_idx * U.o_rs;
+            if (U.n_kv == 0) {
+                // No key is visible to any row of this tile: O = 0, LSE = -inf.
+                if (row_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(t_lane + cs + c * 32, s + c * 32);
-            tmem_ld_wait_regs<kTileN>(s);
-
-            const int k0 = j * kTileN;
-            if ((k0 + kTileN > Lkv) || (p.causal && k0 + kTileN - 1 > row0)) {
-                int lim = Lkv - k0;  // columns c < lim are visible
-                if (p.causal) lim = min(lim, q_idx - k0 + 1);
-#pragma unroll
-                for (int c = 0; c < kTileN; ++c)
-                    if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+                    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                    if (p.lse) p.lse[U.lse_row0 + (int64_t)q_idx * U.lse_rs] = -INFINITY;
+                }
+                continue;
             }
-            // row max: four independent chains of 3-input max
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < kTileN; c += 8) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    mx4[u] = fmax3(mx4[u], __uint_as_float(s[c + 2 * u]),
-                                   __uint_as_float(s[c + 2 * u + 1]));
-            }
-            const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-            const float m_tile = mx * sl2;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (m_tile > m_used + kRescaleThreshold) {
-                rescale = true;
-                alpha = ex2_approx(m_used - m_tile);
-                m_used = m_tile;
-                l *= alpha;
-            }
-            const float base = (m_used == -INFINITY) ? 0.f : m_used;
-            const uint64_t sl2_2 = f2_pack(sl2, sl2), nbase_2 = f2_pack(-base, -base);
-            // P = exp2(s * scale*log2e - base), pairs packed in place into s[0..64)
-            uint64_t sum2[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int i = 0; i < kTileN / 2; ++i) {
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
-                                 sl2_2, nbase_2),
-                          x0, x1);
-                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
-                s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
-            }
-            {
-                float a0, a1;
-                f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), a0, a1);
-                l += a0 + a1;
-            }
-            tmem_st32(t_lane + cs, s);
-            tmem_st32(t_lane + cs + 32, s + 32);
-
-            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-                // O holds P_0..P_{j-1} V products; it may be rescaled only once
-                // the last of them has retired.
-                ok = warp_wait(bar(L::bPVDone), (j - 1) & 1, wc, 9);
+            float m_used = -INFINITY;  // running max used as exponent base (log2 units)
+            float l = 0.f;             // running sum of P
+            for (int j = 0; j < U.n_kv; ++j, ++t) {
+                const uint32_t cs = (t & 1) * 128;
+                ok = warp_wait(bar(L::bSFull + (t & 1)), (t >> 1) & 1, wc, 12);
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(t_lane + L::kColO + c * 32, o);
-                    tmem_ld_wait_regs<32>(o);
+                uint32_t s[kTileN];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(t_lane + L::kColO + c * 32, o);
+                for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(t_lane + cs + c * 32, s + c * 32);
+                tmem_ld_wait_regs<kTileN>(s);
+
+                const int k0 = j * kTileN;
+                if ((k0 + kTileN > U.Lkv) || (p.causal && k0 + kTileN - 1 > U.row0)) {
+                    int lim = U.Lkv - k0;  // columns c < lim are visible
+                    if (p.causal) lim = min(lim, q_idx - k0 + 1);
+#pragma unroll
+                    for (int c = 0; c < kTileN; ++c)
+                        if (c >= lim) s[c] = __float_as_uint(-INFINITY);
                 }
+                // row max: four independent chains of 3-input max
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < kTileN; c += 8) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        mx4[v] = fmax3(mx4[v], __uint_as_float(s[c + 2 * v]),
+                                       __uint_as_float(s[c + 2 * v + 1]));
+                }
+                const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+                const float m_tile = mx * sl2;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (m_tile > m_used + kRescaleThreshold) {
+                    rescale = true;
+                    alpha = ex2_approx(m_used - m_tile);
+                    m_used = m_tile;
+                    l *= alpha;
+                }
+                const float base = (m_used == -INFINITY) ? 0.f : m_used;
+                const uint64_t sl2_2 = f2_pack(sl2, sl2), nbase_2 = f2_pack(-base, -base);
+                // P = exp2(s * scale*log2e - base), pairs packed in place into s[0..64)
+                uint64_t sum2[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int i = 0; i < kTileN / 2; ++i) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                     sl2_2, nbase_2),
+                              x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+                    s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
+                }
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), a0, a1);
+                    l += a0 + a1;
+                }
+                tmem_st32(t_lane + cs, s);
+                tmem_st32(t_lane + cs + 32, s + 32);
+
+                if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                    // O holds the unit's earlier P V products; it may be rescaled
+                    // only once the last of them has retired.
+                    ok = warp_wait(bar(L::bPVDone + ((t - 1) & 1)), ((t - 1) >> 1) & 1, wc, 13);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + L::kColO + c * 32, o);
+                        tmem_ld_wait_regs<32>(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(t_lane + L::kColO + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(L::bPReady + (t & 1)));
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(L::bPReady));
-        }
-        if (ok) ok = warp_wait(bar(L::bPVDone), (n_kv - 1) & 1, wc, 10);
-        if (ok) {
+            if (!ok) break;
+            // epilogue: O / l and LSE; then O's columns are free for the next unit
+            ok = warp_wait(bar(L::bOFull), units & 1, wc, 14);
+            if (!ok) break;
             tc_fence_after();
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            const bool row_ok = q_idx < Lq;
-            io_t *orow = o_base + (int64_t)q_idx * o_rs;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(t_lane + L::kColO + c * 32, o);
                 tmem_ld_wait_regs<32>(o);
+                if (c == D / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(L::bOFree));
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -384,8 +486,9 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
             if (row_ok && p.lse)
-                p.lse[lse_row0 + (int64_t)q_idx * lse_rs] =
+                p.lse[U.lse_row0 + (int64_t)q_idx * U.lse_rs] =
                     (l > 0.f) ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+            ++units;
         }
     }
 

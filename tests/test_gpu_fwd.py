@@ -273,3 +273,22 @@ def test_validation_on_gpu(sdpa):
     with pytest.raises(sdpa.SdpaError) as e:
         sdpa.sdpa_fwd(q, q, q, o, None, 1, 1, 128, 128, 96, 0.125, 1, 0)
     assert e.value.status == 2
+
+
+# ------------------------------------------------- many units per persistent CTA
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_short_units_dense(sdpa, causal):
+    """768+ query tiles with 1-3 key tiles each: every CTA runs many units back to back."""
+    _dense_case(sdpa, 8, 32, 300, 300, 128, causal, seed=41)
+    _dense_case(sdpa, 4, 48, 260, 260, 64, causal, seed=42)
+
+
+def test_many_short_units_varlen_deterministic(sdpa):
+    lens = [129, 300, 1, 256, 257, 64, 200, 130] * 6
+    _varlen_case(sdpa, lens, lens, 16, 128, True, seed=43)
+    q, k, v, _, cu, _ = sdpa_inputs.packed(lens, lens, 16, 128, seed=44)
+    q, k, v, cu = q.cuda(), k.cuda(), v.cuda(), cu.cuda()
+    a = sdpa.attention_varlen(q, k, v, cu, cu, max(lens), max(lens), scale=0.088, causal=True)
+    b = sdpa.attention_varlen(q, k, v, cu, cu, max(lens), max(lens), scale=0.088, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
