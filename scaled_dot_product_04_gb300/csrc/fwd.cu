@@ -50,18 +50,21 @@ struct FwdLayout {
     // K and V have rings of their own: a K stage is released once S = Q K^T
     // has read it, a V stage once O += P V has, so the next loads start early.
     static constexpr int kKStages = (D == 128) ? 3 : 5;
-    static constexpr int kVStages = (D == 128) ? 3 : 4;
+    static constexpr int kVStages = (D == 128) ? 2 : 4;
+    // Q is double-buffered by unit parity so the next unit's Q arrives while
+    // the current unit still runs.
+    static constexpr int kQStages = 2;
     // cu_seqlens entries cached in shared memory (longer lists are read from
     // global memory); at d = 128 only the room left by the rings is used.
     static constexpr int kCuCap = (D == 128) ? 192 : 2048;
     static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTileBytes;
+    static constexpr int kK = kQ + kQStages * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
     static constexpr int kCu = kV + kVStages * kTileBytes;  // int32 cu_q[kCuCap], cu_kv[kCuCap]
     static constexpr int kBar = kCu + 2 * kCuCap * 4;
-    static constexpr int bQFull = 0;
-    static constexpr int bQEmpty = 1;
-    static constexpr int bKFull = 2;
+    static constexpr int bQFull = 0;   // two
+    static constexpr int bQEmpty = 2;  // two
+    static constexpr int bKFull = 4;
     static constexpr int bKEmpty = bKFull + kKStages;
     static constexpr int bVFull = bKEmpty + kKStages;
     static constexpr int bVEmpty = bVFull + kVStages;
@@ -70,15 +73,17 @@ struct FwdLayout {
     // waiter can ever be two phases away from the barrier it polls.
     static constexpr int bPReady = bSFull + 2;   // two
     static constexpr int bPVDone = bPReady + 2;  // two
-    static constexpr int bOFull = bPVDone + 2;   // a unit's last P V retired
-    static constexpr int bOFree = bOFull + 1;    // the epilogue has read O
-    static constexpr int bMmaIdle = bOFree + 1;
+    // O is double-buffered by unit parity: the epilogue of unit k overlaps
+    // the products of unit k+1.
+    static constexpr int bOFull = bPVDone + 2;   // two: a unit's last P V retired
+    static constexpr int bOFree = bOFull + 2;    // two: the epilogue has read O
+    static constexpr int bMmaIdle = bOFree + 2;
     static constexpr int kNumBars = bMmaIdle + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;  // u32[0] TMEM base, u32[1] abort flag
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kSmemAlloc = kBytes + 1024;  // slack to align the base to 1024 B
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColO = 256;
+    static constexpr uint32_t kColO = 256;  // O buffer b at kColO + b * D
 };
 
 constexpr float kLn2 = 0.693147180559945309f;
@@ -173,8 +178,10 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::bQFull), 1);
-        mbar_init(bar(L::bQEmpty), 1);
+        for (int b = 0; b < L::kQStages; ++b) {
+            mbar_init(bar(L::bQFull + b), 1);
+            mbar_init(bar(L::bQEmpty + b), 1);
+        }
         for (int s = 0; s < L::kKStages; ++s) {
             mbar_init(bar(L::bKFull + s), 1);
             mbar_init(bar(L::bKEmpty + s), 1);
@@ -189,8 +196,10 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(L::bPReady + b), kTileM);
             mbar_init(bar(L::bPVDone + b), 1);
         }
-        mbar_init(bar(L::bOFull), 1);
-        mbar_init(bar(L::bOFree), kTileM);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::bOFull + b), 1);
+            mbar_init(bar(L::bOFree + b), kTileM);
+        }
         mbar_init(bar(L::bMmaIdle), 1);
         misc[1] = 0u;
         fence_mbar_init();
@@ -236,14 +245,15 @@ __global__ void __launch_bounds__(192, 1)
                 // the previous unit's last V goes out before waiting for Q's slot
                 if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
                 v_pending = false;
-                if (units > 0 && !mbar_wait(bar(L::bQEmpty), (units - 1) & 1, wc, 1)) break;
+                const int qs = units & 1;
+                if (units > 1 && !mbar_wait(bar(L::bQEmpty + qs), ((units - 2) >> 1) & 1, wc, 1)) break;
                 const int qy = kPacked ? U.head : U.row0;
                 const int qz = kPacked ? U.tok_q0 + U.row0 : U.slice;
-                mbar_arrive_expect_tx(bar(L::bQFull), L::kTileBytes);
+                mbar_arrive_expect_tx(bar(L::bQFull + qs), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kQ + c * L::kChunkBytes, &tm_q, bar(L::bQFull), c * 64,
-                                qy, qz);
+                    tma_load_3d(sbase + L::kQ + qs * L::kTileBytes + c * L::kChunkBytes, &tm_q,
+                                bar(L::bQFull + qs), c * 64, qy, qz);
                 ++units;
                 for (int j = 0; j < U.n_kv; ++j) {
                     const int ky = kPacked ? U.head : j * kTileN;
@@ -267,7 +277,8 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (ok && v_pending) issue_v(pv_y, pv_z);
             // Every load issued must land before the CTA may exit.
-            if (units > 0) mbar_wait_drain(bar(L::bQFull), (units - 1) & 1);
+            for (int i = max(0, units - 2); i < units; ++i)
+                mbar_wait_drain(bar(L::bQFull + (i & 1)), (i >> 1) & 1);
             for (int i = max(0, k_it - L::kKStages); i < k_it; ++i)
                 mbar_wait_drain(bar(L::bKFull + i % L::kKStages), (i / L::kKStages) & 1);
             for (int i = max(0, v_it - L::kVStages); i < v_it; ++i)
@@ -280,8 +291,9 @@ __global__ void __launch_bounds__(192, 1)
             constexpr uint32_t idesc_s = make_idesc_f16(kTileM, kTileN, kBf16, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(kTileM, D, kBf16, false, true);
             // S = Q K^T: both operands K-major (head dim contiguous), 16 per step.
+            int units = 0;  // live units processed by this CTA (selects the Q buffer)
             auto issue_s = [&](int ks, uint32_t col) {
-                const uint32_t qs = sbase + L::kQ;
+                const uint32_t qs = sbase + L::kQ + (units & 1) * L::kTileBytes;
                 const uint32_t kb = sbase + L::kK + ks * L::kTileBytes;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -293,11 +305,11 @@ __global__ void __launch_bounds__(192, 1)
             // O += P V: P from TMEM (two bf16 per column, 8 columns per 16 keys),
             // V MN-major (head dim contiguous); 64-wide head-dim halves are
             // 16 KiB apart (leading offset), 8-key groups 1 KiB apart.
-            auto issue_pv = [&](int vs, uint32_t pcol, bool acc) {
+            auto issue_pv = [&](int vs, uint32_t pcol, uint32_t ocol, bool acc) {
                 const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
 #pragma unroll
                 for (int k = 0; k < kTileN / 16; ++k) {
-                    mma_ts(tmem + L::kColO, tmem + pcol + k * 8,
+                    mma_ts(tmem + ocol, tmem + pcol + k * 8,
                            smem_desc_sw128(vb + k * 2048, L::kChunkBytes, 1024), idesc_o,
                            (acc || k > 0) ? 1u : 0u);
                 }
@@ -316,34 +328,35 @@ __global__ void __launch_bounds__(192, 1)
                 mma_commit(bar(L::bKEmpty + x % L::kKStages));
                 return true;
             };
-            int t = 0, units = 0;  // tiles and live units processed by this CTA
+            int t = 0;  // tiles processed by this CTA
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int u = unit_of(k, first, step);
                 if (u >= n_units) break;
                 const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv);
                 if (U.n_kv == 0) continue;
-                ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) && issue_s_tile(t);
+                ok = mbar_wait(bar(L::bQFull + (units & 1)), (units >> 1) & 1, wc, 4) && issue_s_tile(t);
                 if (!ok) break;
-                if (U.n_kv == 1) mma_commit(bar(L::bQEmpty));
+                if (U.n_kv == 1) mma_commit(bar(L::bQEmpty + (units & 1)));
                 for (int j = 0; j < U.n_kv; ++j, ++t) {
                     if (j + 1 < U.n_kv) {
                         if (!(ok = issue_s_tile(t + 1))) break;
-                        if (j + 2 == U.n_kv) mma_commit(bar(L::bQEmpty));  // last reader of Q
+                        if (j + 2 == U.n_kv) mma_commit(bar(L::bQEmpty + (units & 1)));  // last reader of Q
                     }
                     ok = mbar_wait(bar(L::bPReady + (t & 1)), (t >> 1) & 1, wc, 9) &&
                          mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 10);
-                    // The unit's first P V overwrites O: the previous unit's
-                    // epilogue must have read it out.
-                    if (ok && j == 0 && units > 0) ok = mbar_wait(bar(L::bOFree), (units - 1) & 1, wc, 11);
+                    // The unit's first P V overwrites O buffer units&1: the epilogue
+                    // of the unit two back must have read it out.
+                    if (ok && j == 0 && units > 1)
+                        ok = mbar_wait(bar(L::bOFree + (units & 1)), ((units - 2) >> 1) & 1, wc, 11);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(t % L::kVStages, (t & 1) * 128, j > 0);
+                    issue_pv(t % L::kVStages, (t & 1) * 128, L::kColO + (units & 1) * D, j > 0);
                     mma_commit(bar(L::bPVDone + (t & 1)));
                     mma_commit(bar(L::bVEmpty + t % L::kVStages));
                 }
                 if (!ok) break;
-                mma_commit(bar(L::bOFull));
+                mma_commit(bar(L::bOFull + (units & 1)));
                 ++units;
             }
             // Let every MMA issued above retire before TMEM is released.
@@ -357,6 +370,48 @@ __global__ void __launch_bounds__(192, 1)
         const int r = quad * 32 + lane;  // row of the tile == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
         const float sl2 = p.scale_log2;
+        // A unit's epilogue (O / l, LSE) is deferred until the next unit's
+        // first P is out, so the MMA warp has work while O is written.
+        struct Pending {
+            bool on;
+            bool row_ok;
+            int unit;
+            float l, m;
+            io_t *orow;
+            float *lse;
+        } pend{false, false, 0, 0.f, 0.f, nullptr, nullptr};
+        auto epilogue = [&]() -> bool {
+            const int ob = pend.unit & 1;
+            if (!warp_wait(bar(L::bOFull + ob), (pend.unit >> 1) & 1, wc, 14)) return false;
+            tc_fence_after();
+            const float inv_l = (pend.l > 0.f) ? 1.f / pend.l : 0.f;
+            const uint32_t ocol = L::kColO + ob * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(t_lane + ocol + c * 32, o);
+                tmem_ld_wait_regs<32>(o);
+                if (c == D / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(L::bOFree + ob));
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                         __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (pend.row_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(pend.orow + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (pend.row_ok && pend.lse)
+                *pend.lse = (pend.l > 0.f) ? (pend.m + lg2_approx(pend.l)) * kLn2 : -INFINITY;
+            pend.on = false;
+            return true;
+        };
         int t = 0, units = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -367,16 +422,18 @@ __global__ void __launch_bounds__(192, 1)
             const int q_idx = U.row0 + r;
             const bool row_ok = q_idx < U.Lq;
             io_t *orow = reinterpret_cast<io_t *>(p.o) + U.o_row0 + (int64_t)q_idx * U.o_rs;
+            float *lse_ptr = p.lse ? p.lse + U.lse_row0 + (int64_t)q_idx * U.lse_rs : nullptr;
             if (U.n_kv == 0) {
                 // No key is visible to any row of this tile: O = 0, LSE = -inf.
                 if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
                     for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-                    if (p.lse) p.lse[U.lse_row0 + (int64_t)q_idx * U.lse_rs] = -INFINITY;
+                    if (lse_ptr) *lse_ptr = -INFINITY;
                 }
                 continue;
             }
+            const uint32_t ocol = L::kColO + (units & 1) * D;
             float m_used = -INFINITY;  // running max used as exponent base (log2 units)
             float l = 0.f;             // running sum of P
             for (int j = 0; j < U.n_kv; ++j, ++t) {
@@ -447,49 +504,24 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(t_lane + L::kColO + c * 32, o);
+                        tmem_ld32(t_lane + ocol + c * 32, o);
                         tmem_ld_wait_regs<32>(o);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(t_lane + L::kColO + c * 32, o);
+                        tmem_st32(t_lane + ocol + c * 32, o);
                     }
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(L::bPReady + (t & 1)));
+                // the previous unit's epilogue, now that this unit's first P is out
+                if (j == 0 && pend.on && !(ok = epilogue())) break;
             }
             if (!ok) break;
-            // epilogue: O / l and LSE; then O's columns are free for the next unit
-            ok = warp_wait(bar(L::bOFull), units & 1, wc, 14);
-            if (!ok) break;
-            tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(t_lane + L::kColO + c * 32, o);
-                tmem_ld_wait_regs<32>(o);
-                if (c == D / 32 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar(L::bOFree));
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
-                                         __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                }
-            }
-            if (row_ok && p.lse)
-                p.lse[U.lse_row0 + (int64_t)q_idx * U.lse_rs] =
-                    (l > 0.f) ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+            pend = Pending{true, row_ok, units, l, m_used, orow, lse_ptr};
             ++units;
         }
+        if (ok && pend.on) epilogue();
     }
 
     tc_fence_before();
