@@ -205,6 +205,17 @@ int sdpa_check_device_error(sdpa_stream_t stream);
  */
 void sdpa_set_kernel_timer(void *start_event, void *stop_event);
 
+/*
+ * Forward kernel choice for later calls on this host thread (a tuning and
+ * testing hook; no counterpart on the pages).  0 (default): automatic -- the
+ * two-tile kernel (256 query rows per work unit, two softmax warpgroups
+ * ping-ponging on the tensor core) for dense d = 128 problems with s_q and
+ * s_kv >= 2048, the one-tile kernel (128 rows per unit) otherwise.  1: always
+ * one-tile.  2: always two-tile.  Both compute the same result to rounding.
+ * Returns SDPA_ERR_INVALID_ARG for other values.
+ */
+int sdpa_set_forward_variant(int variant);
+
 /* Library version string, e.g. "sdpa_gb300 0.1 sm_103a". */
 const char *sdpa_version(void);
 

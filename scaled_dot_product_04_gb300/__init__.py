@@ -14,13 +14,13 @@ import math
 
 from ._lib import (SDPA_BF16, SDPA_FP16, SdpaError, dtype_code, load, sdpa_bwd,  # noqa: F401
                    sdpa_bwd_noalloc, sdpa_bwd_workspace_size, sdpa_check_device_error, sdpa_fwd, sdpa_last_error,
-                   sdpa_set_kernel_timer, sdpa_varlen_bwd, sdpa_varlen_bwd_workspace_size,
+                   sdpa_set_forward_variant, sdpa_set_kernel_timer, sdpa_varlen_bwd, sdpa_varlen_bwd_workspace_size,
                    sdpa_varlen_fwd, sdpa_version)
 
 __all__ = ["attention", "attention_varlen", "attention_bwd", "attention_varlen_bwd",
            "sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd", "sdpa_bwd_noalloc",
            "sdpa_bwd_workspace_size", "sdpa_varlen_bwd_workspace_size", "sdpa_last_error",
-           "sdpa_check_device_error", "sdpa_set_kernel_timer", "sdpa_version", "SdpaError",
+           "sdpa_check_device_error", "sdpa_set_forward_variant", "sdpa_set_kernel_timer", "sdpa_version", "SdpaError",
            "load"]
 
 

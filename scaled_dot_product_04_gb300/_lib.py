@@ -31,7 +31,8 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
 EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd",
            "sdpa_varlen_bwd_workspace_size", "sdpa_varlen_bwd", "sdpa_bwd_noalloc",
            "sdpa_last_error",
-           "sdpa_check_device_error", "sdpa_set_kernel_timer", "sdpa_version")
+           "sdpa_check_device_error", "sdpa_set_forward_variant", "sdpa_set_kernel_timer",
+           "sdpa_version")
 
 
 class SdpaError(RuntimeError):
@@ -80,6 +81,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sdpa_last_error.restype = ctypes.c_char_p
         lib.sdpa_check_device_error.argtypes = [_P]
         lib.sdpa_version.restype = ctypes.c_char_p
+        lib.sdpa_set_forward_variant.argtypes = [_I]
+        lib.sdpa_set_forward_variant.restype = _I
         lib.sdpa_set_kernel_timer.argtypes = [_P, _P]
         lib.sdpa_set_kernel_timer.restype = None
         for name in ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
@@ -184,6 +187,11 @@ def sdpa_set_kernel_timer(start_event=None, stop_event=None) -> None:
             ev.record()
         return ev.cuda_event
     load().sdpa_set_kernel_timer(handle(start_event), handle(stop_event))
+
+
+def sdpa_set_forward_variant(variant: int) -> None:
+    """0: automatic forward kernel choice, 1: one-tile kernel, 2: two-tile kernel."""
+    _check(load().sdpa_set_forward_variant(int(variant)))
 
 
 def sdpa_version() -> str:

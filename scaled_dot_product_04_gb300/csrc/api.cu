@@ -25,6 +25,16 @@ __device__ uint32_t g_error_word;
 
 thread_local std::string t_last_error;
 thread_local KernelTimer t_timer;
+thread_local int t_fwd_variant = 0;  // 0 auto, 1 one-tile, 2 two-tile
+
+// Forward kernel choice.  The two-tile kernel (256 query rows per unit, two
+// softmax warpgroups) wins when every unit visits many key tiles; short or
+// packed problems do better with the one-tile kernel's 128-row units.
+bool use_pair_kernel(bool packed, int d, int64_t rows_q, int64_t rows_kv) {
+    if (t_fwd_variant == 1) return false;
+    if (t_fwd_variant == 2) return true;
+    return !packed && d == 128 && rows_q >= 2048 && rows_kv >= 2048;
+}
 
 int fail(int status, const char *fmt, ...) {
     char buf[512];
@@ -215,6 +225,13 @@ const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
 const char *sdpa_version(void) { return "sdpa_gb300 0.1 sm_103a"; }
 
+int sdpa_set_forward_variant(int variant) {
+    if (variant < 0 || variant > 2)
+        return fail(SDPA_ERR_INVALID_ARG, "forward variant %d (0 auto, 1 one-tile, 2 two-tile)", variant);
+    t_fwd_variant = variant;
+    return ok();
+}
+
 void sdpa_set_kernel_timer(void *start_event, void *stop_event) {
     t_timer.start = static_cast<cudaEvent_t>(start_event);
     t_timer.stop = static_cast<cudaEvent_t>(stop_event);
@@ -245,7 +262,9 @@ int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
         return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d h=%d s_q=%d s_kv=%d)", b, h, s_q, s_kv);
     const int64_t bh = (int64_t)b * h;
     if (bh == 0 || s_q == 0) return ok();
-    const int64_t q_tiles = (s_q + kTileM - 1) / kTileM;
+    const bool pair = use_pair_kernel(false, d, s_q, s_kv);
+    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
+    const int64_t q_tiles = (s_q + unit_rows - 1) / unit_rows;
     if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
     const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh * s_kv * d * 2;
@@ -272,8 +291,10 @@ int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     p.n_units = (int)(q_tiles * bh);
     p.causal = causal;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, false, std::min(p.n_units, dev->sm_count),
-                                    static_cast<cudaStream_t>(stream), t_timer),
+    const int grid = std::min(p.n_units, dev->sm_count);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer)
+                              : launch_fwd(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer),
                          "sdpa_fwd");
 }
 
@@ -306,7 +327,9 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;
+    const bool pair = use_pair_kernel(true, d, max_seqlen_q, max_seqlen_kv);
+    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
+    const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
     const int64_t slices = (int64_t)num_seqs * h;
     if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
@@ -337,8 +360,10 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
     p.n_units = (int)(q_tiles * slices);
     p.causal = causal;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_fwd(tq, tk, tv, p, d, bf16, true, std::min(p.n_units, dev->sm_count),
-                                    static_cast<cudaStream_t>(stream), t_timer),
+    const int grid = std::min(p.n_units, dev->sm_count);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer)
+                              : launch_fwd(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer),
                          "sdpa_varlen_fwd");
 }
 

@@ -32,7 +32,8 @@ struct FwdParams {
     int h;
     int s_q, s_kv;               // dense lengths
     int num_seqs;                // packed
-    int q_tiles;                 // dense: ceil(s_q/128); packed: ceil(max_seqlen_q/128)
+    int q_tiles;                 // row blocks per slice (128 rows, or 256 for the
+                                 // two-tile kernel): dense from s_q, packed from max_seqlen_q
     int n_units;                 // q_tiles * bh (units a persistent CTA may visit)
     int causal;
     float scale_log2;            // attn_scale * log2(e)
@@ -63,6 +64,12 @@ struct KernelTimer {
     cudaEvent_t start = nullptr, stop = nullptr;
 };
 
+// Two-tile forward (fwd_pair.cu): 256 query rows per unit; q_tiles / n_units
+// then count 256-row blocks.
+int fwd_pair_rows();
+cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const FwdParams &p, int d, bool bf16, bool packed, int grid,
+                            cudaStream_t stream, const KernelTimer &timer);
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
                        cudaStream_t stream, const KernelTimer &timer);

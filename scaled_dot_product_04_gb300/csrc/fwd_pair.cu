@@ -1,0 +1,561 @@
+// Fused attention forward, two-tile variant: each work unit is 256 query rows
+// held as two 128-row tiles A and B that share every K/V tile, so the MMA
+// warp can run one tile's products while the other tile's softmax works.
+// Same operation, mask, statistics and layouts as fwd.cu ("Inside NVIDIA's
+// cuDNN Graph API" (tradepoint.io), section 5; cudnn-frontend PR #554 notes
+// on scale_softmax_log2, LSE layouts, persistent scheduling and the packed
+// total clamp); the host picks this kernel for long dense d = 128 problems,
+// where every unit visits many key tiles.
+//
+// Roles inside a CTA (12 warps):
+//   warp 0       TMA producer: Q_A, Q_B of each unit, then K_j and V_j into
+//                two rings (V one tile behind K);
+//   warp 1       MMA issuer (one thread).  Per key tile j it issues
+//                O_A += P_A(j) V_j, S_A(j+1) = Q_A K_{j+1}^T,
+//                O_B += P_B(j) V_j, S_B(j+1) = Q_B K_{j+1}^T.
+//                Each S follows its own tile's P V, so the two chains run half
+//                a period apart and each softmax is covered by two products
+//                of the other tile (and the two softmaxes do not contend for
+//                the exponent unit at the same time);
+//   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B (thread r
+//                owns row r = TMEM lane r), as in fwd.cu.
+// TMEM columns: S_A 0, S_B 128, O_A 256, O_B 256 + d.  S_X(j+1) is issued only
+// after O_X += P_X(j) V_j has retired (P_X lives in the S_X columns), so when
+// the softmax sees S_X(j+1), O_X holds every earlier product and may be
+// rescaled without further waiting.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sdpa {
+namespace {
+
+constexpr int kPairThreads = 384;
+constexpr int kPairRows = 2 * kTileM;  // query rows per work unit
+
+template <int D>
+struct PairLayout {
+    static constexpr int kChunks = D / 64;            // 128-byte swizzle columns per row
+    static constexpr int kChunkBytes = kTileM * 128;  // 16 KiB: 128 rows x 64 elements
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kKStages = (D == 128) ? 3 : 5;
+    static constexpr int kVStages = (D == 128) ? 2 : 4;
+    static constexpr int kCuCap = (D == 128) ? 192 : 2048;  // cu_seqlens entries cached
+    static constexpr int kQ = 0;                             // Q_A, Q_B
+    static constexpr int kK = kQ + 2 * kTileBytes;
+    static constexpr int kV = kK + kKStages * kTileBytes;
+    static constexpr int kCu = kV + kVStages * kTileBytes;  // int32 cu_q[kCuCap], cu_kv[kCuCap]
+    static constexpr int kBar = kCu + 2 * kCuCap * 4;
+    static constexpr int bQFull = 0;
+    static constexpr int bQEmpty = 1;
+    static constexpr int bKFull = 2;
+    static constexpr int bKEmpty = bKFull + kKStages;
+    static constexpr int bVFull = bKEmpty + kKStages;
+    static constexpr int bVEmpty = bVFull + kVStages;
+    // per tile X in {A, B}: index + X
+    static constexpr int bSFull = bVEmpty + kVStages;
+    static constexpr int bPReady = bSFull + 2;
+    static constexpr int bPVDone = bPReady + 2;
+    static constexpr int bOFull = bPVDone + 2;
+    static constexpr int bOFree = bOFull + 2;
+    static constexpr int bMmaIdle = bOFree + 2;
+    static constexpr int kNumBars = bMmaIdle + 1;
+    static constexpr int kMisc = kBar + kNumBars * 8;  // u32[0] TMEM base, u32[1] abort flag
+    static constexpr int kBytes = kMisc + 16;
+    static constexpr int kSmemAlloc = kBytes + 1024;  // slack to align the base to 1024 B
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;    // S_X at kColS + X * 128
+    static constexpr uint32_t kColO = 256;  // O_X at kColO + X * D
+};
+
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by 2^8
+
+SDPA_DEV bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
+    bool ok = mbar_wait(bar, parity, w, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// k-th unit of CTA `first` out of `step`: boustrophedon walk over the
+// heaviest-first list (c, 2G-1-c, 2G+c, 4G-1-c, ...).
+SDPA_DEV int unit_of(int k, int first, int step) {
+    return k * step + ((k & 1) ? step - 1 - first : first);
+}
+
+// One work unit: rows [row0, row0 + 256) of one slice; tile A is the first
+// 128 rows, tile B the next 128.
+struct PairUnit {
+    int slice, head, Lq, Lkv, tok_q0, tok_kv0, row0;
+    int n_kv[2];  // key tiles tile A / tile B visits (0: no row, or no key)
+    bool live;    // tile A holds at least one query row
+    int64_t o_row0, o_rs, lse_row0, lse_rs;
+};
+
+template <int D, bool kPacked>
+SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const int *cu_kv) {
+    PairUnit U;
+    const int qp = p.q_tiles - 1 - u / p.bh;  // latest (heaviest) rows first
+    U.slice = u % p.bh;
+    if constexpr (!kPacked) {
+        U.head = 0;
+        U.tok_q0 = U.tok_kv0 = 0;
+        U.Lq = p.s_q;
+        U.Lkv = p.s_kv;
+        U.o_row0 = (int64_t)U.slice * p.s_q * D;
+        U.o_rs = D;
+        U.lse_row0 = (int64_t)U.slice * p.s_q;
+        U.lse_rs = 1;
+    } else {
+        const int n = U.slice / p.h;
+        U.head = U.slice % p.h;
+        U.tok_q0 = cu_q[n];
+        U.tok_kv0 = cu_kv[n];
+        U.Lq = cu_q[n + 1] - U.tok_q0;
+        U.Lkv = cu_kv[n + 1] - U.tok_kv0;
+        U.o_row0 = ((int64_t)U.tok_q0 * p.h + U.head) * D;
+        U.o_rs = (int64_t)p.h * D;
+        U.lse_row0 = (int64_t)U.tok_q0 * p.h + U.head;
+        U.lse_rs = p.h;
+    }
+    U.row0 = qp * kPairRows;
+    U.live = U.row0 < U.Lq;
+    const int kv_tiles = (U.Lkv + kTileN - 1) / kTileN;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const int r0 = U.row0 + x * kTileM;
+        int n = 0;
+        if (r0 < U.Lq) {
+            n = kv_tiles;
+            if (p.causal) n = min(n, min(r0 + kTileM - 1, U.Lq - 1) / kTileN + 1);
+        }
+        U.n_kv[x] = n;
+    }
+    return U;
+}
+
+template <int D, bool kBf16, bool kPacked>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using L = PairLayout<D>;
+    using io_t = uint16_t;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw_base);
+    auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+
+    // cu_seqlens of packed inputs, cached when they fit
+    int *cu_q_s = reinterpret_cast<int *>(smem + L::kCu);
+    int *cu_kv_s = cu_q_s + L::kCuCap;
+    const int *cu_q = p.cu_q, *cu_kv = p.cu_kv;
+    if constexpr (kPacked) {
+        if (p.num_seqs + 1 <= L::kCuCap) {
+            for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) {
+                cu_q_s[i] = p.cu_q[i];
+                cu_kv_s[i] = p.cu_kv[i];
+            }
+            cu_q = cu_q_s;
+            cu_kv = cu_kv_s;
+        }
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::bQFull), 1);
+        mbar_init(bar(L::bQEmpty), 1);
+        for (int s = 0; s < L::kKStages; ++s) {
+            mbar_init(bar(L::bKFull + s), 1);
+            mbar_init(bar(L::bKEmpty + s), 1);
+        }
+        for (int s = 0; s < L::kVStages; ++s) {
+            mbar_init(bar(L::bVFull + s), 1);
+            mbar_init(bar(L::bVEmpty + s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(L::bSFull + x), 1);
+            mbar_init(bar(L::bPReady + x), kTileM);
+            mbar_init(bar(L::bPVDone + x), 1);
+            mbar_init(bar(L::bOFull + x), 1);
+            mbar_init(bar(L::bOFree + x), kTileM);
+        }
+        mbar_init(bar(L::bMmaIdle), 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::kMisc, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const WaitCtx wc{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.err, kTagFwd};
+    const int first = blockIdx.x, step = gridDim.x, n_units = p.n_units;
+
+    if (warp == 0) {
+        // ============================================================ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            // V_x goes out one tile after K_x, so a wait for a free V stage
+            // never holds back the K load the next S products need first.
+            int k_it = 0, v_it = 0, units = 0;
+            int pv_y = 0, pv_z = 0;
+            bool v_pending = false, ok = true;
+            auto issue_v = [&](int y, int z) -> bool {
+                const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
+                if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) return false;
+                mbar_arrive_expect_tx(bar(L::bVFull + vs), L::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
+                                bar(L::bVFull + vs), c * 64, y, z);
+                ++v_it;
+                return true;
+            };
+            for (int k = 0; ok; ++k) {
+                const int u = unit_of(k, first, step);
+                if (u >= n_units) break;
+                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv);
+                const int nmax = max(U.n_kv[0], U.n_kv[1]);
+                if (nmax == 0) continue;
+                // the previous unit's last V goes out before waiting for Q's slot
+                if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
+                v_pending = false;
+                if (units > 0 && !mbar_wait(bar(L::bQEmpty), (units - 1) & 1, wc, 1)) break;
+                mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTileBytes);
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int qy = kPacked ? U.head : U.row0 + x * kTileM;
+                    const int qz = kPacked ? U.tok_q0 + U.row0 + x * kTileM : U.slice;
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(sbase + L::kQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q,
+                                    bar(L::bQFull), c * 64, qy, qz);
+                }
+                ++units;
+                for (int j = 0; j < nmax; ++j) {
+                    const int ky = kPacked ? U.head : j * kTileN;
+                    const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.slice;
+                    const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
+                    if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(L::bKFull + ks), L::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
+                                    bar(L::bKFull + ks), c * 64, ky, kz);
+                    ++k_it;
+                    if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
+                    pv_y = ky;
+                    pv_z = kz;
+                    v_pending = true;
+                }
+            }
+            if (ok && v_pending) issue_v(pv_y, pv_z);
+            // Every load issued must land before the CTA may exit.
+            if (units > 0) mbar_wait_drain(bar(L::bQFull), (units - 1) & 1);
+            for (int i = max(0, k_it - L::kKStages); i < k_it; ++i)
+                mbar_wait_drain(bar(L::bKFull + i % L::kKStages), (i / L::kKStages) & 1);
+            for (int i = max(0, v_it - L::kVStages); i < v_it; ++i)
+                mbar_wait_drain(bar(L::bVFull + i % L::kVStages), (i / L::kVStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = make_idesc_f16(kTileM, kTileN, kBf16, false, false);
+            constexpr uint32_t idesc_o = make_idesc_f16(kTileM, D, kBf16, false, true);
+            // S_X = Q_X K^T: both operands K-major (head dim contiguous), 16 per step.
+            auto issue_s = [&](int x, int ks) {
+                const uint32_t qb = sbase + L::kQ + x * L::kTileBytes;
+                const uint32_t kb = sbase + L::kK + ks * L::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
+                    mma_ss(tmem + L::kColS + x * 128, smem_desc_sw128(qb + off, 16, 1024),
+                           smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                }
+            };
+            // O_X += P_X V: P from TMEM (two bf16 per column, 8 columns per 16
+            // keys), V MN-major (head dim contiguous); 64-wide head-dim halves
+            // are 16 KiB apart (leading offset), 8-key groups 1 KiB apart.
+            auto issue_pv = [&](int x, int vs, bool acc) {
+                const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < kTileN / 16; ++k) {
+                    mma_ts(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8,
+                           smem_desc_sw128(vb + k * 2048, L::kChunkBytes, 1024), idesc_o,
+                           (acc || k > 0) ? 1u : 0u);
+                }
+            };
+            // cnt[x]: products P_X V issued so far (one per tile of X); uo[x]:
+            // units in which tile X took part.  Every phase of bPVDone + x is
+            // waited here, in order, before S_X reuses its columns.
+            int t = 0, units = 0, cnt[2] = {0, 0}, uo[2] = {0, 0};
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int u = unit_of(k, first, step);
+                if (u >= n_units) break;
+                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv);
+                const int nmax = max(U.n_kv[0], U.n_kv[1]);
+                if (nmax == 0) continue;
+                ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) &&
+                     mbar_wait(bar(L::bKFull + t % L::kKStages), (t / L::kKStages) & 1, wc, 5);
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (!ok || U.n_kv[x] == 0) continue;
+                    if (cnt[x] > 0) ok = mbar_wait(bar(L::bPVDone + x), (cnt[x] - 1) & 1, wc, 6);
+                    if (!ok) continue;
+                    tc_fence_after();
+                    issue_s(x, t % L::kKStages);
+                    mma_commit(bar(L::bSFull + x));
+                }
+                if (!ok) break;
+                mma_commit(bar(L::bKEmpty + t % L::kKStages));
+                if (nmax == 1) mma_commit(bar(L::bQEmpty));
+                // Per key tile j: O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1).
+                for (int j = 0; j < nmax; ++j, ++t) {
+                    const int t1 = t + 1;
+                    bool k_next = false;  // K_{j+1} seen to have landed
+                    ok = mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 7);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (!ok || j >= U.n_kv[x]) continue;
+                        ok = mbar_wait(bar(L::bPReady + x), cnt[x] & 1, wc, 8);
+                        // the unit's first P V overwrites O_X: its previous
+                        // epilogue must have read it out
+                        if (ok && j == 0 && uo[x] > 0)
+                            ok = mbar_wait(bar(L::bOFree + x), (uo[x] - 1) & 1, wc, 9);
+                        if (!ok) continue;
+                        tc_fence_after();
+                        issue_pv(x, t % L::kVStages, j > 0);
+                        mma_commit(bar(L::bPVDone + x));
+                        ++cnt[x];
+                        if (j + 1 >= U.n_kv[x]) continue;
+                        if (!k_next) {
+                            ok = mbar_wait(bar(L::bKFull + t1 % L::kKStages), (t1 / L::kKStages) & 1,
+                                           wc, 10);
+                            k_next = true;
+                        }
+                        // S_X(j+1) overwrites the P_X(j) that O_X += P_X V reads
+                        if (ok) ok = mbar_wait(bar(L::bPVDone + x), (cnt[x] - 1) & 1, wc, 11);
+                        if (!ok) continue;
+                        tc_fence_after();
+                        issue_s(x, t1 % L::kKStages);
+                        mma_commit(bar(L::bSFull + x));
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(L::bVEmpty + t % L::kVStages));
+                    if (j + 1 < nmax) {
+                        mma_commit(bar(L::bKEmpty + t1 % L::kKStages));
+                        if (j + 2 == nmax) mma_commit(bar(L::bQEmpty));  // last reader of Q
+                    }
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (U.n_kv[x] == 0) continue;
+                    mma_commit(bar(L::bOFull + x));
+                    ++uo[x];
+                }
+                ++units;
+            }
+            // Let every MMA issued above retire before TMEM is released.
+            mma_commit(bar(L::bMmaIdle));
+            mbar_wait_drain(bar(L::bMmaIdle), 0);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ============================================================ softmax
+        const int x = (warp - 4) >> 2;  // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // row of the tile == TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t scol = L::kColS + x * 128, ocol = L::kColO + x * D;
+        const float sl2 = p.scale_log2;
+        int cnt = 0, uo = 0;  // tiles and units of this tile's chain
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int u = unit_of(k, first, step);
+            if (u >= n_units) break;
+            const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv);
+            const int row0 = U.row0 + x * kTileM;
+            if (!U.live || row0 >= U.Lq) continue;  // no row of this tile
+            const int q_idx = row0 + r;
+            const bool row_ok = q_idx < U.Lq;
+            io_t *orow = reinterpret_cast<io_t *>(p.o) + U.o_row0 + (int64_t)q_idx * U.o_rs;
+            float *lse_ptr = p.lse ? p.lse + U.lse_row0 + (int64_t)q_idx * U.lse_rs : nullptr;
+            const int n_kv = U.n_kv[x];
+            if (n_kv == 0) {
+                // No key is visible to any row of this tile: O = 0, LSE = -inf.
+                if (row_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow);
+#pragma unroll
+                    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                    if (lse_ptr) *lse_ptr = -INFINITY;
+                }
+                continue;
+            }
+            float m_used = -INFINITY;  // running max used as exponent base (log2 units)
+            float l = 0.f;             // running sum of P
+            for (int j = 0; j < n_kv; ++j, ++cnt) {
+                ok = warp_wait(bar(L::bSFull + x), cnt & 1, wc, 12);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t s[kTileN];
+#pragma unroll
+                for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(t_lane + scol + c * 32, s + c * 32);
+                tmem_ld_wait_regs<kTileN>(s);
+
+                const int k0 = j * kTileN;
+                if ((k0 + kTileN > U.Lkv) || (p.causal && k0 + kTileN - 1 > row0)) {
+                    int lim = U.Lkv - k0;  // columns c < lim are visible
+                    if (p.causal) lim = min(lim, q_idx - k0 + 1);
+#pragma unroll
+                    for (int c = 0; c < kTileN; ++c)
+                        if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+                }
+                // row max: four independent chains of 3-input max
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < kTileN; c += 8) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        mx4[v] = fmax3(mx4[v], __uint_as_float(s[c + 2 * v]),
+                                       __uint_as_float(s[c + 2 * v + 1]));
+                }
+                const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+                const float m_tile = mx * sl2;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (m_tile > m_used + kRescaleThreshold) {
+                    rescale = true;
+                    alpha = ex2_approx(m_used - m_tile);
+                    m_used = m_tile;
+                    l *= alpha;
+                }
+                const float base = (m_used == -INFINITY) ? 0.f : m_used;
+                const uint64_t sl2_2 = f2_pack(sl2, sl2), nbase_2 = f2_pack(-base, -base);
+                // P = exp2(s * scale*log2e - base), pairs packed in place into s[0..64)
+                uint64_t sum2[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int i = 0; i < kTileN / 2; ++i) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                     sl2_2, nbase_2),
+                              x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+                    s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
+                }
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), a0, a1);
+                    l += a0 + a1;
+                }
+                tmem_st32(t_lane + scol, s);
+                tmem_st32(t_lane + scol + 32, s + 32);
+
+                if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                    // S_X(j) was issued after O_X += P_X(j-1) V retired, so O_X
+                    // holds every earlier product and nothing writes it now.
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + ocol + c * 32, o);
+                        tmem_ld_wait_regs<32>(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(t_lane + ocol + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(L::bPReady + x));
+            }
+            if (!ok) break;
+            // epilogue: O / l and LSE; then O_X is free for the next unit
+            ok = warp_wait(bar(L::bOFull + x), uo & 1, wc, 14);
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(t_lane + ocol + c * 32, o);
+                tmem_ld_wait_regs<32>(o);
+                if (c == D / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(L::bOFree + x));
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                         __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (row_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (row_ok && lse_ptr) *lse_ptr = (l > 0.f) ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+            ++uo;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+template <int D, bool kBf16, bool kPacked>
+cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const FwdParams &p, int grid, cudaStream_t stream,
+                          const KernelTimer &timer) {
+    using L = PairLayout<D>;
+    auto kern = fwd_pair_kernel<D, kBf16, kPacked>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    if (timer.start) cudaEventRecord(timer.start, stream);
+    kern<<<grid, kPairThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, p);
+    e = cudaGetLastError();
+    if (timer.stop) cudaEventRecord(timer.stop, stream);
+    return e;
+}
+
+}  // namespace
+
+int fwd_pair_rows() { return kPairRows; }
+
+cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const FwdParams &p, int d, bool bf16, bool packed, int grid,
+                            cudaStream_t stream, const KernelTimer &timer) {
+#define SDPA_PAIR_CASE(D_, BF_, PK_)                                           \
+    if (d == D_ && bf16 == BF_ && packed == PK_)                               \
+        return launch_pair_t<D_, BF_, PK_>(tq, tk, tv, p, grid, stream, timer);
+    SDPA_PAIR_CASE(64, true, false)
+    SDPA_PAIR_CASE(64, true, true)
+    SDPA_PAIR_CASE(64, false, false)
+    SDPA_PAIR_CASE(64, false, true)
+    SDPA_PAIR_CASE(128, true, false)
+    SDPA_PAIR_CASE(128, true, true)
+    SDPA_PAIR_CASE(128, false, false)
+    SDPA_PAIR_CASE(128, false, true)
+#undef SDPA_PAIR_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sdpa

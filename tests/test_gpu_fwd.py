@@ -26,6 +26,14 @@ def sdpa():
     return m
 
 
+@pytest.fixture(autouse=True, params=[1, 2], ids=["one_tile", "two_tile"])
+def fwd_variant(request, sdpa):
+    """Every forward case runs on both forward kernels (128- and 256-row units)."""
+    sdpa.sdpa_set_forward_variant(request.param)
+    yield request.param
+    sdpa.sdpa_set_forward_variant(0)
+
+
 def _dense_case(sdpa, b, h, s_q, s_kv, d, causal, dtype=torch.bfloat16, seed=0, qk_mult=1.0):
     q, k, v, _ = sdpa_inputs.dense(b, h, s_q, s_kv, d, seed=seed, dtype=dtype, qk_mult=qk_mult)
     scale = 1.0 / math.sqrt(d)
