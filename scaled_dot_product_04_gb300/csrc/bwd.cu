@@ -174,10 +174,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t sbase = smem_u32(smem);
 
     // ---------------------------------------------------------------- work unit
-    // Key tiles in ascending order: under the causal mask the first key tiles
-    // see the most query tiles, so the heaviest units start first.
-    const int kt = blockIdx.x / p.bh;
-    const int slice = blockIdx.x % p.bh;
+    // Head-major order: all key tiles of one (batch, head) or (sequence, head)
+    // slice run back to back, ascending (under the causal mask the first key
+    // tiles see the most query tiles, so each slice's heaviest units start
+    // first).  The CTAs resident at any time then share a slice or two, whose
+    // fp32 dQ accumulator, Q and dO stay in L2 instead of every head's at once.
+    const int slice = blockIdx.x / p.kv_tiles;
+    const int kt = blockIdx.x % p.kv_tiles;
     int Lq, Lkv, tok_q0 = 0, tok_kv0 = 0, head = 0;
     RowMap qm, km;
     if constexpr (!kPacked) {
