@@ -39,10 +39,11 @@ BWD_FACTOR = 2.5          # backward FLOPs per forward FLOP
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 REF_PREFIX = 2048         # tokens of one head per oracle sample
 
-# DRAM bytes per launch of the dominant kernel from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel and the
-# library version the capture was taken with.  None until captured.
-TRAFFIC = {}
+# DRAM bytes per launch of the dominant kernel from one ncu capture of the
+# full workload (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel
+# and the library version the capture was taken with; any other version
+# reports null.  Source: profiles/bwd_main_dram_c5_b1h32s16384d128.md.
+TRAFFIC = {("bwd_main", "sdpa_gb300 0.2 sm_103a"): 0.81081e9 + 0.49864e9}
 
 
 def fwd_flops(w) -> float:
