@@ -17,10 +17,16 @@
 //   dP^T = V dO^T
 //   dV  += P^T dO                        (A = P^T straight from TMEM)
 //   dS^T = P^T o (dP^T - D) * scale      (bf16, written once to shared memory)
+//   dQ_t = dS K                          (A = dS^T's bytes, M-major view)
 //   dK  += dS^T Q                        (A = dS^T, K-major view)
-//   dQ_t = dS K                          (A = the same bytes, M-major view)
 //   dQacc[rows of the query tile] += dQ_t  (fp32 reductions into global memory)
 // scale is folded into dS once, so dK and dQ need no further multiply.
+//
+// Two compute warpgroups split every tile's 128 query columns in halves, so
+// each SM sub-partition has two warps on the exponentials and dS (whose
+// latencies one warp alone leaves exposed).  The MMA warp issues dQ before dK:
+// dQ shares its TMEM columns with dP at d = 128, and the dQ epilogue's read-out
+// then overlaps dK, so dP of the next tile follows without a gap.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -162,7 +168,9 @@ struct BwdLayout {
     static constexpr uint32_t kColDQ = kDQAliasDP ? kColDP : 2 * D + 256;
 };
 
-constexpr int kBwdThreads = 320;  // warps: 0 TMA, 1 MMA, 2-5 compute, 6-9 dQ epilogue
+// warps: 0 TMA, 1 MMA, 2-5 compute (queries 0-63 of a tile), 6-9 compute
+// (queries 64-127), 10-13 dQ epilogue
+constexpr int kBwdThreads = 448;
 
 template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -242,8 +250,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(bar(L::bSFull), 1);
         mbar_init(bar(L::bDPFull), 1);
-        mbar_init(bar(L::bPReady), 128);
-        mbar_init(bar(L::bDSReady), 128);
+        mbar_init(bar(L::bPReady), 256);
+        mbar_init(bar(L::bDSReady), 256);
         mbar_init(bar(L::bDVDone), 1);
         mbar_init(bar(L::bDQFull), 1);
         mbar_init(bar(L::bDQFree), 128);
@@ -296,19 +304,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 bar(L::bQFull + st), c * 64, qy, qz);
             }
             issued = i + 1;
-            // Row statistics of the query tile: LSE*log2(e) and D.  Rows past
-            // the sequence get +inf / 0 so their P (and so dS) is exactly 0.
+            // Row statistics of the query tile, negated for the fused
+            // multiply-adds: -LSE*log2(e) and -D*scale.  Rows past the
+            // sequence get -inf / 0 so their P (and so dS) is exactly 0.
             float *lse2 = stats + st * 256;
             float *dd = lse2 + 128;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int r = u * 32 + lane;
                 const int q = q0 + r;
-                float a = INFINITY, b = 0.f;
+                float a = -INFINITY, b = 0.f;
                 if (q < Lq) {
                     const int64_t idx = qm.st0 + (int64_t)q * qm.st_rs;
-                    a = p.lse[idx] * kLog2eF;
-                    b = p.delta[idx];
+                    a = -p.lse[idx] * kLog2eF;
+                    b = -p.delta[idx] * p.scale;
                 }
                 lse2[r] = a;
                 dd[r] = b;
@@ -365,13 +374,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t sQ = sbase + L::kQ + st * L::kTileBytes;
                 const int dst = i % L::kDOStages;
                 const uint32_t sDO = sbase + L::kDO + dst * L::kTileBytes;
-                // dV += P^T dO  (P^T bf16 in the S columns)
+                // dV += P^T dO.  P^T is packed two per column into the first 32
+                // columns of each compute group's 64 S^T columns.
                 ok = mbar_wait(bar(L::bPReady), i & 1, wc, 5);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 128 / 16; ++k)
-                    mma_ts(tmem + L::kColDV, tmem + L::kColS + k * 8,
+                    mma_ts(tmem + L::kColDV, tmem + L::kColS + (k >> 2) * 64 + (k & 3) * 8,
                            smem_desc_sw128(sDO + k * 2048, L::kChunkBytes, 1024), id_mn,
                            (i > 0 || k > 0) ? 1u : 0u);
                 mma_commit(bar(L::bDVDone));
@@ -386,10 +396,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     issue_kmajor(sK, sbase + L::kQ + st1 * L::kTileBytes, L::kColS);
                     mma_commit(bar(L::bSFull));
                 }
-                // dK += dS^T Q (last reader of Q_i), then dQ_i = dS K
+                // dQ_i = dS K, then dK += dS^T Q (last reader of Q_i)
                 ok = mbar_wait(bar(L::bDSReady), i & 1, wc, 8);
+                if (ok && !L::kDQAliasDP && i > 0) ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
                 if (!ok) break;
                 tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k)
+                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
+                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
+                mma_commit(bar(L::bDQFull));
 #pragma unroll
                 for (int k = 0; k < 128 / 16; ++k) {
                     const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
@@ -398,16 +414,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            (i > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(L::bQEmpty + st));
-                if (!L::kDQAliasDP && i > 0) {
-                    ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int k = 0; k < 128 / 16; ++k)
-                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
-                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
-                mma_commit(bar(L::bDQFull));
                 mma_commit(bar(L::bDSFree));
                 // dP^T_{i+1}
                 if (i + 1 < n_q) {
@@ -424,163 +430,174 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_wait_drain(bar(L::bMmaIdle), 0);
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ============================================================ compute
+        // Group g (warps 2-5 or 6-9) owns queries [64g, 64g+64) of every
+        // tile for all 128 key rows: its S^T and dP^T columns are
+        // [64g, 64g+64) of those regions, P^T goes back packed into the first
+        // 32 of its S^T columns, and dS^T into the g-th 128-byte chunk.
+        const int grp = (int)(warp - 2) >> 2;
         const int quad = warp & 3;
         const int j = quad * 32 + lane;  // key row of the tile == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t col_s = t_lane + L::kColS + grp * 64;
+        const uint32_t col_dp = t_lane + L::kColDP + grp * 64;
         const int key = k0 + j;
         const bool key_ok = key < Lkv;
-        const float sl2 = p.scale_log2;
-        const float scale = p.scale;
-        uint8_t *ds_row = smem + L::kDS + j * 128;
+        const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t scl = f2_pack(p.scale, p.scale);
+        uint8_t *ds_row = smem + L::kDS + grp * L::kChunkBytes + j * 128;
         bool ok = true;
         for (int i = 0; i < n_q; ++i) {
             const int st = i & 1;
-            const int q0 = (qt_begin + i) * kTileM;
-            const float *lse2 = stats + st * 256;
-            const float *dd = lse2 + 128;
+            const int q0 = (qt_begin + i) * kTileM + grp * 64;  // query of local column 0
+            const float *nlse2 = stats + st * 256 + grp * 64;   // -LSE*log2(e)
+            const float *nds = nlse2 + 128;                     // -D*scale
             ok = warp_wait_b(bar(L::bSFull), i & 1, wc, 12) &&
                  warp_wait_b(bar(L::bStatsFull + st), (i >> 1) & 1, wc, 13);
             if (!ok) break;
             tc_fence_after();
-            uint32_t s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + L::kColS + c * 32, s + c * 32);
-            tmem_ld_wait_regs<128>(s);
+            uint32_t s[64];
+            tmem_ld32(col_s, s);
+            tmem_ld32(col_s + 32, s + 32);
+            tmem_ld_wait_regs<64>(s);
             // visible iff key < Lkv and (not causal or query >= key); query rows
-            // past Lq carry lse2 = +inf and vanish on their own.
-            int lo = 0;  // first visible column
-            if (p.causal) lo = key - q0;
-            if (!key_ok) lo = 128;
-            // P^T in place of S^T, then packed to bf16/fp16 pairs in s[0..64):
-            // the packed copy feeds both the dV product (via TMEM) and dS.
+            // past Lq carry -LSE = -inf and vanish on their own.
+            int lo = p.causal ? key - q0 : 0;  // first visible local column
+            if (!key_ok) lo = 64;
+            uint32_t pk[32];  // P^T, packed pairs: feeds the dV product (via TMEM) and dS
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c);
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x = fmaf(__uint_as_float(s[c + e]), sl2, -lv[e]);
-                    s[c + e] = __float_as_uint((c + e >= lo) ? ex2_approx(x) : 0.f);
-                }
+            for (int c = 0; c < 64; c += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(nlse2 + c);
+                float x0, x1, x2, x3;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2,
+                                 f2_pack(l4.x, l4.y)),
+                          x0, x1);
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2,
+                                 f2_pack(l4.z, l4.w)),
+                          x2, x3);
+                const float p0 = c >= lo ? ex2_approx(x0) : 0.f;
+                const float p1 = c + 1 >= lo ? ex2_approx(x1) : 0.f;
+                const float p2 = c + 2 >= lo ? ex2_approx(x2) : 0.f;
+                const float p3 = c + 3 >= lo ? ex2_approx(x3) : 0.f;
+                pk[c / 2] = pack2<kBf16>(p0, p1);
+                pk[c / 2 + 1] = pack2<kBf16>(p2, p3);
             }
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-                s[c] = pack2<kBf16>(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-            tmem_st32(t_lane + L::kColS, s);
-            tmem_st32(t_lane + L::kColS + 32, s + 32);
+            tmem_st32(col_s, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(L::bPReady));
 
-            // dS^T = P^T o (dP^T - D) * scale  ->  shared memory (bf16, SW128)
+            // dS^T = P^T o (dP^T * scale - D * scale)  ->  shared memory (SW128)
             ok = warp_wait_b(bar(L::bDPFull), i & 1, wc, 14);
             if (ok && i > 0) ok = warp_wait_b(bar(L::bDSFree), (i - 1) & 1, wc, 15);
             if (!ok) break;
             tc_fence_after();
+            uint32_t dp[64];
+            tmem_ld32(col_dp, dp);
+            tmem_ld32(col_dp + 32, dp + 32);
+            tmem_ld_wait_regs<64>(dp);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t dp[32];
-                tmem_ld32(t_lane + L::kColDP + c * 32, dp);
-                tmem_ld_wait_regs<32>(dp);
-                uint32_t w[16];
+            for (int u = 0; u < 8; ++u) {  // 16-byte unit u of the row: queries 8u .. 8u+7
+                uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(dd + c * 32 + e);
-                    const float2 p01 = unpack2<kBf16>(s[(c * 32 + e) / 2]);
-                    const float2 p23 = unpack2<kBf16>(s[(c * 32 + e) / 2 + 1]);
-                    const float g0 = p01.x * (__uint_as_float(dp[e]) - d4.x) * scale;
-                    const float g1 = p01.y * (__uint_as_float(dp[e + 1]) - d4.y) * scale;
-                    const float g2 = p23.x * (__uint_as_float(dp[e + 2]) - d4.z) * scale;
-                    const float g3 = p23.y * (__uint_as_float(dp[e + 3]) - d4.w) * scale;
-                    w[e / 2] = pack2<kBf16>(g0, g1);
-                    w[e / 2 + 1] = pack2<kBf16>(g2, g3);
+                for (int v = 0; v < 4; ++v) {
+                    const int e = u * 8 + v * 2;
+                    const float2 nd = *reinterpret_cast<const float2 *>(nds + e);
+                    const float2 pp = unpack2<kBf16>(pk[e / 2]);
+                    const uint64_t t = f2_fma(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                              scl, f2_pack(nd.x, nd.y));
+                    float g0, g1;
+                    f2_unpack(f2_mul(f2_pack(pp.x, pp.y), t), g0, g1);
+                    w[v] = pack2<kBf16>(g0, g1);
                 }
-                // queries [32c, 32c+32): 128-byte chunk c/2, 16-byte units (c%2)*4 .. +3
-                uint8_t *chunk = ds_row + (c >> 1) * L::kChunkBytes;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int unit = (c & 1) * 4 + u;
-                    *reinterpret_cast<uint4 *>(chunk + ((unit ^ (j & 7)) << 4)) =
-                        make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                }
+                *reinterpret_cast<uint4 *>(ds_row + ((u ^ (j & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(L::bDSReady));
         }
-        // dK, dV epilogue
+        // dK, dV epilogue: group 0 writes dV, group 1 dK
         if (ok) ok = warp_wait_b(bar(L::bMmaIdle), 0, wc, 16);
         if (ok) {
             tc_fence_after();
-            uint16_t *dv_row = static_cast<uint16_t *>(p.dv) + km.io0 + (int64_t)key * km.io_rs;
-            uint16_t *dk_row = static_cast<uint16_t *>(p.dk) + km.io0 + (int64_t)key * km.io_rs;
+            const uint32_t col = grp == 0 ? L::kColDV : L::kColDK;
+            uint16_t *dst_row = static_cast<uint16_t *>(grp == 0 ? p.dv : p.dk) + km.io0 +
+                                (int64_t)key * km.io_rs;
 #pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
-                uint16_t *dst_row = which == 0 ? dv_row : dk_row;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(t_lane + col + c * 32, r);
-                    tmem_ld_wait_regs<32>(r);
-                    if (key_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_lane + col + c * 32, r);
+                tmem_ld_wait_regs<32>(r);
+                if (key_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(
-                                pack2<kBf16>(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
-                                pack2<kBf16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-                                pack2<kBf16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-                                pack2<kBf16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
-                    }
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(
+                            pack2<kBf16>(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
+                            pack2<kBf16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                            pack2<kBf16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                            pack2<kBf16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
                 }
             }
         }
     } else {
         // ============================================================ dQ epilogue
-        // Each warp owns 32 query rows (its TMEM lane quadrant).  dQ_i leaves
-        // TMEM at once (freeing the columns), then goes out in 32 x 32 fp32
-        // boxes: staged in shared memory with the 128-byte swizzle and added
-        // into the fp32 accumulator by TMA reduce-add through tm_dq, two
-        // boxes in flight per warp.  Rows past the sequence carry exact zeros
+        // Each warp owns 32 query rows (its TMEM lane quadrant).  dQ_i goes
+        // out in 32 x 32 fp32 boxes, staged in shared memory with the 128-byte
+        // swizzle and added into the fp32 accumulator by TMA reduce-add
+        // through tm_dq.  A warp has two staging boxes: columns 0-63 are
+        // staged and sent while columns 64-127 are read from TMEM, which are
+        // then freed before they are staged in turn (a warp holds at most 64
+        // of them in registers).  Rows past the sequence carry exact zeros
         // (their P is 0); rows past the accumulator are dropped by the map.
         const int quad = warp & 3;
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
         const uint32_t stage = sbase + L::kDQStage + quad * 8192;
-        uint8_t *stage_ptr = smem + L::kDQStage + quad * 8192;
+        uint8_t *stage_ptr = smem + L::kDQStage + quad * 8192 + lane * 128;
         const int acc_row0 = (int)(qm.acc0 / D);
-        int boxes = 0;
+        // one 32-column box: registers -> staging slot -> reduce-add
+        auto send = [&](const uint32_t *r, int slot, int col, int qrow) {
+            uint8_t *row = stage_ptr + slot * 4096;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4 *>(row + ((u ^ (lane & 7)) << 4)) =
+                    make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_reduce_add_2d(&tm_dq, stage + slot * 4096, col, acc_row0 + qrow);
+                bulk_commit();
+            }
+        };
         for (int i = 0; i < n_q; ++i) {
             if (!warp_wait_b(bar(L::bDQFull), i & 1, wc, 17)) break;
             tc_fence_after();
-            uint32_t r[D];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(t_lane + L::kColDQ + c * 32, r + c * 32);
-            tmem_ld_wait_regs<D>(r);
+            const int qrow0 = (qt_begin + i) * kTileM + quad * 32;
+            const bool live = qrow0 < Lq;  // any live row in this warp's quarter
+            uint32_t r[64];
+            tmem_ld32(t_lane + L::kColDQ, r);
+            if constexpr (D > 32) tmem_ld32(t_lane + L::kColDQ + 32, r + 32);
+            tmem_ld_wait_regs<(D > 32 ? 64 : 32)>(r);
+            if (live) {
+                if (lane == 0) bulk_wait_read<0>();  // both slots free again
+                __syncwarp();
+                send(r, 0, 0, qrow0);
+                if constexpr (D > 32) send(r + 32, 1, 32, qrow0);
+            }
+            if constexpr (D > 64) {
+                tmem_ld32(t_lane + L::kColDQ + 64, r);
+                tmem_ld32(t_lane + L::kColDQ + 96, r + 32);
+                tmem_ld_wait_regs<64>(r);
+            }
             tc_fence_before();
             mbar_arrive(bar(L::bDQFree));
-            const int qrow0 = (qt_begin + i) * kTileM + quad * 32;
-            if (qrow0 >= Lq) continue;  // no live row in this warp's quarter
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c, ++boxes) {
-                const int slot = boxes & 1;
-                if (boxes >= 2) {
-                    if (lane == 0) bulk_wait_read<1>();  // the slot's previous box has been read
+            if constexpr (D > 64) {
+                if (live) {
+                    if (lane == 0) bulk_wait_read<0>();
                     __syncwarp();
-                }
-                uint8_t *row = stage_ptr + slot * 4096 + lane * 128;
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<uint4 *>(row + ((u ^ (lane & 7)) << 4)) =
-                        make_uint4(r[c * 32 + 4 * u], r[c * 32 + 4 * u + 1], r[c * 32 + 4 * u + 2],
-                                   r[c * 32 + 4 * u + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_reduce_add_2d(&tm_dq, stage + slot * 4096, c * 32, acc_row0 + qrow0);
-                    bulk_commit();
+                    send(r, 0, 64, qrow0);
+                    send(r + 32, 1, 96, qrow0);
                 }
             }
         }

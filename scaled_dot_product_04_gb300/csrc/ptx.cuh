@@ -272,6 +272,11 @@ SDPA_DEV uint64_t f2_add(uint64_t x, uint64_t y) {
     asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
     return r;
 }
+SDPA_DEV uint64_t f2_mul(uint64_t x, uint64_t y) {
+    uint64_t r;
+    asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    return r;
+}
 SDPA_DEV float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
