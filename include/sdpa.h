@@ -107,11 +107,12 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o,
                     sdpa_stream_t stream);
 
 /*
- * Workspace bytes sdpa_bwd needs: an fp32 dQ accumulator [b,h,s_q,d] and the
- * fp32 row terms D_i = sum_k dO_ik O_ik [b,h,s_q] (cudnn-frontend PR #554:
- * the backward chain's "do_dot" step and its fp32 dQ accumulator), rounded
- * up for alignment.  Returns 0 for an empty problem, (size_t)-1 for invalid
- * sizes.
+ * Workspace bytes sdpa_bwd needs: an fp32 dQ accumulator [b,h,s_q,d] and
+ * 16 bytes of fp32 row terms per query row [b,h,s_q]: -LSE/scale and
+ * -D_i, D_i = sum_k dO_ik O_ik, each as a pair of tf32-exact parts
+ * (cudnn-frontend PR #554: the backward chain's "do_dot" step and its fp32
+ * dQ accumulator), each part rounded up to 256 bytes.  Returns 0 for an
+ * empty problem, (size_t)-1 for invalid sizes.
  */
 size_t sdpa_bwd_workspace_size(int b, int h, int s_q, int d);
 
@@ -163,8 +164,8 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
  * The scratch that sdpa_bwd keeps in its workspace comes instead from a
  * 32 MiB array inside the library's device image, which every GPU that
  * loads the library holds until the process exits.  Problems whose
- * sdpa_bwd_workspace_size exceeds 32 MiB (about b*h*s_q*(d+1)*4 bytes: up
- * to 65,027 rows of b*h*s_q at d = 128) are rejected with
+ * sdpa_bwd_workspace_size exceeds 32 MiB (about b*h*s_q*(d+4)*4 bytes: up
+ * to 63,550 rows of b*h*s_q at d = 128) are rejected with
  * SDPA_ERR_WORKSPACE before anything is launched.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call

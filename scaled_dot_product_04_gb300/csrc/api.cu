@@ -142,17 +142,33 @@ int packed_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int h, int64_t
     return encode_map(m, ptr, bf16, d, h, tokens, (uint64_t)d * 2, (uint64_t)h * d * 2, 1, 128);
 }
 
-// fp32 dQ accumulator [rows][d] as a 2-D map with 32 x 32 boxes (128-byte rows,
-// 128-byte swizzle) for TMA reduce-add.
+// fp32 dQ accumulator [rows][d] as a 2-D map with 16 x 32 boxes (64-byte rows,
+// 64-byte swizzle) for TMA reduce-add.
 int acc_map(CUtensorMap *m, float *acc, int d, int64_t rows) {
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)d * 4};
-    cuuint32_t box[2] = {32, 32};
+    cuuint32_t box[2] = {16, 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled (dQ accumulator) failed (%d)", (int)r);
+    return SDPA_OK;
+}
+
+// Backward row terms (four fp32 per query row, in the row order of lse) as a
+// 3-D map over [dim2][dim1][4]; a box is 128 rows of one slice or head, 16
+// bytes each, unswizzled.  Rows past the extent read as zeros.
+int rowx_map(CUtensorMap *m, float4 *rowx, uint64_t dim1, uint64_t dim2, uint32_t box1,
+             uint32_t box2) {
+    cuuint64_t dims[3] = {4, dim1, dim2};
+    cuuint64_t strides[2] = {16, (cuuint64_t)dim1 * 16};
+    cuuint32_t box[3] = {4, box1, box2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rowx, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled (row terms) failed (%d)", (int)r);
     return SDPA_OK;
 }
 
@@ -371,16 +387,16 @@ size_t sdpa_bwd_workspace_size(int b, int h, int s_q, int d) {
     if (b < 0 || h < 0 || s_q < 0 || (d != 64 && d != 128)) return (size_t)-1;
     const size_t rows = (size_t)b * h * s_q;
     if (rows == 0) return 0;
-    const size_t acc = rows * d * 4, delta = rows * 4;
-    return ((acc + 255) & ~(size_t)255) + ((delta + 255) & ~(size_t)255);
+    const size_t acc = rows * d * 4, rowx = rows * 16;
+    return ((acc + 255) & ~(size_t)255) + ((rowx + 255) & ~(size_t)255);
 }
 
 size_t sdpa_varlen_bwd_workspace_size(int total_q, int h, int d) {
     if (total_q < 0 || h < 0 || (d != 64 && d != 128)) return (size_t)-1;
     const size_t rows = (size_t)total_q * h;
     if (rows == 0) return 0;
-    const size_t acc = rows * d * 4, delta = rows * 4;
-    return ((acc + 255) & ~(size_t)255) + ((delta + 255) & ~(size_t)255);
+    const size_t acc = rows * d * 4, rowx = rows * 16;
+    return ((acc + 255) & ~(size_t)255) + ((rowx + 255) & ~(size_t)255);
 }
 
 static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -426,8 +442,6 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     if ((st = dense_map(&tk, k, bf16, d, s_kv, bh))) return st;
     if ((st = dense_map(&tv, v, bf16, d, s_kv, bh))) return st;
     if ((st = dense_map(&tdo, dout, bf16, d, s_q, bh))) return st;
-    CUtensorMap tdq;
-    if ((st = acc_map(&tdq, static_cast<float *>(workspace), d, bh * s_q))) return st;
     BwdParams p{};
     p.o = o;
     p.dout = dout;
@@ -436,8 +450,11 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     p.dk = dk;
     p.dv = dv;
     p.dq_acc = static_cast<float *>(workspace);
-    p.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+    p.rowx = reinterpret_cast<float4 *>(static_cast<char *>(workspace) +
                                         round256((size_t)bh * s_q * d * 4));
+    CUtensorMap tdq, trx;
+    if ((st = acc_map(&tdq, p.dq_acc, d, bh * s_q))) return st;
+    if ((st = rowx_map(&trx, p.rowx, s_q, bh, 128, 1))) return st;
     p.err = dev->err;
     p.bh = (int)bh;
     p.h = h;
@@ -448,7 +465,7 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     p.causal = causal;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
+    return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
 }
 
 int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -494,8 +511,6 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     if ((st = packed_map(&tk, k, bf16, d, h, total_kv))) return st;
     if ((st = packed_map(&tv, v, bf16, d, h, total_kv))) return st;
     if ((st = packed_map(&tdo, dout, bf16, d, h, total_q))) return st;
-    CUtensorMap tdq;
-    if ((st = acc_map(&tdq, static_cast<float *>(workspace), d, (int64_t)total_q * h))) return st;
     BwdParams p{};
     p.o = o;
     p.dout = dout;
@@ -504,8 +519,11 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     p.dk = dk;
     p.dv = dv;
     p.dq_acc = static_cast<float *>(workspace);
-    p.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+    p.rowx = reinterpret_cast<float4 *>(static_cast<char *>(workspace) +
                                         round256((size_t)total_q * h * d * 4));
+    CUtensorMap tdq, trx;
+    if ((st = acc_map(&tdq, p.dq_acc, d, (int64_t)total_q * h))) return st;
+    if ((st = rowx_map(&trx, p.rowx, h, total_q, 1, 128))) return st;
     p.cu_q = cu_seqlens_q;
     p.cu_kv = cu_seqlens_kv;
     p.err = dev->err;
@@ -517,7 +535,7 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     p.causal = causal;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
-    return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
+    return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
 }
 
 }  // extern "C"

@@ -4,23 +4,32 @@
 // The chain follows the backward structure cudnn-frontend PR #554 describes
 // for its SM80 kernels ("do_dot", main kernel, "dQ cast"), rebuilt for
 // tcgen05/TMEM:
-//   bwd_preprocess   D_i = sum_k dO_ik O_ik (fp32) and zeroing of the fp32 dQ
-//                    accumulator (the PR's fp32 dq accumulator);
+//   bwd_preprocess   D_i = sum_k dO_ik O_ik (fp32), the row terms below and
+//                    zeroing of the fp32 dQ accumulator (the PR's fp32 dq
+//                    accumulator);
 //   bwd_main         one CTA per (slice, 128-key tile), walking the query
 //                    tiles that can see those keys;
 //   bwd_dq_convert   fp32 accumulator -> dQ in the I/O dtype and Q's layout.
 //
 // Math per (key tile, query tile), all in the transposed orientation so the
 // key tile's rows are TMEM lanes:
-//   S^T  = K Q^T                         (tcgen05, K-major operands)
-//   P^T  = exp2(S^T * scale*log2e - LSE*log2e), masked        (registers)
-//   dP^T = V dO^T
+//   S'^T = K Q^T - LSE/scale             (tcgen05, K-major operands)
+//   P^T  = exp2(S'^T * scale*log2e), masked                   (registers)
+//   dP'^T = V dO^T - D
 //   dV  += P^T dO                        (A = P^T straight from TMEM)
-//   dS^T = P^T o (dP^T - D) * scale      (bf16, written once to shared memory)
-//   dQ_t = dS K                          (A = dS^T's bytes, M-major view)
-//   dK  += dS^T Q                        (A = dS^T, K-major view)
+//   dS'^T = P^T o dP'^T                  (bf16, written once to shared memory)
+//   dQ_t = dS' K                         (A = dS'^T's bytes, M-major view)
+//   dK  += dS'^T Q                       (A = dS'^T, K-major view)
 //   dQacc[rows of the query tile] += dQ_t  (fp32 reductions into global memory)
-// scale is folded into dS once, so dK and dQ need no further multiply.
+// dS = scale * dS', so dK and dQ take the factor once, when they are written.
+// The row terms -LSE/scale and -D enter the two products as one more K-step
+// each (kind::tf32, K = 8): the preprocess kernel stores them per query row as
+// tf32 pairs (hi, lo) that sum to the fp32 value within 2^-21 relative, the
+// producer loads the 128 rows of a query tile with the tile's Q, and a
+// constant operand of 0.5s selects the pair (LSE or D) and adds it into every
+// key row of the accumulator.  The compute warps then need no per-query
+// statistics at all: those broadcast reads from shared memory had cost as
+// many shared-memory cycles as the dS stores and the dQ staging together.
 //
 // Two compute warpgroups split every tile's 128 query columns in halves, so
 // each SM sub-partition has two warps on the exponentials and dS (whose
@@ -33,7 +42,9 @@
 namespace sdpa {
 namespace {
 
-constexpr float kLog2eF = 1.4426950408889634f;
+// x rounded to the 11 significant bits a tf32 operand keeps (x - result is
+// then exact in fp32 and is the low part of the pair).
+SDPA_DEV float tf32_hi(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
 
 SDPA_DEV bool warp_wait_b(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
     bool ok = mbar_wait(bar, parity, w, site);
@@ -42,13 +53,12 @@ SDPA_DEV bool warp_wait_b(uint32_t bar, uint32_t parity, const WaitCtx &w, uint3
 
 // -------------------------------------------------------------------- layouts
 // Row r of a problem slice in the I/O tensors and in the fp32 buffers:
-//   dense  : I/O element offset (slice*S + r)*d, stats offset slice*S + r
-//   packed : I/O element offset ((tok0 + r)*h + head)*d, stats (tok0 + r)*h + head
+//   dense  : I/O element offset (slice*S + r)*d, row-term index slice*S + r
+//   packed : I/O element offset ((tok0 + r)*h + head)*d, row terms (tok0 + r)*h + head
 // The dQ accumulator is head-major in both cases: [slices or heads][rows][d],
 // so a query tile of one head is contiguous.
 struct RowMap {
     int64_t io0, io_rs;      // I/O tensors (elements)
-    int64_t st0, st_rs;      // LSE / D
     int64_t acc0;            // dQ accumulator row 0 (elements, row stride d)
 };
 
@@ -83,7 +93,21 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
             acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (r < rows && part == 0) p.delta[r] = acc;  // stats layout == I/O row order
+        if (r < rows && part == 0) {  // row-term layout == I/O row order
+            // A row with no visible key (LSE = -inf: a sequence without keys)
+            // is masked wherever it appears, also as a tail row of another
+            // sequence's tile; its term is made finite so that the 0 * inf of
+            // the other row-term K-step cannot turn that tile's dP' into NaN.
+            float cl = -p.lse[r] / p.scale;
+            if (!isfinite(cl)) cl = 0.f;
+            const float cd = -acc;
+            float4 t;
+            t.x = tf32_hi(cl);
+            t.y = cl - t.x;
+            t.z = tf32_hi(cd);
+            t.w = cd - t.z;
+            p.rowx[r] = t;
+        }
     }
     // zero the fp32 dQ accumulator
     float4 *acc4 = reinterpret_cast<float4 *>(p.dq_acc);
@@ -114,10 +138,11 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BwdParams p, 
         const float4 *src = reinterpret_cast<const float4 *>(p.dq_acc + acc_row * D + part * 8);
         const float4 a = src[0], b = src[1];
         uint4 out;
-        out.x = pack2<kBf16>(a.x, a.y);
-        out.y = pack2<kBf16>(a.z, a.w);
-        out.z = pack2<kBf16>(b.x, b.y);
-        out.w = pack2<kBf16>(b.z, b.w);
+        const float sc = p.scale;  // the accumulator holds dS' K
+        out.x = pack2<kBf16>(a.x * sc, a.y * sc);
+        out.y = pack2<kBf16>(a.z * sc, a.w * sc);
+        out.z = pack2<kBf16>(b.x * sc, b.y * sc);
+        out.w = pack2<kBf16>(b.z * sc, b.w * sc);
         *reinterpret_cast<uint4 *>(dq + r * D + part * 8) = out;
     }
 }
@@ -137,15 +162,19 @@ struct BwdLayout {
     static constexpr int kQ = kV + kTileBytes;               // 2 stages
     static constexpr int kDO = kQ + 2 * kTileBytes;          // kDOStages stages
     static constexpr int kDS = kDO + kDOStages * kTileBytes; // 128 keys x 128 queries bf16
-    static constexpr int kDQStage = kDS + 2 * kChunkBytes;   // 4 warps x 2 boxes x 4 KiB fp32
-    static constexpr int kStats = kDQStage + 4 * 2 * 4096;   // 2 stages x (lse2[128], D[128])
-    static constexpr int kBar = kStats + 2 * 2 * 128 * 4;
+    static constexpr int kDQBoxBytes = 32 * 16 * 4;           // 32 rows x 16 fp32
+    static constexpr int kDQSlots = 3;                        // staging boxes per warp
+    static constexpr int kDQStage = kDS + 2 * kChunkBytes;   // 4 warps x kDQSlots boxes
+    static constexpr int kRowXBytes = 128 * 16;               // 128 query rows x 4 fp32
+    static constexpr int kRowX = kDQStage + 4 * kDQSlots * kDQBoxBytes;  // 2 stages, with Q
+    static constexpr int kAexS = kRowX + 2 * kRowXBytes;      // 128 rows (0.5, 0.5, 0, 0)
+    static constexpr int kAexD = kAexS + kRowXBytes;          // 128 rows (0, 0, 0.5, 0.5)
+    static constexpr int kBar = kAexD + kRowXBytes;
     // barriers
     static constexpr int bKVFull = 0;
-    static constexpr int bQFull = 1;       // 2
+    static constexpr int bQFull = 1;       // 2: Q and its row terms
     static constexpr int bDOFull = 3;      // 2
-    static constexpr int bStatsFull = 5;   // 2
-    static constexpr int bQEmpty = 7;      // 2: Q (and row stats) stage, freed after dK
+    static constexpr int bQEmpty = 7;      // 2: Q (and row terms) stage, freed after dK
     static constexpr int bDOEmpty = 18;    // kDOStages: dO stage, freed after dV
     static constexpr int bSFull = 9;
     static constexpr int bDPFull = 10;
@@ -176,7 +205,8 @@ template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_rx,
+                    const BwdParams p) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -194,8 +224,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if constexpr (!kPacked) {
         Lq = p.s_q;
         Lkv = p.s_kv;
-        qm = {(int64_t)slice * p.s_q * D, D, (int64_t)slice * p.s_q, 1, (int64_t)slice * p.s_q * D};
-        km = {(int64_t)slice * p.s_kv * D, D, 0, 0, 0};
+        qm = {(int64_t)slice * p.s_q * D, D, (int64_t)slice * p.s_q * D};
+        km = {(int64_t)slice * p.s_kv * D, D, 0};
     } else {
         const int n = slice / p.h;
         head = slice % p.h;
@@ -203,9 +233,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tok_kv0 = p.cu_kv[n];
         Lq = p.cu_q[n + 1] - tok_q0;
         Lkv = p.cu_kv[n + 1] - tok_kv0;
-        qm = {((int64_t)tok_q0 * p.h + head) * D, (int64_t)p.h * D, (int64_t)tok_q0 * p.h + head,
-              p.h, ((int64_t)head * p.total_q + tok_q0) * D};
-        km = {((int64_t)tok_kv0 * p.h + head) * D, (int64_t)p.h * D, 0, 0, 0};
+        qm = {((int64_t)tok_q0 * p.h + head) * D, (int64_t)p.h * D,
+              ((int64_t)head * p.total_q + tok_q0) * D};
+        km = {((int64_t)tok_kv0 * p.h + head) * D, (int64_t)p.h * D, 0};
     }
     const int k0 = kt * kTileN;
     if (k0 >= Lkv) return;  // packed: this sequence has fewer key tiles
@@ -237,14 +267,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         return;
     }
     auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
-    float *stats = reinterpret_cast<float *>(smem + L::kStats);  // [stage][2][128]
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::bKVFull), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(L::bQFull + s), 1);
             mbar_init(bar(L::bDOFull + s), 1);
-            mbar_init(bar(L::bStatsFull + s), 32);
             mbar_init(bar(L::bQEmpty + s), 1);
             if (s < L::kDOStages) mbar_init(bar(L::bDOEmpty + s), 1);
         }
@@ -264,6 +292,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_alloc(sbase + L::kMisc, L::kTmemCols);
         tmem_relinquish();
     }
+    if (threadIdx.x >= 128 && threadIdx.x < 256) {
+        // The constant A operands of the row-term K-steps, one 16-byte row
+        // per key (unswizzled core matrices, rows 16 bytes apart).
+        const int r = threadIdx.x - 128;
+        reinterpret_cast<float4 *>(smem + L::kAexS)[r] = make_float4(0.5f, 0.5f, 0.f, 0.f);
+        reinterpret_cast<float4 *>(smem + L::kAexD)[r] = make_float4(0.f, 0.f, 0.5f, 0.5f);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -279,6 +315,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_do);
+            tma_prefetch_desc(&tm_rx);
             mbar_arrive_expect_tx(bar(L::bKVFull), 2 * L::kTileBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
@@ -297,32 +334,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // dV_{i-kDOStages}) only by dP^T_i.
             if (use > 0 && !warp_wait_b(bar(L::bQEmpty + st), (use - 1) & 1, wc, 18)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(L::bQFull + st), L::kTileBytes);
+                mbar_arrive_expect_tx(bar(L::bQFull + st), L::kTileBytes + L::kRowXBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kQ + st * L::kTileBytes + c * L::kChunkBytes, &tm_q,
                                 bar(L::bQFull + st), c * 64, qy, qz);
+                tma_load_3d(sbase + L::kRowX + st * L::kRowXBytes, &tm_rx, bar(L::bQFull + st), 0,
+                            qy, qz);
             }
             issued = i + 1;
-            // Row statistics of the query tile, negated for the fused
-            // multiply-adds: -LSE*log2(e) and -D*scale.  Rows past the
-            // sequence get -inf / 0 so their P (and so dS) is exactly 0.
-            float *lse2 = stats + st * 256;
-            float *dd = lse2 + 128;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int r = u * 32 + lane;
-                const int q = q0 + r;
-                float a = -INFINITY, b = 0.f;
-                if (q < Lq) {
-                    const int64_t idx = qm.st0 + (int64_t)q * qm.st_rs;
-                    a = -p.lse[idx] * kLog2eF;
-                    b = -p.delta[idx] * p.scale;
-                }
-                lse2[r] = a;
-                dd[r] = b;
-            }
-            mbar_arrive(bar(L::bStatsFull + st));
             if (duse > 0 && !warp_wait_b(bar(L::bDOEmpty + dst), (duse - 1) & 1, wc, 1)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(L::bDOFull + dst), L::kTileBytes);
@@ -347,6 +367,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t id_sq = make_idesc_f16(128, 128, kBf16, false, false);
             constexpr uint32_t id_mn = make_idesc_f16(128, D, kBf16, false, true);
             constexpr uint32_t id_dq = make_idesc_f16(128, D, kBf16, true, true);
+            constexpr uint32_t id_rx = make_idesc_tf32(128, 128);
             const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
             // X^T = A B^T over the head dim (both K-major), 128 x 128
             auto issue_kmajor = [&](uint32_t a_s, uint32_t b_s, uint32_t col) {
@@ -357,16 +378,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            smem_desc_sw128(b_s + off, 16, 1024), id_sq, k > 0);
                 }
             };
+            // + the row terms of query stage `st`: A rows (0.5, 0.5, 0, 0) or
+            // (0, 0, 0.5, 0.5), B rows (hi_l, lo_l, hi_d, lo_d); both operands
+            // name their first 16-byte core matrix twice (K-direction offset
+            // 0), so the K = 8 sum is 2 * 0.5 * (hi + lo).
+            auto issue_rowterm = [&](uint32_t a_ex, int st, uint32_t col) {
+                mma_ss_tf32(tmem + col, smem_desc_plain(a_ex, 0, 128),
+                            smem_desc_plain(sbase + L::kRowX + st * L::kRowXBytes, 0, 128), id_rx, 1u);
+            };
             bool ok = mbar_wait(bar(L::bKVFull), 0, wc, 2) && mbar_wait(bar(L::bQFull), 0, wc, 3);
             if (ok) {
                 tc_fence_after();
-                issue_kmajor(sK, sbase + L::kQ, L::kColS);  // S^T_0
+                issue_kmajor(sK, sbase + L::kQ, L::kColS);  // S'^T_0
+                issue_rowterm(sbase + L::kAexS, 0, L::kColS);
                 mma_commit(bar(L::bSFull));
                 ok = mbar_wait(bar(L::bDOFull), 0, wc, 4);
             }
             if (ok) {
                 tc_fence_after();
-                issue_kmajor(sV, sbase + L::kDO, L::kColDP);  // dP^T_0
+                issue_kmajor(sV, sbase + L::kDO, L::kColDP);  // dP'^T_0
+                issue_rowterm(sbase + L::kAexD, 0, L::kColDP);
                 mma_commit(bar(L::bDPFull));
             }
             for (int i = 0; ok && i < n_q; ++i) {
@@ -394,6 +425,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_kmajor(sK, sbase + L::kQ + st1 * L::kTileBytes, L::kColS);
+                    issue_rowterm(sbase + L::kAexS, st1, L::kColS);
                     mma_commit(bar(L::bSFull));
                 }
                 // dQ_i = dS K, then dK += dS^T Q (last reader of Q_i)
@@ -423,6 +455,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_kmajor(sV, sbase + L::kDO + dst1 * L::kTileBytes, L::kColDP);
+                    issue_rowterm(sbase + L::kAexD, (i + 1) & 1, L::kColDP);
                     mma_commit(bar(L::bDPFull));
                 }
             }
@@ -445,50 +478,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int key = k0 + j;
         const bool key_ok = key < Lkv;
         const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
-        const uint64_t scl = f2_pack(p.scale, p.scale);
         uint8_t *ds_row = smem + L::kDS + grp * L::kChunkBytes + j * 128;
         bool ok = true;
         for (int i = 0; i < n_q; ++i) {
-            const int st = i & 1;
             const int q0 = (qt_begin + i) * kTileM + grp * 64;  // query of local column 0
-            const float *nlse2 = stats + st * 256 + grp * 64;   // -LSE*log2(e)
-            const float *nds = nlse2 + 128;                     // -D*scale
-            ok = warp_wait_b(bar(L::bSFull), i & 1, wc, 12) &&
-                 warp_wait_b(bar(L::bStatsFull + st), (i >> 1) & 1, wc, 13);
+            ok = warp_wait_b(bar(L::bSFull), i & 1, wc, 12);
             if (!ok) break;
             tc_fence_after();
             uint32_t s[64];
             tmem_ld32(col_s, s);
             tmem_ld32(col_s + 32, s + 32);
             tmem_ld_wait_regs<64>(s);
-            // visible iff key < Lkv and (not causal or query >= key); query rows
-            // past Lq carry -LSE = -inf and vanish on their own.
-            int lo = p.causal ? key - q0 : 0;  // first visible local column
+            // Local column c is visible iff lo <= c < hi: key < Lkv, query <
+            // Lq (rows past it carry no row terms) and, causal, query >= key.
+            int lo = p.causal ? key - q0 : 0;
             if (!key_ok) lo = 64;
+            const int hi = Lq - q0;
             uint32_t pk[32];  // P^T, packed pairs: feeds the dV product (via TMEM) and dS
+            if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 l4 = *reinterpret_cast<const float4 *>(nlse2 + c);
-                float x0, x1, x2, x3;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2,
-                                 f2_pack(l4.x, l4.y)),
-                          x0, x1);
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2,
-                                 f2_pack(l4.z, l4.w)),
-                          x2, x3);
-                const float p0 = c >= lo ? ex2_approx(x0) : 0.f;
-                const float p1 = c + 1 >= lo ? ex2_approx(x1) : 0.f;
-                const float p2 = c + 2 >= lo ? ex2_approx(x2) : 0.f;
-                const float p3 = c + 3 >= lo ? ex2_approx(x3) : 0.f;
-                pk[c / 2] = pack2<kBf16>(p0, p1);
-                pk[c / 2 + 1] = pack2<kBf16>(p2, p3);
+                for (int c = 0; c < 64; c += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2), x0, x1);
+                    pk[c / 2] = pack2<kBf16>(ex2_approx(x0), ex2_approx(x1));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_mul(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2), x0, x1);
+                    const float p0 = (c >= lo && c < hi) ? ex2_approx(x0) : 0.f;
+                    const float p1 = (c + 1 >= lo && c + 1 < hi) ? ex2_approx(x1) : 0.f;
+                    pk[c / 2] = pack2<kBf16>(p0, p1);
+                }
             }
             tmem_st32(col_s, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(L::bPReady));
 
-            // dS^T = P^T o (dP^T * scale - D * scale)  ->  shared memory (SW128)
+            // dS'^T = P^T o dP'^T  ->  shared memory (SW128)
             ok = warp_wait_b(bar(L::bDPFull), i & 1, wc, 14);
             if (ok && i > 0) ok = warp_wait_b(bar(L::bDSFree), (i - 1) & 1, wc, 15);
             if (!ok) break;
@@ -503,12 +532,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int e = u * 8 + v * 2;
-                    const float2 nd = *reinterpret_cast<const float2 *>(nds + e);
                     const float2 pp = unpack2<kBf16>(pk[e / 2]);
-                    const uint64_t t = f2_fma(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                                              scl, f2_pack(nd.x, nd.y));
                     float g0, g1;
-                    f2_unpack(f2_mul(f2_pack(pp.x, pp.y), t), g0, g1);
+                    f2_unpack(f2_mul(f2_pack(pp.x, pp.y),
+                                     f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1]))),
+                              g0, g1);
                     w[v] = pack2<kBf16>(g0, g1);
                 }
                 *reinterpret_cast<uint4 *>(ds_row + ((u ^ (j & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -524,6 +552,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t col = grp == 0 ? L::kColDV : L::kColDK;
             uint16_t *dst_row = static_cast<uint16_t *>(grp == 0 ? p.dv : p.dk) + km.io0 +
                                 (int64_t)key * km.io_rs;
+            const float f = grp == 0 ? 1.f : p.scale;  // dK = scale * sum dS'^T Q
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -531,73 +560,88 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_ld_wait_regs<32>(r);
                 if (key_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
+                    auto g = [&](int e) { return __uint_as_float(r[e]) * f; };
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(
-                            pack2<kBf16>(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
-                            pack2<kBf16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-                            pack2<kBf16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-                            pack2<kBf16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+                        dst[v] = make_uint4(pack2<kBf16>(g(8 * v), g(8 * v + 1)),
+                                            pack2<kBf16>(g(8 * v + 2), g(8 * v + 3)),
+                                            pack2<kBf16>(g(8 * v + 4), g(8 * v + 5)),
+                                            pack2<kBf16>(g(8 * v + 6), g(8 * v + 7)));
                 }
             }
         }
     } else {
         // ============================================================ dQ epilogue
         // Each warp owns 32 query rows (its TMEM lane quadrant).  dQ_i goes
-        // out in 32 x 32 fp32 boxes, staged in shared memory with the 128-byte
+        // out in 32 x 16 fp32 boxes, staged in shared memory with the 64-byte
         // swizzle and added into the fp32 accumulator by TMA reduce-add
-        // through tm_dq.  A warp has two staging boxes: columns 0-63 are
-        // staged and sent while columns 64-127 are read from TMEM, which are
-        // then freed before they are staged in turn (a warp holds at most 64
-        // of them in registers).  Rows past the sequence carry exact zeros
-        // (their P is 0); rows past the accumulator are dropped by the map.
+        // through tm_dq, kDQSlots boxes in flight per warp.  At d = 128 the
+        // first 96 columns are read from TMEM at once, the first two boxes go
+        // out, the last 32 columns take their registers and the columns are
+        // freed before the remaining six boxes are staged.  Rows past the
+        // sequence carry exact zeros (their P is 0); rows past the
+        // accumulator are dropped by the map.
         const int quad = warp & 3;
-        const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-        const uint32_t stage = sbase + L::kDQStage + quad * 8192;
-        uint8_t *stage_ptr = smem + L::kDQStage + quad * 8192 + lane * 128;
+        const uint32_t t_dq = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
+        const uint32_t stage = sbase + L::kDQStage + quad * (L::kDQSlots * L::kDQBoxBytes);
+        uint8_t *stage_ptr = smem + L::kDQStage + quad * (L::kDQSlots * L::kDQBoxBytes) + lane * 64;
         const int acc_row0 = (int)(qm.acc0 / D);
-        // one 32-column box: registers -> staging slot -> reduce-add
-        auto send = [&](const uint32_t *r, int slot, int col, int qrow) {
-            uint8_t *row = stage_ptr + slot * 4096;
+        int boxes = 0, slot = 0;  // boxes sent by this warp; slot of the next one
+        // one 32 x 16 box: registers r[0..16) -> staging slot -> reduce-add
+        auto send = [&](const uint32_t *r, int col, int qrow) {
+            if (boxes >= L::kDQSlots) {
+                if (lane == 0) bulk_wait_read<L::kDQSlots - 1>();  // the slot's last box was read
+                __syncwarp();
+            }
+            uint8_t *row = stage_ptr + slot * L::kDQBoxBytes;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                *reinterpret_cast<uint4 *>(row + ((u ^ (lane & 7)) << 4)) =
+            for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4 *>(row + ((u ^ ((lane >> 1) & 3)) << 4)) =
                     make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_reduce_add_2d(&tm_dq, stage + slot * 4096, col, acc_row0 + qrow);
+                tma_reduce_add_2d(&tm_dq, stage + slot * L::kDQBoxBytes, col, acc_row0 + qrow);
                 bulk_commit();
             }
+            ++boxes;
+            slot = slot + 1 == L::kDQSlots ? 0 : slot + 1;
         };
         for (int i = 0; i < n_q; ++i) {
             if (!warp_wait_b(bar(L::bDQFull), i & 1, wc, 17)) break;
             tc_fence_after();
             const int qrow0 = (qt_begin + i) * kTileM + quad * 32;
             const bool live = qrow0 < Lq;  // any live row in this warp's quarter
-            uint32_t r[64];
-            tmem_ld32(t_lane + L::kColDQ, r);
-            if constexpr (D > 32) tmem_ld32(t_lane + L::kColDQ + 32, r + 32);
-            tmem_ld_wait_regs<(D > 32 ? 64 : 32)>(r);
-            if (live) {
-                if (lane == 0) bulk_wait_read<0>();  // both slots free again
-                __syncwarp();
-                send(r, 0, 0, qrow0);
-                if constexpr (D > 32) send(r + 32, 1, 32, qrow0);
-            }
-            if constexpr (D > 64) {
-                tmem_ld32(t_lane + L::kColDQ + 64, r);
-                tmem_ld32(t_lane + L::kColDQ + 96, r + 32);
-                tmem_ld_wait_regs<64>(r);
-            }
-            tc_fence_before();
-            mbar_arrive(bar(L::bDQFree));
-            if constexpr (D > 64) {
+            if constexpr (D == 128) {
+                uint32_t r[96];
+                tmem_ld32(t_dq, r);
+                tmem_ld32(t_dq + 32, r + 32);
+                tmem_ld32(t_dq + 64, r + 64);
+                tmem_ld_wait_regs<96>(r);
                 if (live) {
-                    if (lane == 0) bulk_wait_read<0>();
-                    __syncwarp();
-                    send(r, 0, 64, qrow0);
-                    send(r + 32, 1, 96, qrow0);
+                    send(r, 0, qrow0);
+                    send(r + 16, 16, qrow0);
+                }
+                tmem_ld32(t_dq + 96, r);
+                tmem_ld_wait_regs<32>(r);
+                tc_fence_before();
+                mbar_arrive(bar(L::bDQFree));
+                if (live) {
+#pragma unroll
+                    for (int c = 32; c < 96; c += 16) send(r + c, c, qrow0);
+                    send(r, 96, qrow0);
+                    send(r + 16, 112, qrow0);
+                }
+            } else {
+                uint32_t r[D];
+#pragma unroll
+                for (int c = 0; c < D; c += 32) tmem_ld32(t_dq + c, r + c);
+                tmem_ld_wait_regs<D>(r);
+                tc_fence_before();
+                mbar_arrive(bar(L::bDQFree));
+                if (live) {
+#pragma unroll
+                    for (int c = 0; c < D; c += 16) send(r + c, c, qrow0);
                 }
             }
         }
@@ -615,8 +659,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool kBf16, bool kPacked>
 cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &p,
-                         cudaStream_t stream, const KernelTimer &timer) {
+                         const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &trx,
+                         const BwdParams &p, cudaStream_t stream, const KernelTimer &timer) {
     using L = BwdLayout<D>;
     const int64_t rows = kPacked ? (int64_t)p.total_q * p.h : (int64_t)p.bh * p.s_q;
     const int64_t acc_elems = rows * D;
@@ -632,7 +676,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     if (e != cudaSuccess) return e;
     const int grid = p.kv_tiles * p.bh;
     if (timer.start) cudaEventRecord(timer.start, stream);
-    kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, trx, p);
     e = cudaGetLastError();
     if (timer.stop) cudaEventRecord(timer.stop, stream);
     if (e != cudaSuccess) return e;
@@ -643,11 +687,12 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &p, int d,
-                       bool bf16, bool packed, cudaStream_t stream, const KernelTimer &timer) {
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &trx,
+                       const BwdParams &p, int d, bool bf16, bool packed, cudaStream_t stream,
+                       const KernelTimer &timer) {
 #define SDPA_BWD_CASE(D_, BF_, PK_)                                            \
     if (d == D_ && bf16 == BF_ && packed == PK_)                               \
-        return launch_bwd_t<D_, BF_, PK_>(tq, tk, tv, tdo, tdq, p, stream, timer);
+        return launch_bwd_t<D_, BF_, PK_>(tq, tk, tv, tdo, tdq, trx, p, stream, timer);
     SDPA_BWD_CASE(64, true, false)
     SDPA_BWD_CASE(64, true, true)
     SDPA_BWD_CASE(64, false, false)

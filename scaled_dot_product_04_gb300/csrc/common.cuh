@@ -44,7 +44,8 @@ struct BwdParams {
     const float *lse;            // [b,h,s_q] or [T,h]
     void *dq, *dk, *dv;          // outputs, I/O dtype
     float *dq_acc;               // fp32 [rows, h?, d] accumulator (Q layout, fp32)
-    float *delta;                // fp32 D_i, same layout as lse
+    float4 *rowx;                // per query row, same layout as lse: the row terms
+                                 // -LSE/scale and -D, each split into a tf32 pair (hi, lo)
     const int32_t *cu_q, *cu_kv;
     uint32_t *err;
     int bh, h;
@@ -73,9 +74,11 @@ cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
                        cudaStream_t stream, const KernelTimer &timer);
-// tdq: 2-D fp32 map over the dQ accumulator [rows][d], box 32 x 32, 128-byte swizzle.
+// tdq: 2-D fp32 map over the dQ accumulator [rows][d], box 16 x 32, 64-byte swizzle.
+// trx: map over the row terms (dense [b*h][s_q][4], packed [T][h][4] fp32), 128-row boxes.
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdParams &p, int d,
-                       bool bf16, bool packed, cudaStream_t stream, const KernelTimer &timer);
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &trx,
+                       const BwdParams &p, int d, bool bf16, bool packed, cudaStream_t stream,
+                       const KernelTimer &timer);
 
 }  // namespace sdpa

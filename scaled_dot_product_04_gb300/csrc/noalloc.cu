@@ -22,7 +22,7 @@
 
 namespace {
 
-// 32 MiB: enough for b*h*s_q up to 65,027 rows at d = 128 (129,055 at d = 64).
+// 32 MiB: enough for b*h*s_q up to 63,550 rows at d = 128 (123,361 at d = 64).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

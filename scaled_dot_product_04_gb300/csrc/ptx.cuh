@@ -68,8 +68,11 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // two seconds
 SDPA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = global_timer_ns();
-    while (true) {
+    // The abort flag and the clock are looked at every 16th poll only: each
+    // look is a shared-memory read that competes with the operand traffic.
+    for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) != 0u) continue;
         if (*w.abort_flag) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *w.abort_flag = 1u;
@@ -168,6 +171,16 @@ SDPA_DEV void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem desc] * B[smem desc] with tf32 operands (K = 8)
+SDPA_DEV void mma_ss_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread has
 // completed.
 SDPA_DEV void mma_commit(uint32_t bar) {
@@ -229,6 +242,17 @@ SDPA_DEV uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t s
     return d;
 }
 
+// Descriptor of a K-major operand without swizzle: 8-row x 16-byte core
+// matrices, `lbo_bytes` apart along K and `sbo_bytes` apart along M/N.
+SDPA_DEV uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    return d;
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (0 = f16,
 //   1 = bf16); bit 15/16 A/B major (0 = K-major, 1 = MN-major);
@@ -238,6 +262,12 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool bf16, b
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
            ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Same layout for kind::tf32 (A and B format 2 = tf32, both K-major).
+__host__ __device__ constexpr uint32_t make_idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ math
