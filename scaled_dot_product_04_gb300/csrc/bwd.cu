@@ -368,94 +368,103 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t id_mn = make_idesc_f16(128, D, kBf16, false, true);
             constexpr uint32_t id_dq = make_idesc_f16(128, D, kBf16, true, true);
             constexpr uint32_t id_rx = make_idesc_tf32(128, 128);
-            const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
-            // X^T = A B^T over the head dim (both K-major), 128 x 128
-            auto issue_kmajor = [&](uint32_t a_s, uint32_t b_s, uint32_t col) {
+            // Operand descriptors, built once: a descriptor's low 14 bits are
+            // the address / 16, so a tile offset is added to it directly
+            // (every address stays below 256 KiB).  K-major views step 32
+            // bytes per K-step within a 128-byte row and a 16 KiB chunk per
+            // 64 elements; MN-major views step 16 rows (2 KiB) per K-step.
+            constexpr uint32_t kChunk16 = L::kChunkBytes >> 4, kTile16 = L::kTileBytes >> 4;
+            auto kstep = [](int k) -> uint32_t { return (uint32_t)((k >> 2) * kChunk16 + (k & 3) * 2); };
+            const uint64_t dK_k = smem_desc_sw128(sbase + L::kK, 16, 1024);
+            const uint64_t dK_mn = smem_desc_sw128(sbase + L::kK, L::kChunkBytes, 1024);
+            const uint64_t dV_k = smem_desc_sw128(sbase + L::kV, 16, 1024);
+            const uint64_t dQ_k = smem_desc_sw128(sbase + L::kQ, 16, 1024);
+            const uint64_t dQ_mn = smem_desc_sw128(sbase + L::kQ, L::kChunkBytes, 1024);
+            const uint64_t dDO_k = smem_desc_sw128(sbase + L::kDO, 16, 1024);
+            const uint64_t dDO_mn = smem_desc_sw128(sbase + L::kDO, L::kChunkBytes, 1024);
+            const uint64_t dDS_k = smem_desc_sw128(sbase + L::kDS, 16, 1024);
+            const uint64_t dDS_mn = smem_desc_sw128(sbase + L::kDS, L::kChunkBytes, 1024);
+            // Row terms: A rows (0.5, 0.5, 0, 0) or (0, 0, 0.5, 0.5), B rows
+            // (hi_l, lo_l, hi_d, lo_d) of query stage st; both operands name
+            // their first 16-byte core matrix twice (K-direction offset 0), so
+            // the K = 8 sum is 2 * 0.5 * (hi + lo).
+            const uint64_t dAS = smem_desc_plain(sbase + L::kAexS, 0, 128);
+            const uint64_t dAD = smem_desc_plain(sbase + L::kAexD, 0, 128);
+            const uint64_t dRX = smem_desc_plain(sbase + L::kRowX, 0, 128);
+            constexpr uint32_t kRowX16 = L::kRowXBytes >> 4;
+            // X'^T = A B^T over the head dim (both K-major) + row term, 128 x 128
+            auto issue_kmajor = [&](uint64_t a, uint64_t b, uint64_t a_ex, int st, uint32_t col) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
-                    mma_ss(tmem + col, smem_desc_sw128(a_s + off, 16, 1024),
-                           smem_desc_sw128(b_s + off, 16, 1024), id_sq, k > 0);
-                }
-            };
-            // + the row terms of query stage `st`: A rows (0.5, 0.5, 0, 0) or
-            // (0, 0, 0.5, 0.5), B rows (hi_l, lo_l, hi_d, lo_d); both operands
-            // name their first 16-byte core matrix twice (K-direction offset
-            // 0), so the K = 8 sum is 2 * 0.5 * (hi + lo).
-            auto issue_rowterm = [&](uint32_t a_ex, int st, uint32_t col) {
-                mma_ss_tf32(tmem + col, smem_desc_plain(a_ex, 0, 128),
-                            smem_desc_plain(sbase + L::kRowX + st * L::kRowXBytes, 0, 128), id_rx, 1u);
+                for (int k = 0; k < D / 16; ++k)
+                    mma_ss(tmem + col, a + kstep(k), b + kstep(k), id_sq, k > 0);
+                mma_ss_tf32(tmem + col, a_ex, dRX + st * kRowX16, id_rx, 1u);
             };
             bool ok = mbar_wait(bar(L::bKVFull), 0, wc, 2) && mbar_wait(bar(L::bQFull), 0, wc, 3);
             if (ok) {
                 tc_fence_after();
-                issue_kmajor(sK, sbase + L::kQ, L::kColS);  // S'^T_0
-                issue_rowterm(sbase + L::kAexS, 0, L::kColS);
+                issue_kmajor(dK_k, dQ_k, dAS, 0, L::kColS);  // S'^T_0
                 mma_commit(bar(L::bSFull));
                 ok = mbar_wait(bar(L::bDOFull), 0, wc, 4);
             }
             if (ok) {
                 tc_fence_after();
-                issue_kmajor(sV, sbase + L::kDO, L::kColDP);  // dP'^T_0
-                issue_rowterm(sbase + L::kAexD, 0, L::kColDP);
+                issue_kmajor(dV_k, dDO_k, dAD, 0, L::kColDP);  // dP'^T_0
                 mma_commit(bar(L::bDPFull));
             }
             for (int i = 0; ok && i < n_q; ++i) {
                 const int st = i & 1;
-                const uint32_t sQ = sbase + L::kQ + st * L::kTileBytes;
-                const int dst = i % L::kDOStages;
-                const uint32_t sDO = sbase + L::kDO + dst * L::kTileBytes;
+                const int dst = L::kDOStages == 1 ? 0 : (i & 1);
                 // dV += P^T dO.  P^T is packed two per column into the first 32
                 // columns of each compute group's 64 S^T columns.
                 ok = mbar_wait(bar(L::bPReady), i & 1, wc, 5);
                 if (!ok) break;
                 tc_fence_after();
+                {
+                    const uint64_t b = dDO_mn + dst * kTile16;
 #pragma unroll
-                for (int k = 0; k < 128 / 16; ++k)
-                    mma_ts(tmem + L::kColDV, tmem + L::kColS + (k >> 2) * 64 + (k & 3) * 8,
-                           smem_desc_sw128(sDO + k * 2048, L::kChunkBytes, 1024), id_mn,
-                           (i > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 128 / 16; ++k)
+                        mma_ts(tmem + L::kColDV, tmem + L::kColS + (k >> 2) * 64 + (k & 3) * 8,
+                               b + k * 128, id_mn, (i > 0 || k > 0) ? 1u : 0u);
+                }
                 mma_commit(bar(L::bDVDone));
                 mma_commit(bar(L::bDOEmpty + dst));
-                // S^T_{i+1}, once the dV product has finished reading P^T_i
+                // S'^T_{i+1}, once the dV product has finished reading P^T_i
                 if (i + 1 < n_q) {
                     const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
                     ok = mbar_wait(bar(L::bQFull + st1), use1 & 1, wc, 6) &&
                          mbar_wait(bar(L::bDVDone), i & 1, wc, 7);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_kmajor(sK, sbase + L::kQ + st1 * L::kTileBytes, L::kColS);
-                    issue_rowterm(sbase + L::kAexS, st1, L::kColS);
+                    issue_kmajor(dK_k, dQ_k + st1 * kTile16, dAS, st1, L::kColS);
                     mma_commit(bar(L::bSFull));
                 }
-                // dQ_i = dS K, then dK += dS^T Q (last reader of Q_i)
+                // dQ_i = dS' K, then dK += dS'^T Q (last reader of Q_i)
                 ok = mbar_wait(bar(L::bDSReady), i & 1, wc, 8);
                 if (ok && !L::kDQAliasDP && i > 0) ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 128 / 16; ++k)
-                    mma_ss(tmem + L::kColDQ, smem_desc_sw128(sDS + k * 2048, L::kChunkBytes, 1024),
-                           smem_desc_sw128(sK + k * 2048, L::kChunkBytes, 1024), id_dq, k > 0);
+                    mma_ss(tmem + L::kColDQ, dDS_mn + k * 128, dK_mn + k * 128, id_dq, k > 0);
                 mma_commit(bar(L::bDQFull));
+                {
+                    const uint64_t b = dQ_mn + st * kTile16;
 #pragma unroll
-                for (int k = 0; k < 128 / 16; ++k) {
-                    const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
-                    mma_ss(tmem + L::kColDK, smem_desc_sw128(sDS + off, 16, 1024),
-                           smem_desc_sw128(sQ + k * 2048, L::kChunkBytes, 1024), id_mn,
-                           (i > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 128 / 16; ++k)
+                        mma_ss(tmem + L::kColDK, dDS_k + kstep(k), b + k * 128, id_mn,
+                               (i > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(L::bQEmpty + st));
                 mma_commit(bar(L::bDSFree));
-                // dP^T_{i+1}
+                // dP'^T_{i+1}
                 if (i + 1 < n_q) {
-                    const int dst1 = (i + 1) % L::kDOStages, duse1 = (i + 1) / L::kDOStages;
+                    const int dst1 = L::kDOStages == 1 ? 0 : ((i + 1) & 1);
+                    const int duse1 = (i + 1) / L::kDOStages;
                     ok = mbar_wait(bar(L::bDOFull + dst1), duse1 & 1, wc, 10);
                     if (ok && L::kDQAliasDP) ok = mbar_wait(bar(L::bDQFree), i & 1, wc, 11);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_kmajor(sV, sbase + L::kDO + dst1 * L::kTileBytes, L::kColDP);
-                    issue_rowterm(sbase + L::kAexD, (i + 1) & 1, L::kColDP);
+                    issue_kmajor(dV_k, dDO_k + dst1 * kTile16, dAD, (i + 1) & 1, L::kColDP);
                     mma_commit(bar(L::bDPFull));
                 }
             }
