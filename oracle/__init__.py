@@ -68,6 +68,19 @@ def _load():
                                                _int, _dbl, _int]
         lib.oracle_sdpa_varlen_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _ip, _ip,
                                                _int, _int, _int, _dbl, _int]
+        lib.oracle_attn_fwd_rows_ex.argtypes = [_dp, _i64, _dp, _i64, _dp, _i64, _dp, _dp,
+                                                _int, _int, _int, _dbl, _int, _int, _ip, _int]
+        lib.oracle_attn_bwd_rows_ex.argtypes = [_dp, _i64, _dp, _i64, _dp, _i64, _dp, _i64,
+                                                _dp, _dp, _dp, _int, _int, _int, _dbl, _int,
+                                                _int, _ip, _int, _ip, _int]
+        lib.oracle_sdpa_fwd_ex.argtypes = [_dp, _dp, _dp, _dp, _dp, _int, _int, _int, _int,
+                                           _int, _int, _dbl, _int, _int]
+        lib.oracle_sdpa_bwd_ex.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _int, _int, _int,
+                                           _int, _int, _int, _dbl, _int, _int]
+        lib.oracle_sdpa_varlen_fwd_ex.argtypes = [_dp, _dp, _dp, _dp, _dp, _ip, _ip, _int, _int,
+                                                  _int, _int, _dbl, _int, _int]
+        lib.oracle_sdpa_varlen_bwd_ex.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _ip, _ip,
+                                                  _int, _int, _int, _int, _dbl, _int, _int]
         lib.oracle_num_threads.restype = _int
         _lib = lib
         return lib
@@ -189,4 +202,106 @@ def attn_bwd_rows(q, k, v, dout, q_rows, kv_rows, scale: float, causal: bool):
     _load().oracle_attn_bwd_rows(_p(q), d, _p(k), d, _p(v), d, _p(dout), d, _p(dq), _p(dk),
                                  _p(dv), n_q, n_kv, d, float(scale), int(bool(causal)),
                                  _pi(q_rows), len(q_rows), _pi(kv_rows), len(kv_rows))
+    return dq, dk, dv
+
+
+# ----------------------------------------------------------------- masks, GQA
+#: mask names of the extended entry points: none, causal aligned top-left
+#: (query i sees keys j <= i) or bottom-right (j <= i + n_kv - n_q).
+MASKS = {"none": 0, "top_left": 1, "bottom_right": 2}
+
+
+def _mask(mask) -> int:
+    return MASKS[mask] if isinstance(mask, str) else int(mask)
+
+
+def sdpa_fwd_ex(q, k, v, scale: float, mask="top_left", window_left: int = -1):
+    """Dense forward with grouped key/value heads and the extended masks.
+
+    q [b,h,s_q,d]; k/v [b,h_kv,s_kv,d] with h a multiple of h_kv (query head
+    hq reads key/value head hq // (h // h_kv)).  window_left >= 0 keeps that
+    many keys left of the (aligned) diagonal visible.  -> (o, lse).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b, h, s_q, d = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    o = np.zeros((b, h, s_q, d))
+    lse = np.zeros((b, h, s_q))
+    _load().oracle_sdpa_fwd_ex(_p(q), _p(k), _p(v), _p(o), _p(lse), b, h, h_kv, s_q, s_kv, d,
+                               float(scale), _mask(mask), int(window_left))
+    return o, lse
+
+
+def sdpa_bwd_ex(q, k, v, dout, scale: float, mask="top_left", window_left: int = -1):
+    """Dense backward of sdpa_fwd_ex -> (dq [b,h,s_q,d], dk, dv [b,h_kv,s_kv,d])."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    b, h, s_q, d = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    _load().oracle_sdpa_bwd_ex(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), b, h,
+                               h_kv, s_q, s_kv, d, float(scale), _mask(mask), int(window_left))
+    return dq, dk, dv
+
+
+def sdpa_varlen_fwd_ex(q, k, v, cu_q, cu_kv, scale: float, mask="top_left",
+                       window_left: int = -1):
+    """Packed forward: q [Tq,h,d], k/v [Tkv,h_kv,d] -> (o [Tq,h,d], lse [Tq,h])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cu_q, cu_kv = _i32(cu_q), _i32(cu_kv)
+    _, h, d = q.shape
+    h_kv = k.shape[1]
+    o = np.zeros_like(q)
+    lse = np.full(q.shape[:2], np.nan)
+    _load().oracle_sdpa_varlen_fwd_ex(_p(q), _p(k), _p(v), _p(o), _p(lse), _pi(cu_q),
+                                      _pi(cu_kv), len(cu_q) - 1, h, h_kv, d, float(scale),
+                                      _mask(mask), int(window_left))
+    return o, lse
+
+
+def sdpa_varlen_bwd_ex(q, k, v, dout, cu_q, cu_kv, scale: float, mask="top_left",
+                       window_left: int = -1):
+    """Packed backward of sdpa_varlen_fwd_ex -> (dq, dk, dv) in the packed layouts."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    cu_q, cu_kv = _i32(cu_q), _i32(cu_kv)
+    _, h, d = q.shape
+    h_kv = k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    _load().oracle_sdpa_varlen_bwd_ex(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv),
+                                      _pi(cu_q), _pi(cu_kv), len(cu_q) - 1, h, h_kv, d,
+                                      float(scale), _mask(mask), int(window_left))
+    return dq, dk, dv
+
+
+def attn_fwd_rows_ex(q, k, v, rows, scale: float, mask="top_left", window_left: int = -1):
+    """One problem (q [n_q,d], k/v [n_kv,d]), listed query rows, extended masks."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    rows = _i32(rows)
+    n_q, d = q.shape
+    n_kv = k.shape[0]
+    o = np.zeros((len(rows), d))
+    lse = np.zeros(len(rows))
+    _load().oracle_attn_fwd_rows_ex(_p(q), d, _p(k), d, _p(v), d, _p(o), _p(lse), n_q, n_kv, d,
+                                    float(scale), _mask(mask), int(window_left), _pi(rows),
+                                    len(rows))
+    return o, lse
+
+
+def attn_bwd_rows_ex(q, k, v, dout, q_rows, kv_rows, scale: float, mask="top_left",
+                     window_left: int = -1):
+    """One problem; dQ of the listed query rows, dK/dV of the listed key rows."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    q_rows, kv_rows = _i32(q_rows), _i32(kv_rows)
+    n_q, d = q.shape
+    n_kv = k.shape[0]
+    dq = np.zeros((len(q_rows), d))
+    dk = np.zeros((len(kv_rows), d))
+    dv = np.zeros((len(kv_rows), d))
+    _load().oracle_attn_bwd_rows_ex(_p(q), d, _p(k), d, _p(v), d, _p(dout), d, _p(dq), _p(dk),
+                                    _p(dv), n_q, n_kv, d, float(scale), _mask(mask),
+                                    int(window_left), _pi(q_rows), len(q_rows), _pi(kv_rows),
+                                    len(kv_rows))
     return dq, dk, dv
