@@ -74,6 +74,26 @@ typedef enum {
 typedef enum { SDPA_BF16 = 0, SDPA_FP16 = 1 } sdpa_dtype;
 
 /*
+ * Masks of the extended entry points (cudnn-frontend PR #554, the `sdpa`
+ * op's is_causal, causal_bottom_right and window_left arguments).  Within one
+ * sequence of Lq queries and Lkv keys, query i sees key j iff lo_i <= j <
+ * hi_i, with delta = Lkv - Lq for SDPA_MASK_CAUSAL_BOTTOM_RIGHT and 0
+ * otherwise:
+ *   hi_i = Lkv                          for SDPA_MASK_NONE,
+ *   hi_i = min(Lkv, i + delta + 1)      for the two causal masks;
+ *   lo_i = max(0, i + delta - window_left) when window_left >= 0 (that many
+ *          keys left of the diagonal stay visible), 0 when window_left = -1.
+ * A query row that sees no key gets O = 0 and LSE = -inf and adds nothing to
+ * any gradient (bottom-right alignment with Lq > Lkv leaves the first
+ * Lq - Lkv rows so).
+ */
+typedef enum {
+    SDPA_MASK_NONE = 0,
+    SDPA_MASK_CAUSAL = 1,              /* top-left: j <= i */
+    SDPA_MASK_CAUSAL_BOTTOM_RIGHT = 2  /* j <= i + Lkv - Lq */
+} sdpa_mask;
+
+/*
  * Dense forward (BHSD).
  *   q, o : [b, h, s_q, d]   (dtype)      k, v : [b, h, s_kv, d] (dtype)
  *   lse  : [b, h, s_q] fp32, or NULL to skip writing it.
@@ -105,6 +125,33 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o,
                     int total_kv, int max_seqlen_q, int max_seqlen_kv, int h,
                     int d, float attn_scale, int causal, int dtype,
                     sdpa_stream_t stream);
+
+/*
+ * Extended dense forward: grouped key/value heads and the masks above.
+ *   q, o : [b, h, s_q, d]   k, v : [b, h_kv, s_kv, d]   lse : [b, h, s_q] or NULL
+ *   h must be a multiple of h_kv (h_kv = h: one key/value head per query
+ *   head; h_kv = 1: multi-query); query head hq reads key/value head
+ *   hq / (h / h_kv) (cudnn-frontend PR #554 GQA cases).
+ *   mask: an sdpa_mask value.  window_left: -1 (none) or >= 0.
+ * sdpa_fwd(..., causal, ...) is this call with h_kv = h, mask = causal ?
+ * SDPA_MASK_CAUSAL : SDPA_MASK_NONE and window_left = -1.
+ */
+int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                int b, int h, int h_kv, int s_q, int s_kv, int d,
+                float attn_scale, int mask, int window_left, int dtype,
+                sdpa_stream_t stream);
+
+/*
+ * Extended packed forward: as sdpa_varlen_fwd with k, v : [total_kv, h_kv, d]
+ * and the mask / window of sdpa_fwd_ex, applied per sequence with that
+ * sequence's own lengths (the bottom-right offset is Lkv(n) - Lq(n)).
+ */
+int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o,
+                       float *lse, const int32_t *cu_seqlens_q,
+                       const int32_t *cu_seqlens_kv, int num_seqs, int total_q,
+                       int total_kv, int max_seqlen_q, int max_seqlen_kv, int h,
+                       int h_kv, int d, float attn_scale, int mask,
+                       int window_left, int dtype, sdpa_stream_t stream);
 
 /*
  * Workspace bytes sdpa_bwd needs: an fp32 dQ accumulator [b,h,s_q,d] and
@@ -149,6 +196,41 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
                     int d, float attn_scale, int causal, int dtype,
                     void *workspace, size_t workspace_bytes,
                     sdpa_stream_t stream);
+
+/* Workspace bytes of the extended backward calls (the same content as
+ * sdpa_bwd's; the query-side sizes decide it, h_kv does not).
+ * deterministic must be 0 or 1; (size_t)-1 otherwise. */
+size_t sdpa_bwd_ex_workspace_size(int b, int h, int s_q, int d, int deterministic);
+size_t sdpa_varlen_bwd_ex_workspace_size(int total_q, int h, int d, int deterministic);
+
+/*
+ * Extended dense backward: the gradients of sdpa_fwd_ex with the same
+ * arguments.  dq : [b, h, s_q, d]; dk, dv : [b, h_kv, s_kv, d], each the sum
+ * over the h / h_kv query heads that share the key/value head
+ * (cudnn-frontend PR #554: "GQA reduces" in the backward chain).
+ * deterministic: 0 accumulates dQ with fp32 reductions whose order may vary
+ * between runs; 1 asks for bitwise reproducible gradients (returns
+ * SDPA_ERR_UNSUPPORTED until that variant is built).
+ */
+int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
+                const void *dout, const float *lse, void *dq, void *dk,
+                void *dv, int b, int h, int h_kv, int s_q, int s_kv, int d,
+                float attn_scale, int mask, int window_left, int deterministic,
+                int dtype, void *workspace, size_t workspace_bytes,
+                sdpa_stream_t stream);
+
+/* Extended packed backward: sdpa_varlen_bwd with the arguments of
+ * sdpa_varlen_fwd_ex and sdpa_bwd_ex. */
+int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v,
+                       const void *o, const void *dout, const float *lse,
+                       void *dq, void *dk, void *dv,
+                       const int32_t *cu_seqlens_q,
+                       const int32_t *cu_seqlens_kv, int num_seqs,
+                       int total_q, int total_kv, int max_seqlen_q,
+                       int max_seqlen_kv, int h, int h_kv, int d,
+                       float attn_scale, int mask, int window_left,
+                       int deterministic, int dtype, void *workspace,
+                       size_t workspace_bytes, sdpa_stream_t stream);
 
 /*
  * Dense backward that allocates nothing and takes no workspace (the pages

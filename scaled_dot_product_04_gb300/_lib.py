@@ -22,15 +22,19 @@ SDPA_ERR_CUDA = 5
 SDPA_ERR_TIMEOUT = 6
 SDPA_BF16 = 0
 SDPA_FP16 = 1
+SDPA_MASK_NONE = 0
+SDPA_MASK_CAUSAL = 1
+SDPA_MASK_CAUSAL_BOTTOM_RIGHT = 2
 
 STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED",
                 3: "SDPA_ERR_MISALIGNED", 4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA",
                 6: "SDPA_ERR_TIMEOUT"}
 
 # Exported symbols, in the order include/sdpa.h declares them.
-EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd",
-           "sdpa_varlen_bwd_workspace_size", "sdpa_varlen_bwd", "sdpa_bwd_noalloc",
-           "sdpa_last_error",
+EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_fwd_ex", "sdpa_varlen_fwd_ex",
+           "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_varlen_bwd_workspace_size",
+           "sdpa_varlen_bwd", "sdpa_bwd_ex_workspace_size", "sdpa_varlen_bwd_ex_workspace_size",
+           "sdpa_bwd_ex", "sdpa_varlen_bwd_ex", "sdpa_bwd_noalloc", "sdpa_last_error",
            "sdpa_check_device_error", "sdpa_set_forward_variant", "sdpa_set_kernel_timer",
            "sdpa_version")
 
@@ -68,6 +72,17 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sdpa_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]
         lib.sdpa_varlen_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                         _F, _I, _I, _P]
+        lib.sdpa_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]
+        lib.sdpa_varlen_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                           _I, _F, _I, _I, _I, _P]
+        lib.sdpa_bwd_ex_workspace_size.argtypes = [_I, _I, _I, _I, _I]
+        lib.sdpa_bwd_ex_workspace_size.restype = _Z
+        lib.sdpa_varlen_bwd_ex_workspace_size.argtypes = [_I, _I, _I, _I]
+        lib.sdpa_varlen_bwd_ex_workspace_size.restype = _Z
+        lib.sdpa_bwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                    _F, _I, _I, _I, _I, _P, _Z, _P]
+        lib.sdpa_varlen_bwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
+                                           _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _P, _Z, _P]
         lib.sdpa_bwd_workspace_size.argtypes = [_I, _I, _I, _I]
         lib.sdpa_bwd_workspace_size.restype = _Z
         lib.sdpa_varlen_bwd_workspace_size.argtypes = [_I, _I, _I]
@@ -86,6 +101,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sdpa_set_kernel_timer.argtypes = [_P, _P]
         lib.sdpa_set_kernel_timer.restype = None
         for name in ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
+                     "sdpa_fwd_ex", "sdpa_varlen_fwd_ex", "sdpa_bwd_ex", "sdpa_varlen_bwd_ex",
                      "sdpa_bwd_noalloc", "sdpa_check_device_error"):
             getattr(lib, name).restype = _I
         _lib = lib
@@ -135,6 +151,51 @@ def sdpa_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, tota
                                   _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), num_seqs, total_q,
                                   total_kv, max_seqlen_q, max_seqlen_kv, h, d, float(attn_scale),
                                   int(causal), int(dtype), _stream(stream)))
+
+
+def sdpa_fwd_ex(q, k, v, o, lse, b, h, h_kv, s_q, s_kv, d, attn_scale, mask, window_left, dtype,
+                stream=None):
+    _check(load().sdpa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, h, h_kv, s_q, s_kv,
+                              d, float(attn_scale), int(mask), int(window_left), int(dtype),
+                              _stream(stream)))
+
+
+def sdpa_varlen_fwd_ex(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                       max_seqlen_q, max_seqlen_kv, h, h_kv, d, attn_scale, mask, window_left,
+                       dtype, stream=None):
+    _check(load().sdpa_varlen_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                     _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), num_seqs, total_q,
+                                     total_kv, max_seqlen_q, max_seqlen_kv, h, h_kv, d,
+                                     float(attn_scale), int(mask), int(window_left), int(dtype),
+                                     _stream(stream)))
+
+
+def sdpa_bwd_ex_workspace_size(b, h, s_q, d, deterministic=0) -> int:
+    return int(load().sdpa_bwd_ex_workspace_size(b, h, s_q, d, int(deterministic)))
+
+
+def sdpa_varlen_bwd_ex_workspace_size(total_q, h, d, deterministic=0) -> int:
+    return int(load().sdpa_varlen_bwd_ex_workspace_size(total_q, h, d, int(deterministic)))
+
+
+def sdpa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, b, h, h_kv, s_q, s_kv, d, attn_scale, mask,
+                window_left, deterministic, dtype, workspace, workspace_bytes, stream=None):
+    _check(load().sdpa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), b, h, h_kv, s_q, s_kv, d, float(attn_scale),
+                              int(mask), int(window_left), int(deterministic), int(dtype),
+                              _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def sdpa_varlen_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, num_seqs,
+                       total_q, total_kv, max_seqlen_q, max_seqlen_kv, h, h_kv, d, attn_scale,
+                       mask, window_left, deterministic, dtype, workspace, workspace_bytes,
+                       stream=None):
+    _check(load().sdpa_varlen_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q),
+                                     _ptr(cu_seqlens_kv), num_seqs, total_q, total_kv,
+                                     max_seqlen_q, max_seqlen_kv, h, h_kv, d, float(attn_scale),
+                                     int(mask), int(window_left), int(deterministic), int(dtype),
+                                     _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def sdpa_bwd_workspace_size(b, h, s_q, d) -> int:

@@ -186,13 +186,29 @@ bool overlaps(const Span &a, const Span &b) {
     return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
 }
 
-int check_common(int d, int dtype, int causal, float scale) {
+int check_common(int d, int dtype, float scale) {
     if (dtype != SDPA_BF16 && dtype != SDPA_FP16)
         return fail(SDPA_ERR_UNSUPPORTED, "dtype %d is not SDPA_BF16 or SDPA_FP16", dtype);
     if (d != 64 && d != 128) return fail(SDPA_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
-    if (causal != 0 && causal != 1) return fail(SDPA_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", causal);
     if (!(scale > 0.f) || !std::isfinite(scale))
         return fail(SDPA_ERR_INVALID_ARG, "attn_scale must be finite and > 0 (got %g)", (double)scale);
+    return SDPA_OK;
+}
+
+int check_causal(int causal) {
+    if (causal != 0 && causal != 1) return fail(SDPA_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", causal);
+    return SDPA_OK;
+}
+
+// Mask kind, left window and head grouping of the extended entry points.
+int check_mask_heads(int mask, int window_left, int h, int h_kv) {
+    if (mask != SDPA_MASK_NONE && mask != SDPA_MASK_CAUSAL && mask != SDPA_MASK_CAUSAL_BOTTOM_RIGHT)
+        return fail(SDPA_ERR_INVALID_ARG, "mask must be SDPA_MASK_NONE, SDPA_MASK_CAUSAL or "
+                                          "SDPA_MASK_CAUSAL_BOTTOM_RIGHT (got %d)", mask);
+    if (window_left < -1) return fail(SDPA_ERR_INVALID_ARG, "window_left must be -1 or >= 0 (got %d)", window_left);
+    if (h < 0 || h_kv < 0) return fail(SDPA_ERR_INVALID_ARG, "negative head count (h=%d h_kv=%d)", h, h_kv);
+    if (h > 0 && (h_kv == 0 || h % h_kv != 0))
+        return fail(SDPA_ERR_INVALID_ARG, "h=%d is not a multiple of h_kv=%d", h, h_kv);
     return SDPA_OK;
 }
 
@@ -269,21 +285,22 @@ int sdpa_check_device_error(sdpa_stream_t stream) {
                 tag < 5 ? names[tag] : "?", word & 0xffffu);
 }
 
-int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b, int h,
-             int s_q, int s_kv, int d, float attn_scale, int causal, int dtype,
-             sdpa_stream_t stream) {
-    int st = check_common(d, dtype, causal, attn_scale);
+int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int b, int h,
+                int h_kv, int s_q, int s_kv, int d, float attn_scale, int mask, int window_left,
+                int dtype, sdpa_stream_t stream) {
+    int st = check_common(d, dtype, attn_scale);
     if (st) return st;
-    if (b < 0 || h < 0 || s_q < 0 || s_kv < 0)
-        return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d h=%d s_q=%d s_kv=%d)", b, h, s_q, s_kv);
-    const int64_t bh = (int64_t)b * h;
+    if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
+    if (b < 0 || s_q < 0 || s_kv < 0)
+        return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d s_q=%d s_kv=%d)", b, s_q, s_kv);
+    const int64_t bh = (int64_t)b * h, bh_kv = (int64_t)b * h_kv;
     if (bh == 0 || s_q == 0) return ok();
-    const bool pair = use_pair_kernel(false, d, s_q, s_kv);
+    const bool pair = window_left < 0 && use_pair_kernel(false, d, s_q, s_kv);
     const int unit_rows = pair ? fwd_pair_rows() : kTileM;
     const int64_t q_tiles = (s_q + unit_rows - 1) / unit_rows;
     if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
-    const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh * s_kv * d * 2;
+    const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh_kv * s_kv * d * 2;
     const Span in[3] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}};
     const Span out[2] = {{o, qbytes, "o"}, {lse, lse ? (size_t)bh * s_q * 4 : 0, "lse"}};
     if ((st = check_ptrs(in, 3, out, 2))) return st;
@@ -293,25 +310,37 @@ int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
     const bool bf16 = dtype == SDPA_BF16;
     CUtensorMap tq, tk, tv;
     if ((st = dense_map(&tq, q, bf16, d, s_q, bh))) return st;
-    if ((st = dense_map(&tk, k, bf16, d, s_kv, bh))) return st;
-    if ((st = dense_map(&tv, v, bf16, d, s_kv, bh))) return st;
+    if ((st = dense_map(&tk, k, bf16, d, s_kv, bh_kv))) return st;
+    if ((st = dense_map(&tv, v, bf16, d, s_kv, bh_kv))) return st;
     FwdParams p{};
     p.o = o;
     p.lse = lse;
     p.err = dev->err;
     p.bh = (int)bh;
     p.h = h;
+    p.h_kv = h_kv;
+    p.group = h / h_kv;
     p.s_q = s_q;
     p.s_kv = s_kv;
     p.q_tiles = (int)q_tiles;
     p.n_units = (int)(q_tiles * bh);
-    p.causal = causal;
+    p.mask = mask;
+    p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
     const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer)
                               : launch_fwd(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer),
                          "sdpa_fwd");
+}
+
+int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b, int h,
+             int s_q, int s_kv, int d, float attn_scale, int causal, int dtype,
+             sdpa_stream_t stream) {
+    int st = check_causal(causal);
+    if (st) return st;
+    return sdpa_fwd_ex(q, k, v, o, lse, b, h, h, s_q, s_kv, d, attn_scale,
+                       causal ? SDPA_MASK_CAUSAL : SDPA_MASK_NONE, -1, dtype, stream);
 }
 
 static int check_varlen_sizes(const int32_t *cu_q, const int32_t *cu_kv, int num_seqs, int total_q,
@@ -333,23 +362,25 @@ static int check_varlen_sizes(const int32_t *cu_q, const int32_t *cu_kv, int num
     return SDPA_OK;
 }
 
-int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
-                    int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int h, int d,
-                    float attn_scale, int causal, int dtype, sdpa_stream_t stream) {
-    int st = check_common(d, dtype, causal, attn_scale);
+int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                       int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int h,
+                       int h_kv, int d, float attn_scale, int mask, int window_left, int dtype,
+                       sdpa_stream_t stream) {
+    int st = check_common(d, dtype, attn_scale);
     if (st) return st;
+    if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
     if ((st = check_varlen_sizes(cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const bool pair = use_pair_kernel(true, d, max_seqlen_q, max_seqlen_kv);
+    const bool pair = window_left < 0 && use_pair_kernel(true, d, max_seqlen_q, max_seqlen_kv);
     const int unit_rows = pair ? fwd_pair_rows() : kTileM;
     const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
     const int64_t slices = (int64_t)num_seqs * h;
     if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
-    const size_t qbytes = (size_t)total_q * h * d * 2, kvbytes = (size_t)total_kv * h * d * 2;
+    const size_t qbytes = (size_t)total_q * h * d * 2, kvbytes = (size_t)total_kv * h_kv * d * 2;
     const Span in[5] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"},
                         {cu_seqlens_q, (size_t)(num_seqs + 1) * 4, "cu_seqlens_q", 4},
                         {cu_seqlens_kv, (size_t)(num_seqs + 1) * 4, "cu_seqlens_kv", 4}};
@@ -361,8 +392,8 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
     const bool bf16 = dtype == SDPA_BF16;
     CUtensorMap tq, tk, tv;
     if ((st = packed_map(&tq, q, bf16, d, h, total_q))) return st;
-    if ((st = packed_map(&tk, k, bf16, d, h, total_kv))) return st;
-    if ((st = packed_map(&tv, v, bf16, d, h, total_kv))) return st;
+    if ((st = packed_map(&tk, k, bf16, d, h_kv, total_kv))) return st;
+    if ((st = packed_map(&tv, v, bf16, d, h_kv, total_kv))) return st;
     FwdParams p{};
     p.o = o;
     p.lse = lse;
@@ -371,16 +402,30 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
     p.err = dev->err;
     p.bh = (int)slices;
     p.h = h;
+    p.h_kv = h_kv;
+    p.group = h / h_kv;
     p.num_seqs = num_seqs;
     p.q_tiles = (int)q_tiles;
     p.n_units = (int)(q_tiles * slices);
-    p.causal = causal;
+    p.mask = mask;
+    p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
     const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer)
                               : launch_fwd(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer),
                          "sdpa_varlen_fwd");
+}
+
+int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                    int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int h, int d,
+                    float attn_scale, int causal, int dtype, sdpa_stream_t stream) {
+    int st = check_causal(causal);
+    if (st) return st;
+    return sdpa_varlen_fwd_ex(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q,
+                              total_kv, max_seqlen_q, max_seqlen_kv, h, h, d, attn_scale,
+                              causal ? SDPA_MASK_CAUSAL : SDPA_MASK_NONE, -1, dtype, stream);
 }
 
 size_t sdpa_bwd_workspace_size(int b, int h, int s_q, int d) {
@@ -401,20 +446,34 @@ size_t sdpa_varlen_bwd_workspace_size(int total_q, int h, int d) {
 
 static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
-             const float *lse, void *dq, void *dk, void *dv, int b, int h, int s_q, int s_kv,
-             int d, float attn_scale, int causal, int dtype, void *workspace,
-             size_t workspace_bytes, sdpa_stream_t stream) {
-    int st = check_common(d, dtype, causal, attn_scale);
+size_t sdpa_bwd_ex_workspace_size(int b, int h, int s_q, int d, int deterministic) {
+    if (deterministic != 0 && deterministic != 1) return (size_t)-1;
+    return sdpa_bwd_workspace_size(b, h, s_q, d);
+}
+
+size_t sdpa_varlen_bwd_ex_workspace_size(int total_q, int h, int d, int deterministic) {
+    if (deterministic != 0 && deterministic != 1) return (size_t)-1;
+    return sdpa_varlen_bwd_workspace_size(total_q, h, d);
+}
+
+int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                const float *lse, void *dq, void *dk, void *dv, int b, int h, int h_kv, int s_q,
+                int s_kv, int d, float attn_scale, int mask, int window_left, int deterministic,
+                int dtype, void *workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+    int st = check_common(d, dtype, attn_scale);
     if (st) return st;
-    if (b < 0 || h < 0 || s_q < 0 || s_kv < 0)
-        return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d h=%d s_q=%d s_kv=%d)", b, h, s_q, s_kv);
-    const int64_t bh = (int64_t)b * h;
+    if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
+    if (deterministic != 0 && deterministic != 1)
+        return fail(SDPA_ERR_INVALID_ARG, "deterministic must be 0 or 1 (got %d)", deterministic);
+    if (deterministic) return fail(SDPA_ERR_UNSUPPORTED, "the deterministic backward is not built yet");
+    if (b < 0 || s_q < 0 || s_kv < 0)
+        return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d s_q=%d s_kv=%d)", b, s_q, s_kv);
+    const int64_t bh = (int64_t)b * h, bh_kv = (int64_t)b * h_kv;
     if (bh == 0) return ok();
     const int64_t kv_tiles = (s_kv + kTileN - 1) / kTileN;
-    if (bh > INT32_MAX || kv_tiles * bh > INT32_MAX || (int64_t)s_q * bh > INT32_MAX)
+    if (bh > INT32_MAX || kv_tiles * bh_kv > INT32_MAX || (int64_t)s_q * bh > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
-    const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh * s_kv * d * 2;
+    const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh_kv * s_kv * d * 2;
     const size_t need = sdpa_bwd_workspace_size(b, h, s_q, d);
     const Span in[6] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}, {o, qbytes, "o"},
                         {dout, qbytes, "dout"}, {lse, (size_t)bh * s_q * 4, "lse"}};
@@ -439,8 +498,8 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     const bool bf16 = dtype == SDPA_BF16;
     CUtensorMap tq, tk, tv, tdo;
     if ((st = dense_map(&tq, q, bf16, d, s_q, bh))) return st;
-    if ((st = dense_map(&tk, k, bf16, d, s_kv, bh))) return st;
-    if ((st = dense_map(&tv, v, bf16, d, s_kv, bh))) return st;
+    if ((st = dense_map(&tk, k, bf16, d, s_kv, bh_kv))) return st;
+    if ((st = dense_map(&tv, v, bf16, d, s_kv, bh_kv))) return st;
     if ((st = dense_map(&tdo, dout, bf16, d, s_q, bh))) return st;
     BwdParams p{};
     p.o = o;
@@ -458,33 +517,53 @@ int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const v
     p.err = dev->err;
     p.bh = (int)bh;
     p.h = h;
+    p.h_kv = h_kv;
+    p.group = h / h_kv;
+    p.kv_slices = (int)bh_kv;
     p.s_q = s_q;
     p.s_kv = s_kv;
     p.kv_tiles = (int)kv_tiles;
     p.total_q = (int)(bh * s_q);
-    p.causal = causal;
+    p.mask = mask;
+    p.window = window_left;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
     return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
 }
 
-int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
-                    const float *lse, void *dq, void *dk, void *dv, const int32_t *cu_seqlens_q,
-                    const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int total_kv,
-                    int max_seqlen_q, int max_seqlen_kv, int h, int d, float attn_scale,
-                    int causal, int dtype, void *workspace, size_t workspace_bytes,
-                    sdpa_stream_t stream) {
-    int st = check_common(d, dtype, causal, attn_scale);
+int sdpa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+             const float *lse, void *dq, void *dk, void *dv, int b, int h, int s_q, int s_kv,
+             int d, float attn_scale, int causal, int dtype, void *workspace,
+             size_t workspace_bytes, sdpa_stream_t stream) {
+    int st = check_causal(causal);
     if (st) return st;
+    return sdpa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, b, h, h, s_q, s_kv, d, attn_scale,
+                       causal ? SDPA_MASK_CAUSAL : SDPA_MASK_NONE, -1, 0, dtype, workspace,
+                       workspace_bytes, stream);
+}
+
+int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *o,
+                       const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_kv, int num_seqs,
+                       int total_q, int total_kv, int max_seqlen_q, int max_seqlen_kv, int h,
+                       int h_kv, int d, float attn_scale, int mask, int window_left,
+                       int deterministic, int dtype, void *workspace, size_t workspace_bytes,
+                       sdpa_stream_t stream) {
+    int st = check_common(d, dtype, attn_scale);
+    if (st) return st;
+    if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
+    if (deterministic != 0 && deterministic != 1)
+        return fail(SDPA_ERR_INVALID_ARG, "deterministic must be 0 or 1 (got %d)", deterministic);
+    if (deterministic) return fail(SDPA_ERR_UNSUPPORTED, "the deterministic backward is not built yet");
     if ((st = check_varlen_sizes(cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || num_seqs == 0 || (total_q == 0 && total_kv == 0)) return ok();
     const int64_t kv_tiles = (max_seqlen_kv + kTileN - 1) / kTileN;
-    const int64_t slices = (int64_t)num_seqs * h;
-    if (slices > INT32_MAX || kv_tiles * slices > INT32_MAX || (int64_t)total_q * h > INT32_MAX)
+    const int64_t slices = (int64_t)num_seqs * h, kv_slices = (int64_t)num_seqs * h_kv;
+    if (slices > INT32_MAX || kv_tiles * kv_slices > INT32_MAX || (int64_t)total_q * h > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
-    const size_t qbytes = (size_t)total_q * h * d * 2, kvbytes = (size_t)total_kv * h * d * 2;
+    const size_t qbytes = (size_t)total_q * h * d * 2, kvbytes = (size_t)total_kv * h_kv * d * 2;
     const size_t need = sdpa_varlen_bwd_workspace_size(total_q, h, d);
     const Span in[8] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}, {o, qbytes, "o"},
                         {dout, qbytes, "dout"}, {lse, (size_t)total_q * h * 4, "lse"},
@@ -508,8 +587,8 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     const bool bf16 = dtype == SDPA_BF16;
     CUtensorMap tq, tk, tv, tdo;
     if ((st = packed_map(&tq, q, bf16, d, h, total_q))) return st;
-    if ((st = packed_map(&tk, k, bf16, d, h, total_kv))) return st;
-    if ((st = packed_map(&tv, v, bf16, d, h, total_kv))) return st;
+    if ((st = packed_map(&tk, k, bf16, d, h_kv, total_kv))) return st;
+    if ((st = packed_map(&tv, v, bf16, d, h_kv, total_kv))) return st;
     if ((st = packed_map(&tdo, dout, bf16, d, h, total_q))) return st;
     BwdParams p{};
     p.o = o;
@@ -529,13 +608,31 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, 
     p.err = dev->err;
     p.bh = (int)slices;
     p.h = h;
+    p.h_kv = h_kv;
+    p.group = h / h_kv;
+    p.kv_slices = (int)kv_slices;
     p.num_seqs = num_seqs;
     p.kv_tiles = (int)kv_tiles;
     p.total_q = total_q;
-    p.causal = causal;
+    p.mask = mask;
+    p.window = window_left;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
     return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
+}
+
+int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                    const float *lse, void *dq, void *dk, void *dv, const int32_t *cu_seqlens_q,
+                    const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int total_kv,
+                    int max_seqlen_q, int max_seqlen_kv, int h, int d, float attn_scale,
+                    int causal, int dtype, void *workspace, size_t workspace_bytes,
+                    sdpa_stream_t stream) {
+    int st = check_causal(causal);
+    if (st) return st;
+    return sdpa_varlen_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv,
+                              num_seqs, total_q, total_kv, max_seqlen_q, max_seqlen_kv, h, h, d,
+                              attn_scale, causal ? SDPA_MASK_CAUSAL : SDPA_MASK_NONE, -1, 0,
+                              dtype, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

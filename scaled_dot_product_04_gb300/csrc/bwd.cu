@@ -212,36 +212,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t sbase = smem_u32(smem);
 
     // ---------------------------------------------------------------- work unit
-    // Head-major order: all key tiles of one (batch, head) or (sequence, head)
-    // slice run back to back, ascending (under the causal mask the first key
-    // tiles see the most query tiles, so each slice's heaviest units start
-    // first).  The CTAs resident at any time then share a slice or two, whose
-    // fp32 dQ accumulator, Q and dO stay in L2 instead of every head's at once.
-    const int slice = blockIdx.x / p.kv_tiles;
+    // A CTA owns one key tile of one key/value slice ((batch, kv head) or
+    // (sequence, kv head)) and walks every query tile that can see it, for
+    // each of the group's h / h_kv query heads in turn, so dK and dV sum over
+    // the group in TMEM.  Head-major order: all key tiles of one slice run
+    // back to back, ascending (under a causal mask the first key tiles see
+    // the most query tiles, so each slice's heaviest units start first).  The
+    // CTAs resident at any time then share a slice or two, whose fp32 dQ
+    // accumulator, Q and dO stay in L2 instead of every head's at once.
+    const int slice = blockIdx.x / p.kv_tiles;  // key/value slice
     const int kt = blockIdx.x % p.kv_tiles;
-    int Lq, Lkv, tok_q0 = 0, tok_kv0 = 0, head = 0;
-    RowMap qm, km;
+    const int hk = slice % p.h_kv;              // key/value head
+    int Lq, Lkv, tok_q0 = 0, tok_kv0 = 0;
+    int q_slice0;                               // dense: query slice of the group's first head
+    RowMap km;
     if constexpr (!kPacked) {
         Lq = p.s_q;
         Lkv = p.s_kv;
-        qm = {(int64_t)slice * p.s_q * D, D, (int64_t)slice * p.s_q * D};
+        q_slice0 = (slice / p.h_kv) * p.h + hk * p.group;
         km = {(int64_t)slice * p.s_kv * D, D, 0};
     } else {
-        const int n = slice / p.h;
-        head = slice % p.h;
+        const int n = slice / p.h_kv;
+        q_slice0 = 0;
         tok_q0 = p.cu_q[n];
         tok_kv0 = p.cu_kv[n];
         Lq = p.cu_q[n + 1] - tok_q0;
         Lkv = p.cu_kv[n + 1] - tok_kv0;
-        qm = {((int64_t)tok_q0 * p.h + head) * D, (int64_t)p.h * D,
-              ((int64_t)head * p.total_q + tok_q0) * D};
-        km = {((int64_t)tok_kv0 * p.h + head) * D, (int64_t)p.h * D, 0};
+        km = {((int64_t)tok_kv0 * p.h_kv + hk) * D, (int64_t)p.h_kv * D, 0};
     }
     const int k0 = kt * kTileN;
     if (k0 >= Lkv) return;  // packed: this sequence has fewer key tiles
-    const int q_tiles = (Lq + kTileM - 1) / kTileM;
-    const int qt_begin = p.causal ? k0 / kTileM : 0;
-    const int n_q = max(0, q_tiles - qt_begin);
+    // Query rows that see at least one key of [k0, k_last]: a causal mask
+    // needs i + delta >= k0, a window i + delta - window <= k_last.
+    const int delta = mask_delta(p.mask, Lq, Lkv);
+    const int k_last = min(k0 + kTileN, Lkv) - 1;
+    const int row_lo = p.mask != kMaskNone ? max(0, k0 - delta) : 0;
+    const int row_hi = p.window >= 0 ? min(Lq, k_last - delta + p.window + 1) : Lq;
+    const int qt_begin = row_lo / kTileM;
+    const int n_q = row_hi > row_lo ? (row_hi + kTileM - 1) / kTileM - qt_begin : 0;
+    const int n_it = n_q * p.group;  // (query head, query tile) pairs, head-major
+    // Iteration i: query head hk * group + i / n_q, query tile qt_begin + i % n_q;
+    // the dQ accumulator row of that head's query row r is acc_base(i) + r.
+    auto q_head = [&](int i) { return hk * p.group + i / n_q; };
+    auto q_tile_row0 = [&](int i) { return (qt_begin + i % n_q) * kTileM; };
+    auto acc_base = [&](int i) -> int {
+        return kPacked ? q_head(i) * p.total_q + tok_q0 : (q_slice0 + i / n_q) * p.s_q;
+    };
 
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == 0) {
         // ============================================================ producer
-        const int ky = kPacked ? head : k0;
+        const int ky = kPacked ? hk : k0;
         const int kz = kPacked ? tok_kv0 + k0 : slice;
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -324,12 +340,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         }
         int issued = 0, issued_do = 0;
-        for (int i = 0; i < n_q; ++i) {
+        for (int i = 0; i < n_it; ++i) {
             const int st = i & 1, use = i >> 1;
             const int dst = i % L::kDOStages, duse = i / L::kDOStages;
-            const int q0 = (qt_begin + i) * kTileM;
-            const int qy = kPacked ? head : q0;
-            const int qz = kPacked ? tok_q0 + q0 : slice;
+            const int q0 = q_tile_row0(i);
+            const int qy = kPacked ? q_head(i) : q0;
+            const int qz = kPacked ? tok_q0 + q0 : q_slice0 + i / n_q;
             // Q_i (freed by dK_{i-2}) is needed first, by S^T_i; dO_i (freed by
             // dV_{i-kDOStages}) only by dP^T_i.
             if (use > 0 && !warp_wait_b(bar(L::bQEmpty + st), (use - 1) & 1, wc, 18)) break;
@@ -411,7 +427,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 issue_kmajor(dV_k, dDO_k, dAD, 0, L::kColDP);  // dP'^T_0
                 mma_commit(bar(L::bDPFull));
             }
-            for (int i = 0; ok && i < n_q; ++i) {
+            for (int i = 0; ok && i < n_it; ++i) {
                 const int st = i & 1;
                 const int dst = L::kDOStages == 1 ? 0 : (i & 1);
                 // dV += P^T dO.  P^T is packed two per column into the first 32
@@ -429,7 +445,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_commit(bar(L::bDVDone));
                 mma_commit(bar(L::bDOEmpty + dst));
                 // S'^T_{i+1}, once the dV product has finished reading P^T_i
-                if (i + 1 < n_q) {
+                if (i + 1 < n_it) {
                     const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
                     ok = mbar_wait(bar(L::bQFull + st1), use1 & 1, wc, 6) &&
                          mbar_wait(bar(L::bDVDone), i & 1, wc, 7);
@@ -457,7 +473,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_commit(bar(L::bQEmpty + st));
                 mma_commit(bar(L::bDSFree));
                 // dP'^T_{i+1}
-                if (i + 1 < n_q) {
+                if (i + 1 < n_it) {
                     const int dst1 = L::kDOStages == 1 ? 0 : ((i + 1) & 1);
                     const int duse1 = (i + 1) / L::kDOStages;
                     ok = mbar_wait(bar(L::bDOFull + dst1), duse1 & 1, wc, 10);
@@ -489,8 +505,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
         uint8_t *ds_row = smem + L::kDS + grp * L::kChunkBytes + j * 128;
         bool ok = true;
-        for (int i = 0; i < n_q; ++i) {
-            const int q0 = (qt_begin + i) * kTileM + grp * 64;  // query of local column 0
+        for (int i = 0; i < n_it; ++i) {
+            const int q0 = q_tile_row0(i) + grp * 64;  // query of local column 0
             ok = warp_wait_b(bar(L::bSFull), i & 1, wc, 12);
             if (!ok) break;
             tc_fence_after();
@@ -498,11 +514,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld32(col_s, s);
             tmem_ld32(col_s + 32, s + 32);
             tmem_ld_wait_regs<64>(s);
-            // Local column c is visible iff lo <= c < hi: key < Lkv, query <
-            // Lq (rows past it carry no row terms) and, causal, query >= key.
-            int lo = p.causal ? key - q0 : 0;
+            // Local column c (query q0 + c) is visible iff lo <= c < hi: key <
+            // Lkv, query < Lq (rows past it carry no row terms), under a causal
+            // mask query + delta >= key, under a window query + delta -
+            // window <= key.
+            int lo = p.mask != kMaskNone ? key - delta - q0 : 0;
+            int hi = Lq - q0;
+            if (p.window >= 0) hi = min(hi, key - delta + p.window + 1 - q0);
             if (!key_ok) lo = 64;
-            const int hi = Lq - q0;
             uint32_t pk[32];  // P^T, packed pairs: feeds the dV product (via TMEM) and dS
             if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64)) {
 #pragma unroll
@@ -594,10 +613,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t t_dq = tmem + ((uint32_t)(quad * 32) << 16) + L::kColDQ;
         const uint32_t stage = sbase + L::kDQStage + quad * (L::kDQSlots * L::kDQBoxBytes);
         uint8_t *stage_ptr = smem + L::kDQStage + quad * (L::kDQSlots * L::kDQBoxBytes) + lane * 64;
-        const int acc_row0 = (int)(qm.acc0 / D);
         int boxes = 0, slot = 0;  // boxes sent by this warp; slot of the next one
         // one 32 x 16 box: registers r[0..16) -> staging slot -> reduce-add
-        auto send = [&](const uint32_t *r, int col, int qrow) {
+        // into accumulator rows [arow, arow + 32), columns [col, col + 16)
+        auto send = [&](const uint32_t *r, int col, int arow) {
             if (boxes >= L::kDQSlots) {
                 if (lane == 0) bulk_wait_read<L::kDQSlots - 1>();  // the slot's last box was read
                 __syncwarp();
@@ -610,16 +629,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_reduce_add_2d(&tm_dq, stage + slot * L::kDQBoxBytes, col, acc_row0 + qrow);
+                tma_reduce_add_2d(&tm_dq, stage + slot * L::kDQBoxBytes, col, arow);
                 bulk_commit();
             }
             ++boxes;
             slot = slot + 1 == L::kDQSlots ? 0 : slot + 1;
         };
-        for (int i = 0; i < n_q; ++i) {
+        for (int i = 0; i < n_it; ++i) {
             if (!warp_wait_b(bar(L::bDQFull), i & 1, wc, 17)) break;
             tc_fence_after();
-            const int qrow0 = (qt_begin + i) * kTileM + quad * 32;
+            const int qrow0 = q_tile_row0(i) + quad * 32;
+            const int arow = acc_base(i) + qrow0;
             const bool live = qrow0 < Lq;  // any live row in this warp's quarter
             if constexpr (D == 128) {
                 uint32_t r[96];
@@ -628,8 +648,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_ld32(t_dq + 64, r + 64);
                 tmem_ld_wait_regs<96>(r);
                 if (live) {
-                    send(r, 0, qrow0);
-                    send(r + 16, 16, qrow0);
+                    send(r, 0, arow);
+                    send(r + 16, 16, arow);
                 }
                 tmem_ld32(t_dq + 96, r);
                 tmem_ld_wait_regs<32>(r);
@@ -637,9 +657,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(bar(L::bDQFree));
                 if (live) {
 #pragma unroll
-                    for (int c = 32; c < 96; c += 16) send(r + c, c, qrow0);
-                    send(r, 96, qrow0);
-                    send(r + 16, 112, qrow0);
+                    for (int c = 32; c < 96; c += 16) send(r + c, c, arow);
+                    send(r, 96, arow);
+                    send(r + 16, 112, arow);
                 }
             } else {
                 uint32_t r[D];
@@ -650,7 +670,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(bar(L::bDQFree));
                 if (live) {
 #pragma unroll
-                    for (int c = 0; c < D; c += 16) send(r + c, c, qrow0);
+                    for (int c = 0; c < D; c += 16) send(r + c, c, arow);
                 }
             }
         }
@@ -683,7 +703,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     auto kern = bwd_main_kernel<D, kBf16, kPacked>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    const int grid = p.kv_tiles * p.bh;
+    const int grid = p.kv_tiles * p.kv_slices;
     if (timer.start) cudaEventRecord(timer.start, stream);
     kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, trx, p);
     e = cudaGetLastError();

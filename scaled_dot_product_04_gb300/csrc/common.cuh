@@ -22,22 +22,48 @@ enum KernelTag : uint32_t {
 // tensors are [T, h, d] (row stride h*d).  The TMA maps use the same two
 // shapes, so a tile of 128 rows is addressed by (y, z) = (row0, bh) when
 // dense and (h, tok0) when packed.
+// Masks (cudnn-frontend PR #554 `sdpa` op: is_causal, causal_bottom_right,
+// window_left).  In a sequence of Lq queries and Lkv keys, query i sees keys
+// j with lo_i <= j < hi_i, where delta = Lkv - Lq for kMaskBottomRight and 0
+// otherwise, hi_i = min(Lkv, i + delta + 1) under a causal mask (Lkv without
+// one) and lo_i = max(0, i + delta - window) for window >= 0 (0 without).
+enum MaskKind : int { kMaskNone = 0, kMaskTopLeft = 1, kMaskBottomRight = 2 };
+
 struct FwdParams {
     void *o;                     // output [.. , d] in the I/O dtype
     float *lse;                  // may be null
     const int32_t *cu_q;         // packed only
     const int32_t *cu_kv;        // packed only
     uint32_t *err;               // device error word
-    int bh;                      // dense: b*h.  packed: num_seqs*h
-    int h;
+    int bh;                      // query slices: dense b*h, packed num_seqs*h
+    int h;                       // query heads
+    int h_kv;                    // key/value heads (h is a multiple)
+    int group;                   // h / h_kv: query head hq reads key/value head hq / group
     int s_q, s_kv;               // dense lengths
     int num_seqs;                // packed
     int q_tiles;                 // row blocks per slice (128 rows, or 256 for the
                                  // two-tile kernel): dense from s_q, packed from max_seqlen_q
     int n_units;                 // q_tiles * bh (units a persistent CTA may visit)
-    int causal;
+    int mask;                    // MaskKind
+    int window;                  // window_left, -1 for none
     float scale_log2;            // attn_scale * log2(e)
 };
+
+// Key range [lo, hi) of query row i (see MaskKind), for the row order of one
+// sequence; lo may come out negative and hi above Lkv only where the callers
+// clamp them.
+struct KeyRange {
+    int lo, hi;
+};
+__host__ __device__ inline int mask_delta(int mask, int Lq, int Lkv) {
+    return mask == kMaskBottomRight ? Lkv - Lq : 0;
+}
+__host__ __device__ inline KeyRange key_range(int mask, int window, int i, int delta, int Lkv) {
+    KeyRange r;
+    r.hi = mask != kMaskNone ? (i + delta + 1 < Lkv ? i + delta + 1 : Lkv) : Lkv;
+    r.lo = window >= 0 ? i + delta - window : -(1 << 30);
+    return r;
+}
 
 struct BwdParams {
     const void *o, *dout;        // [.., d] I/O dtype
@@ -48,12 +74,15 @@ struct BwdParams {
                                  // -LSE/scale and -D, each split into a tf32 pair (hi, lo)
     const int32_t *cu_q, *cu_kv;
     uint32_t *err;
-    int bh, h;
+    int bh;                      // query slices: dense b*h, packed num_seqs*h
+    int h, h_kv, group;          // query heads, key/value heads, h / h_kv
+    int kv_slices;               // key/value slices: dense b*h_kv, packed num_seqs*h_kv
     int s_q, s_kv;
     int num_seqs;
     int kv_tiles;                // dense: ceil(s_kv/128); packed: ceil(max_seqlen_kv/128)
     int total_q;                 // packed: number of query tokens; dense: b*h*s_q rows
-    int causal;
+    int mask;                    // MaskKind
+    int window;                  // window_left, -1 for none
     float scale;                 // attn_scale
     float scale_log2;            // attn_scale * log2(e)
 };

@@ -3,7 +3,10 @@
 //
 // Operation: "Inside NVIDIA's cuDNN Graph API" (tradepoint.io), section 5
 // "SDPA (Flash Attention) with causal masking" -- top-left causal alignment,
-// fp32 intermediate and compute type.  Softmax runs in the base-2 domain with
+// fp32 intermediate and compute type -- widened to the masks and grouped
+// key/value heads of the cudnn-frontend PR #554 `sdpa` op (causal_bottom_right,
+// window_left; GQA): a unit visits only the key tiles its rows can see, and
+// query head hq reads key/value head hq / (h / h_kv).  Softmax runs in the base-2 domain with
 // scale*log2(e) folded into one multiplier (cudnn-frontend PR #554, SM100
 // FP8 d512 notes: scale_softmax_log2); LSE is converted back to the natural
 // log on write-out.  Tiles wholly above the causal diagonal are never loaded
@@ -103,9 +106,11 @@ SDPA_DEV int unit_of(int k, int first, int step) {
     return k * step + ((k & 1) ? step - 1 - first : first);
 }
 
-// One work unit: a 128-row query tile of one slice.
+// One work unit: a 128-row query tile of one slice.  It visits key tiles
+// kt0 .. kt0 + n_kv - 1; K/V come from slice kv_slice (dense) or head
+// kv_head (packed).
 struct Unit {
-    int slice, head, Lq, Lkv, tok_q0, tok_kv0, row0, n_kv;
+    int slice, head, kv_slice, kv_head, Lq, Lkv, tok_q0, tok_kv0, row0, kt0, n_kv, delta;
     bool live;  // the tile holds at least one query row
     int64_t o_row0, o_rs, lse_row0, lse_rs;
 };
@@ -117,6 +122,8 @@ SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int 
     U.slice = u % p.bh;
     if constexpr (!kPacked) {
         U.head = 0;
+        U.kv_head = 0;
+        U.kv_slice = (U.slice / p.h) * p.h_kv + (U.slice % p.h) / p.group;
         U.tok_q0 = U.tok_kv0 = 0;
         U.Lq = p.s_q;
         U.Lkv = p.s_kv;
@@ -127,6 +134,8 @@ SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int 
     } else {
         const int n = U.slice / p.h;
         U.head = U.slice % p.h;
+        U.kv_head = U.head / p.group;
+        U.kv_slice = 0;
         U.tok_q0 = cu_q[n];
         U.tok_kv0 = cu_kv[n];
         U.Lq = cu_q[n + 1] - U.tok_q0;
@@ -138,12 +147,13 @@ SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int 
     }
     U.row0 = qt * kTileM;
     U.live = U.row0 < U.Lq;
-    int n_kv = (U.Lkv + kTileN - 1) / kTileN;
-    if (p.causal) {
-        const int q_last = min(U.row0 + kTileM - 1, U.Lq - 1);
-        n_kv = min(n_kv, q_last / kTileN + 1);
-    }
-    U.n_kv = U.live ? max(n_kv, 0) : 0;
+    // keys seen by any row: from the first row's window start to the last
+    // row's causal end
+    U.delta = mask_delta(p.mask, U.Lq, U.Lkv);
+    const int lo = max(0, key_range(p.mask, p.window, U.row0, U.delta, U.Lkv).lo);
+    const int hi = key_range(p.mask, p.window, min(U.row0 + kTileM, U.Lq) - 1, U.delta, U.Lkv).hi;
+    U.kt0 = lo / kTileN;
+    U.n_kv = (U.live && hi > lo) ? (hi + kTileN - 1) / kTileN - U.kt0 : 0;
     return U;
 }
 
@@ -256,8 +266,9 @@ __global__ void __launch_bounds__(192, 1)
                                 bar(L::bQFull + qs), c * 64, qy, qz);
                 ++units;
                 for (int j = 0; j < U.n_kv; ++j) {
-                    const int ky = kPacked ? U.head : j * kTileN;
-                    const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.slice;
+                    const int k0 = (U.kt0 + j) * kTileN;
+                    const int ky = kPacked ? U.kv_head : k0;
+                    const int kz = kPacked ? U.tok_kv0 + k0 : U.kv_slice;
                     const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
                     if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
                         ok = false;
@@ -446,13 +457,16 @@ __global__ void __launch_bounds__(192, 1)
                 for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(t_lane + cs + c * 32, s + c * 32);
                 tmem_ld_wait_regs<kTileN>(s);
 
-                const int k0 = j * kTileN;
-                if ((k0 + kTileN > U.Lkv) || (p.causal && k0 + kTileN - 1 > U.row0)) {
-                    int lim = U.Lkv - k0;  // columns c < lim are visible
-                    if (p.causal) lim = min(lim, q_idx - k0 + 1);
+                const int k0 = (U.kt0 + j) * kTileN;
+                // the tile needs a mask unless every row sees all of its keys
+                if ((k0 + kTileN > U.Lkv) ||
+                    (p.mask != kMaskNone && k0 + kTileN - 1 > U.row0 + U.delta) ||
+                    (p.window >= 0 && k0 < U.row0 + kTileM - 1 + U.delta - p.window)) {
+                    const KeyRange kr = key_range(p.mask, p.window, q_idx, U.delta, U.Lkv);
+                    const int c_lo = kr.lo - k0, c_hi = kr.hi - k0;  // visible: c_lo <= c < c_hi
 #pragma unroll
                     for (int c = 0; c < kTileN; ++c)
-                        if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+                        if (c < c_lo || c >= c_hi) s[c] = __float_as_uint(-INFINITY);
                 }
                 // row max: four independent chains of 3-input max
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};

@@ -1,11 +1,14 @@
 // Fused attention forward, two-tile variant: each work unit is 256 query rows
 // held as two 128-row tiles A and B that share every K/V tile, so the MMA
 // warp can run one tile's products while the other tile's softmax works.
-// Same operation, mask, statistics and layouts as fwd.cu ("Inside NVIDIA's
-// cuDNN Graph API" (tradepoint.io), section 5; cudnn-frontend PR #554 notes
-// on scale_softmax_log2, LSE layouts, persistent scheduling and the packed
-// total clamp); the host picks this kernel for long dense d = 128 problems,
-// where every unit visits many key tiles.
+// Same operation, masks, grouped key/value heads, statistics and layouts as
+// fwd.cu ("Inside NVIDIA's cuDNN Graph API" (tradepoint.io), section 5;
+// cudnn-frontend PR #554 notes on scale_softmax_log2, LSE layouts, the `sdpa`
+// op's masks and GQA, persistent scheduling and the packed total clamp); the
+// host picks this kernel for long dense d = 128 problems without a window,
+// where every unit visits many key tiles.  Both tiles walk key tiles from 0
+// (a window is still honoured, by the mask, at the cost of the tiles it
+// hides).
 //
 // Roles inside a CTA (12 warps):
 //   warp 0       TMA producer: Q_A, Q_B of each unit, then K_j and V_j into
@@ -84,7 +87,7 @@ SDPA_DEV int unit_of(int k, int first, int step) {
 // One work unit: rows [row0, row0 + 256) of one slice; tile A is the first
 // 128 rows, tile B the next 128.
 struct PairUnit {
-    int slice, head, Lq, Lkv, tok_q0, tok_kv0, row0;
+    int slice, head, kv_slice, kv_head, Lq, Lkv, tok_q0, tok_kv0, row0, delta;
     int n_kv[2];  // key tiles tile A / tile B visits (0: no row, or no key)
     bool live;    // tile A holds at least one query row
     int64_t o_row0, o_rs, lse_row0, lse_rs;
@@ -97,6 +100,8 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
     U.slice = u % p.bh;
     if constexpr (!kPacked) {
         U.head = 0;
+        U.kv_head = 0;
+        U.kv_slice = (U.slice / p.h) * p.h_kv + (U.slice % p.h) / p.group;
         U.tok_q0 = U.tok_kv0 = 0;
         U.Lq = p.s_q;
         U.Lkv = p.s_kv;
@@ -107,6 +112,8 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
     } else {
         const int n = U.slice / p.h;
         U.head = U.slice % p.h;
+        U.kv_head = U.head / p.group;
+        U.kv_slice = 0;
         U.tok_q0 = cu_q[n];
         U.tok_kv0 = cu_kv[n];
         U.Lq = cu_q[n + 1] - U.tok_q0;
@@ -118,14 +125,14 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
     }
     U.row0 = qp * kPairRows;
     U.live = U.row0 < U.Lq;
-    const int kv_tiles = (U.Lkv + kTileN - 1) / kTileN;
+    U.delta = mask_delta(p.mask, U.Lq, U.Lkv);
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
         const int r0 = U.row0 + x * kTileM;
         int n = 0;
         if (r0 < U.Lq) {
-            n = kv_tiles;
-            if (p.causal) n = min(n, min(r0 + kTileM - 1, U.Lq - 1) / kTileN + 1);
+            const int hi = key_range(p.mask, p.window, min(r0 + kTileM, U.Lq) - 1, U.delta, U.Lkv).hi;
+            n = hi > 0 ? (hi + kTileN - 1) / kTileN : 0;
         }
         U.n_kv[x] = n;
     }
@@ -239,8 +246,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
                 ++units;
                 for (int j = 0; j < nmax; ++j) {
-                    const int ky = kPacked ? U.head : j * kTileN;
-                    const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.slice;
+                    const int ky = kPacked ? U.kv_head : j * kTileN;
+                    const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.kv_slice;
                     const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
                     if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
                         ok = false;
@@ -415,12 +422,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 tmem_ld_wait_regs<kTileN>(s);
 
                 const int k0 = j * kTileN;
-                if ((k0 + kTileN > U.Lkv) || (p.causal && k0 + kTileN - 1 > row0)) {
-                    int lim = U.Lkv - k0;  // columns c < lim are visible
-                    if (p.causal) lim = min(lim, q_idx - k0 + 1);
+                // the tile needs a mask unless every row sees all of its keys
+                if ((k0 + kTileN > U.Lkv) ||
+                    (p.mask != kMaskNone && k0 + kTileN - 1 > row0 + U.delta) ||
+                    (p.window >= 0 && k0 < row0 + kTileM - 1 + U.delta - p.window)) {
+                    const KeyRange kr = key_range(p.mask, p.window, q_idx, U.delta, U.Lkv);
+                    const int c_lo = kr.lo - k0, c_hi = kr.hi - k0;  // visible: c_lo <= c < c_hi
 #pragma unroll
                     for (int c = 0; c < kTileN; ++c)
-                        if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+                        if (c < c_lo || c >= c_hi) s[c] = __float_as_uint(-INFINITY);
                 }
                 // row max: four independent chains of 3-input max
                 float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};

@@ -64,9 +64,10 @@ def _draw(shapes, seed: int, dtype: torch.dtype):
 
 
 def dense(b: int, h: int, s_q: int, s_kv: int, d: int, seed: int,
-          dtype: torch.dtype = torch.bfloat16, qk_mult: float = 1.0):
-    """Q [b,h,s_q,d], K/V [b,h,s_kv,d], dO [b,h,s_q,d] on the CPU."""
-    q, k, v, do = _draw([(b, h, s_q, d), (b, h, s_kv, d), (b, h, s_kv, d), (b, h, s_q, d)],
+          dtype: torch.dtype = torch.bfloat16, qk_mult: float = 1.0, h_kv: int | None = None):
+    """Q [b,h,s_q,d], K/V [b,h_kv,s_kv,d] (h_kv defaults to h), dO [b,h,s_q,d] on the CPU."""
+    hk = h if h_kv is None else h_kv
+    q, k, v, do = _draw([(b, h, s_q, d), (b, hk, s_kv, d), (b, hk, s_kv, d), (b, h, s_q, d)],
                         seed, dtype)
     if qk_mult != 1.0:
         q = q * qk_mult
@@ -87,10 +88,11 @@ def cu_seqlens(lengths) -> torch.Tensor:
 
 
 def packed(lengths_q, lengths_kv, h: int, d: int, seed: int,
-           dtype: torch.dtype = torch.bfloat16, qk_mult: float = 1.0):
-    """THD tensors: Q/dO [Tq,h,d], K/V [Tkv,h,d] and the two cu_seqlens."""
+           dtype: torch.dtype = torch.bfloat16, qk_mult: float = 1.0, h_kv: int | None = None):
+    """THD tensors: Q/dO [Tq,h,d], K/V [Tkv,h_kv,d] (h_kv defaults to h) and the two cu_seqlens."""
+    hk = h if h_kv is None else h_kv
     tq, tkv = int(sum(lengths_q)), int(sum(lengths_kv))
-    q, k, v, do = _draw([(tq, h, d), (tkv, h, d), (tkv, h, d), (tq, h, d)], seed, dtype)
+    q, k, v, do = _draw([(tq, h, d), (tkv, hk, d), (tkv, hk, d), (tq, h, d)], seed, dtype)
     if qk_mult != 1.0:
         q = q * qk_mult
         k = k * qk_mult
