@@ -197,9 +197,10 @@ int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
                     void *workspace, size_t workspace_bytes,
                     sdpa_stream_t stream);
 
-/* Workspace bytes of the extended backward calls (the same content as
- * sdpa_bwd's; the query-side sizes decide it, h_kv does not).
- * deterministic must be 0 or 1; (size_t)-1 otherwise. */
+/* Workspace bytes of the extended backward calls; the query-side sizes
+ * decide it, h_kv does not.  deterministic = 0: the same content as
+ * sdpa_bwd's (fp32 dQ accumulator and row terms); 1: the row terms alone,
+ * 16 bytes per query row.  (size_t)-1 for invalid arguments. */
 size_t sdpa_bwd_ex_workspace_size(int b, int h, int s_q, int d, int deterministic);
 size_t sdpa_varlen_bwd_ex_workspace_size(int total_q, int h, int d, int deterministic);
 
@@ -209,8 +210,11 @@ size_t sdpa_varlen_bwd_ex_workspace_size(int total_q, int h, int d, int determin
  * over the h / h_kv query heads that share the key/value head
  * (cudnn-frontend PR #554: "GQA reduces" in the backward chain).
  * deterministic: 0 accumulates dQ with fp32 reductions whose order may vary
- * between runs; 1 asks for bitwise reproducible gradients (returns
- * SDPA_ERR_UNSUPPORTED until that variant is built).
+ * between runs (dK and dV are reproducible either way); 1 gives bitwise
+ * reproducible gradients: dQ is then computed by a separate query-stationary
+ * pass that recomputes S and dP per key tile and writes dQ once (cudnn-
+ * frontend PR #554: a separate dQ pass instead of atomics), at about 1.4x
+ * the tensor-core work of the default.
  */
 int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o,
                 const void *dout, const float *lse, void *dq, void *dk,

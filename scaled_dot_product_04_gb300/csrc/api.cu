@@ -279,10 +279,10 @@ int sdpa_check_device_error(sdpa_stream_t stream) {
     if (word == 0) return ok();
     const uint32_t zero = 0;
     cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
-    static const char *names[] = {"?", "fwd", "bwd_preprocess", "bwd_main", "bwd_dq_convert"};
+    static const char *names[] = {"?", "fwd", "bwd_preprocess", "bwd_main", "bwd_dq_convert", "bwd_dq"};
     const uint32_t tag = word >> 16;
     return fail(SDPA_ERR_TIMEOUT, "kernel %s gave up on a bounded wait (site %u)",
-                tag < 5 ? names[tag] : "?", word & 0xffffu);
+                tag < 6 ? names[tag] : "?", word & 0xffffu);
 }
 
 int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int b, int h,
@@ -428,6 +428,8 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
                               causal ? SDPA_MASK_CAUSAL : SDPA_MASK_NONE, -1, dtype, stream);
 }
 
+static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
 size_t sdpa_bwd_workspace_size(int b, int h, int s_q, int d) {
     if (b < 0 || h < 0 || s_q < 0 || (d != 64 && d != 128)) return (size_t)-1;
     const size_t rows = (size_t)b * h * s_q;
@@ -444,16 +446,23 @@ size_t sdpa_varlen_bwd_workspace_size(int total_q, int h, int d) {
     return ((acc + 255) & ~(size_t)255) + ((rowx + 255) & ~(size_t)255);
 }
 
-static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+// Deterministic mode keeps only the row terms (dQ is written directly).
+static size_t ex_workspace(size_t rows, int d, int deterministic) {
+    if (rows == 0) return 0;
+    const size_t rowx = round256(rows * 16);
+    return deterministic ? rowx : round256(rows * d * 4) + rowx;
+}
 
 size_t sdpa_bwd_ex_workspace_size(int b, int h, int s_q, int d, int deterministic) {
     if (deterministic != 0 && deterministic != 1) return (size_t)-1;
-    return sdpa_bwd_workspace_size(b, h, s_q, d);
+    if (b < 0 || h < 0 || s_q < 0 || (d != 64 && d != 128)) return (size_t)-1;
+    return ex_workspace((size_t)b * h * s_q, d, deterministic);
 }
 
 size_t sdpa_varlen_bwd_ex_workspace_size(int total_q, int h, int d, int deterministic) {
     if (deterministic != 0 && deterministic != 1) return (size_t)-1;
-    return sdpa_varlen_bwd_workspace_size(total_q, h, d);
+    if (total_q < 0 || h < 0 || (d != 64 && d != 128)) return (size_t)-1;
+    return ex_workspace((size_t)total_q * h, d, deterministic);
 }
 
 int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -465,7 +474,6 @@ int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o, cons
     if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
     if (deterministic != 0 && deterministic != 1)
         return fail(SDPA_ERR_INVALID_ARG, "deterministic must be 0 or 1 (got %d)", deterministic);
-    if (deterministic) return fail(SDPA_ERR_UNSUPPORTED, "the deterministic backward is not built yet");
     if (b < 0 || s_q < 0 || s_kv < 0)
         return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d s_q=%d s_kv=%d)", b, s_q, s_kv);
     const int64_t bh = (int64_t)b * h, bh_kv = (int64_t)b * h_kv;
@@ -474,7 +482,7 @@ int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o, cons
     if (bh > INT32_MAX || kv_tiles * bh_kv > INT32_MAX || (int64_t)s_q * bh > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
     const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh_kv * s_kv * d * 2;
-    const size_t need = sdpa_bwd_workspace_size(b, h, s_q, d);
+    const size_t need = sdpa_bwd_ex_workspace_size(b, h, s_q, d, deterministic);
     const Span in[6] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}, {o, qbytes, "o"},
                         {dout, qbytes, "dout"}, {lse, (size_t)bh * s_q * 4, "lse"}};
     const Span out[4] = {{dq, qbytes, "dq"}, {dk, kvbytes, "dk"}, {dv, kvbytes, "dv"},
@@ -508,12 +516,20 @@ int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o, cons
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
-    p.dq_acc = static_cast<float *>(workspace);
-    p.rowx = reinterpret_cast<float4 *>(static_cast<char *>(workspace) +
-                                        round256((size_t)bh * s_q * d * 4));
     CUtensorMap tdq, trx;
-    if ((st = acc_map(&tdq, p.dq_acc, d, bh * s_q))) return st;
+    if (deterministic) {
+        p.dq_acc = nullptr;
+        p.rowx = static_cast<float4 *>(workspace);
+        memset(&tdq, 0, sizeof(tdq));  // unused: the main kernel adds no dQ
+    } else {
+        p.dq_acc = static_cast<float *>(workspace);
+        p.rowx = reinterpret_cast<float4 *>(static_cast<char *>(workspace) +
+                                            round256((size_t)bh * s_q * d * 4));
+        if ((st = acc_map(&tdq, p.dq_acc, d, bh * s_q))) return st;
+    }
     if ((st = rowx_map(&trx, p.rowx, s_q, bh, 128, 1))) return st;
+    p.deterministic = deterministic;
+    p.q_tiles = (s_q + kTileM - 1) / kTileM;
     p.err = dev->err;
     p.bh = (int)bh;
     p.h = h;
@@ -554,7 +570,6 @@ int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *
     if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
     if (deterministic != 0 && deterministic != 1)
         return fail(SDPA_ERR_INVALID_ARG, "deterministic must be 0 or 1 (got %d)", deterministic);
-    if (deterministic) return fail(SDPA_ERR_UNSUPPORTED, "the deterministic backward is not built yet");
     if ((st = check_varlen_sizes(cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
@@ -564,7 +579,7 @@ int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *
     if (slices > INT32_MAX || kv_tiles * kv_slices > INT32_MAX || (int64_t)total_q * h > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
     const size_t qbytes = (size_t)total_q * h * d * 2, kvbytes = (size_t)total_kv * h_kv * d * 2;
-    const size_t need = sdpa_varlen_bwd_workspace_size(total_q, h, d);
+    const size_t need = sdpa_varlen_bwd_ex_workspace_size(total_q, h, d, deterministic);
     const Span in[8] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"}, {o, qbytes, "o"},
                         {dout, qbytes, "dout"}, {lse, (size_t)total_q * h * 4, "lse"},
                         {cu_seqlens_q, (size_t)(num_seqs + 1) * 4, "cu_seqlens_q", 4},
@@ -597,12 +612,20 @@ int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
-    p.dq_acc = static_cast<float *>(workspace);
-    p.rowx = reinterpret_cast<float4 *>(static_cast<char *>(workspace) +
-                                        round256((size_t)total_q * h * d * 4));
     CUtensorMap tdq, trx;
-    if ((st = acc_map(&tdq, p.dq_acc, d, (int64_t)total_q * h))) return st;
+    if (deterministic) {
+        p.dq_acc = nullptr;
+        p.rowx = static_cast<float4 *>(workspace);
+        memset(&tdq, 0, sizeof(tdq));  // unused: the main kernel adds no dQ
+    } else {
+        p.dq_acc = static_cast<float *>(workspace);
+        p.rowx = reinterpret_cast<float4 *>(static_cast<char *>(workspace) +
+                                            round256((size_t)total_q * h * d * 4));
+        if ((st = acc_map(&tdq, p.dq_acc, d, (int64_t)total_q * h))) return st;
+    }
     if ((st = rowx_map(&trx, p.rowx, h, total_q, 1, 128))) return st;
+    p.deterministic = deterministic;
+    p.q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;
     p.cu_q = cu_seqlens_q;
     p.cu_kv = cu_seqlens_kv;
     p.err = dev->err;

@@ -454,15 +454,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     issue_kmajor(dK_k, dQ_k + st1 * kTile16, dAS, st1, L::kColS);
                     mma_commit(bar(L::bSFull));
                 }
-                // dQ_i = dS' K, then dK += dS'^T Q (last reader of Q_i)
+                // dQ_i = dS' K (unless the deterministic dQ pass computes dQ),
+                // then dK += dS'^T Q (last reader of Q_i)
+                const bool do_dq = !p.deterministic;
                 ok = mbar_wait(bar(L::bDSReady), i & 1, wc, 8);
-                if (ok && !L::kDQAliasDP && i > 0) ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
+                if (ok && do_dq && !L::kDQAliasDP && i > 0)
+                    ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
                 if (!ok) break;
                 tc_fence_after();
+                if (do_dq) {
 #pragma unroll
-                for (int k = 0; k < 128 / 16; ++k)
-                    mma_ss(tmem + L::kColDQ, dDS_mn + k * 128, dK_mn + k * 128, id_dq, k > 0);
-                mma_commit(bar(L::bDQFull));
+                    for (int k = 0; k < 128 / 16; ++k)
+                        mma_ss(tmem + L::kColDQ, dDS_mn + k * 128, dK_mn + k * 128, id_dq, k > 0);
+                    mma_commit(bar(L::bDQFull));
+                }
                 {
                     const uint64_t b = dQ_mn + st * kTile16;
 #pragma unroll
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const int dst1 = L::kDOStages == 1 ? 0 : ((i + 1) & 1);
                     const int duse1 = (i + 1) / L::kDOStages;
                     ok = mbar_wait(bar(L::bDOFull + dst1), duse1 & 1, wc, 10);
-                    if (ok && L::kDQAliasDP) ok = mbar_wait(bar(L::bDQFree), i & 1, wc, 11);
+                    if (ok && do_dq && L::kDQAliasDP) ok = mbar_wait(bar(L::bDQFree), i & 1, wc, 11);
                     if (!ok) break;
                     tc_fence_after();
                     issue_kmajor(dV_k, dDO_k + dst1 * kTile16, dAD, (i + 1) & 1, L::kColDP);
@@ -635,7 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ++boxes;
             slot = slot + 1 == L::kDQSlots ? 0 : slot + 1;
         };
-        for (int i = 0; i < n_it; ++i) {
+        for (int i = 0; i < (p.deterministic ? 0 : n_it); ++i) {
             if (!warp_wait_b(bar(L::bDQFull), i & 1, wc, 17)) break;
             tc_fence_after();
             const int qrow0 = q_tile_row0(i) + quad * 32;
@@ -697,7 +702,8 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int small_grid = sms * 8;
-    bwd_preprocess_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(p, rows, acc_elems);
+    bwd_preprocess_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(
+        p, rows, p.deterministic ? 0 : acc_elems);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = bwd_main_kernel<D, kBf16, kPacked>;
@@ -709,6 +715,7 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     e = cudaGetLastError();
     if (timer.stop) cudaEventRecord(timer.stop, stream);
     if (e != cudaSuccess) return e;
+    if (p.deterministic) return launch_bwd_dq(tq, tk, tv, tdo, p, p.q_tiles, D, kBf16, kPacked, stream);
     bwd_dq_convert_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(p, rows);
     return cudaGetLastError();
 }

@@ -16,6 +16,7 @@ enum KernelTag : uint32_t {
     kTagBwdPre = 2,
     kTagBwdMain = 3,
     kTagBwdConvert = 4,
+    kTagBwdDq = 5,
 };
 
 // Where a tile lives: dense tensors are [b*h, s, d] (row stride d), packed
@@ -85,6 +86,9 @@ struct BwdParams {
     int window;                  // window_left, -1 for none
     float scale;                 // attn_scale
     float scale_log2;            // attn_scale * log2(e)
+    int deterministic;           // 1: the main kernel skips dQ (bwd_dq.cu computes it)
+    int q_tiles;                 // query tiles per slice: dense ceil(s_q/128), packed
+                                 // ceil(max_seqlen_q/128) (the dQ pass's grid)
 };
 
 // Host launchers (one translation unit each).
@@ -103,6 +107,11 @@ cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
                        cudaStream_t stream, const KernelTimer &timer);
+// Deterministic dQ pass (bwd_dq.cu): one CTA per (query slice, query tile);
+// q_tiles = query tiles per slice.  Writes p.dq from the row terms in p.rowx.
+cudaError_t launch_bwd_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const CUtensorMap &tdo, const BwdParams &p, int q_tiles, int d, bool bf16,
+                          bool packed, cudaStream_t stream);
 // tdq: 2-D fp32 map over the dQ accumulator [rows][d], box 16 x 32, 64-byte swizzle.
 // trx: map over the row terms (dense [b*h][s_q][4], packed [T][h][4] fp32), 128-row boxes.
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

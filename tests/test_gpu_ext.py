@@ -187,3 +187,55 @@ def test_ext_validation(sdpa):
     with pytest.raises(sdpa.SdpaError) as e:
         sdpa.sdpa_fwd_ex(q, k, k, o, lse, 1, 6, 3, 128, 128, 64, 0.1, 1, -2, 0)
     assert e.value.status == L.SDPA_ERR_INVALID_ARG and "window" in str(e.value)
+
+
+# ------------------------------------------------------------ deterministic backward
+DET_DENSE = [
+    (2, 4, 4, 333, 333, 128, "top_left", -1),
+    (1, 8, 2, 700, 700, 64, "bottom_right", -1),
+    (1, 4, 1, 300, 520, 128, "none", -1),
+    (1, 4, 2, 640, 640, 128, "top_left", 100),
+    (1, 2, 2, 460, 200, 128, "bottom_right", -1),   # dead rows
+]
+
+
+@pytest.mark.parametrize("case", DET_DENSE, ids=lambda c: f"b{c[0]}h{c[1]}kv{c[2]}s{c[3]}x{c[4]}d{c[5]}_{c[6]}_w{c[7]}")
+def test_deterministic_dense_bwd_parity_and_bits(sdpa, case):
+    b, h, h_kv, s_q, s_kv, d, mask, window = case
+    q, k, v, do = sdpa_inputs.dense(b, h, s_q, s_kv, d, seed=7000 + s_q + s_kv, h_kv=h_kv)
+    scale = 1.0 / math.sqrt(d)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = sdpa.attention(qc, kc, vc, scale=scale, mask=mask, window_left=window)
+    runs = [sdpa.attention_bwd(qc, kc, vc, o, doc, lse, scale=scale, mask=mask,
+                               window_left=window, deterministic=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    for name, i in (("dq", 0), ("dk", 1), ("dv", 2)):
+        assert torch.equal(runs[0][i], runs[1][i]) and torch.equal(runs[0][i], runs[2][i]), name
+    _grads_ok(runs[0], oracle.sdpa_bwd_ex(q, k, v, do, scale, mask, window))
+    # dK, dV are the default path's bits; dQ agrees to rounding
+    plain = sdpa.attention_bwd(qc, kc, vc, o, doc, lse, scale=scale, mask=mask, window_left=window)
+    torch.cuda.synchronize()
+    assert torch.equal(plain[1], runs[0][1]) and torch.equal(plain[2], runs[0][2])
+    check_rel(runs[0][0], plain[0].double().cpu().numpy(), 1e-2, "dq vs default")
+
+
+@pytest.mark.parametrize("case", PACKED_CASES[:4], ids=lambda c: f"n{len(c[0])}h{c[2]}kv{c[3]}d{c[4]}_{c[5]}_w{c[6]}")
+def test_deterministic_packed_bwd(sdpa, case):
+    lq, lk, h, h_kv, d, mask, window = case
+    q, k, v, do, cu_q, cu_kv = sdpa_inputs.packed(lq, lk, h, d, seed=8000 + sum(lq), h_kv=h_kv)
+    scale = 1.0 / math.sqrt(d)
+    qc, kc, vc, doc, cq, ck = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu_q.cuda(), cu_kv.cuda()
+    o, lse = sdpa.attention_varlen(qc, kc, vc, cq, ck, max(lq), max(lk), scale=scale, mask=mask,
+                                   window_left=window)
+    runs = [sdpa.attention_varlen_bwd(qc, kc, vc, o, doc, lse, cq, ck, max(lq), max(lk),
+                                      scale=scale, mask=mask, window_left=window,
+                                      deterministic=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(runs[0][i], runs[1][i])
+    _grads_ok(runs[0], oracle.sdpa_varlen_bwd_ex(q, k, v, do, cu_q, cu_kv, scale, mask, window))
+
+
+def test_deterministic_workspace_is_the_row_terms(sdpa):
+    assert sdpa.sdpa_bwd_ex_workspace_size(2, 3, 100, 128, 1) == 2 * 3 * 100 * 16 + 256 - (2 * 3 * 100 * 16) % 256
+    assert sdpa.sdpa_bwd_ex_workspace_size(2, 3, 100, 128, 0) == sdpa.sdpa_bwd_workspace_size(2, 3, 100, 128)
