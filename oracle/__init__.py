@@ -81,6 +81,9 @@ def _load():
                                                   _int, _int, _dbl, _int, _int]
         lib.oracle_sdpa_varlen_bwd_ex.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _ip, _ip,
                                                   _int, _int, _int, _int, _dbl, _int, _int]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = _dbl
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.POINTER(ctypes.c_uint8), _dp, _i64, _dbl]
         lib.oracle_num_threads.restype = _int
         _lib = lib
         return lib
@@ -305,3 +308,39 @@ def attn_bwd_rows_ex(q, k, v, dout, q_rows, kv_rows, scale: float, mask="top_lef
                                     int(window_left), _pi(q_rows), len(q_rows), _pi(kv_rows),
                                     len(kv_rows))
     return dq, dk, dv
+
+
+# ------------------------------------------------------------------ FP8 inputs
+def e4m3_decode(code: int) -> float:
+    """Real value of one E4M3 code (see sdpa_oracle.c)."""
+    return float(_load().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_to_f64(codes, descale: float) -> np.ndarray:
+    """Decode an array of E4M3 codes (uint8, any shape) times a per-tensor descale."""
+    try:
+        import torch
+        if isinstance(codes, torch.Tensor):
+            codes = codes.detach().cpu().contiguous().view(torch.uint8).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e4m3_to_f64(c.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), _p(out), c.size,
+                               float(descale))
+    return out
+
+
+def sdpa_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float, scale: float,
+                 mask="top_left", window_left: int = -1):
+    """Dense forward of E4M3 inputs with per-tensor descales: attention of the
+    real values decode(x) * descale_x, in fp64 -> (o, lse)."""
+    return sdpa_fwd_ex(e4m3_to_f64(q, descale_q), e4m3_to_f64(k, descale_k),
+                       e4m3_to_f64(v, descale_v), scale, mask, window_left)
+
+
+def sdpa_varlen_fwd_fp8(q, k, v, cu_q, cu_kv, descale_q: float, descale_k: float,
+                        descale_v: float, scale: float, mask="top_left", window_left: int = -1):
+    """Packed forward of E4M3 inputs with per-tensor descales -> (o, lse)."""
+    return sdpa_varlen_fwd_ex(e4m3_to_f64(q, descale_q), e4m3_to_f64(k, descale_k),
+                              e4m3_to_f64(v, descale_v), cu_q, cu_kv, scale, mask, window_left)

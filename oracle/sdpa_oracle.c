@@ -418,6 +418,32 @@ void oracle_sdpa_varlen_bwd(const double *q, const double *k, const double *v,
                               scale, causal_mask(causal), -1);
 }
 
+/* ------------------------------------------------------------------ */
+/* FP8 E4M3 inputs                                                      */
+/* ------------------------------------------------------------------ */
+
+/* One 8-bit E4M3 code (the OCP "FN" encoding the cudnn-frontend PR #554 FP8
+ * kernels take as input): sign bit 7, exponent bits 6..3 with bias 7,
+ * mantissa bits 2..0.  Exponent field 0 is subnormal, (m / 8) * 2^-6; the
+ * code S.1111.111 is NaN; there are no infinities, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_decode(uint8_t x)
+{
+    int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* dst[i] = decode(src[i]) * descale: the real value an FP8 tensor with a
+ * per-tensor descale stands for. */
+void oracle_e4m3_to_f64(const uint8_t *src, double *dst, int64_t n, double descale)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = oracle_e4m3_decode(src[i]) * descale;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

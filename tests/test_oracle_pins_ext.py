@@ -237,3 +237,35 @@ def test_extended_varlen_equals_dense_per_sequence():
             np.testing.assert_allclose(dq[qs], rdq[0].transpose(1, 0, 2), rtol=0, atol=1e-14)
             np.testing.assert_allclose(dk[ks], rdk[0].transpose(1, 0, 2), rtol=0, atol=1e-14)
             np.testing.assert_allclose(dv[ks], rdv[0].transpose(1, 0, 2), rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------------------------ FP8 E4M3
+def test_e4m3_decoder_matches_torch_on_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2  # S.1111.111
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_decoder_values_from_the_format():
+    # 1.0 = 0.0111.000, 448 = 0.1111.110, smallest subnormal 2^-9 = 0.0000.001
+    assert oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0xB8) == -1.0
+    arr = oracle.e4m3_to_f64(np.array([0x38, 0x40, 0x08], np.uint8), 0.5)
+    np.testing.assert_array_equal(arr, [0.5, 1.0, 0.5 * 2.0 ** -6])
+
+
+def test_fp8_forward_is_attention_of_the_dequantized_values():
+    g = torch.Generator().manual_seed(9)
+    q, k, v = (torch.randn(1, 2, 20, 16, generator=g) for _ in range(3))
+    enc = [x.mul(8.0).to(torch.float8_e4m3fn) for x in (q, k, v)]
+    codes = [e.view(torch.uint8) for e in enc]
+    real = [e.to(torch.float64) / 8.0 for e in enc]
+    o, lse = oracle.sdpa_fwd_fp8(*codes, 0.125, 0.125, 0.125, 0.25, "bottom_right", 5)
+    ro, rlse = oracle.sdpa_fwd_ex(*real, 0.25, "bottom_right", 5)
+    np.testing.assert_array_equal(o, ro)
+    np.testing.assert_array_equal(lse, rlse)
