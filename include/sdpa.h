@@ -71,7 +71,11 @@ typedef enum {
     SDPA_ERR_TIMEOUT = 6      /* a kernel gave up on a bounded wait */
 } sdpa_status;
 
-typedef enum { SDPA_BF16 = 0, SDPA_FP16 = 1 } sdpa_dtype;
+typedef enum {
+    SDPA_BF16 = 0,
+    SDPA_FP16 = 1,
+    SDPA_FP8_E4M3 = 2 /* sdpa_fwd_fp8 / sdpa_varlen_fwd_fp8 only: OCP E4M3 ("FN") */
+} sdpa_dtype;
 
 /*
  * Masks of the extended entry points (cudnn-frontend PR #554, the `sdpa`
@@ -152,6 +156,43 @@ int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o,
                        int total_kv, int max_seqlen_q, int max_seqlen_kv, int h,
                        int h_kv, int d, float attn_scale, int mask,
                        int window_left, int dtype, sdpa_stream_t stream);
+
+/*
+ * FP8 forward (cudnn-frontend PR #554, per-tensor FP8 forward): q, k, v hold
+ * E4M3 codes (one byte per element, layouts and masks as sdpa_fwd_ex, d =
+ * 128) standing for the real values code * descale_x.
+ *   descale_q, descale_k, descale_v : fp32 scalars in DEVICE memory, read by
+ *     the kernel (no host read-back); descale_q * descale_k joins the
+ *     softmax multiplier, descale_v the output factor.
+ *   out_dtype : SDPA_BF16, SDPA_FP16 or SDPA_FP8_E4M3 for o; an E4M3 output
+ *     holds round-to-nearest, saturated codes of O * (*scale_o) (scale_o, a
+ *     device fp32 scalar, is required then and ignored otherwise).
+ *   amax_o : NULL, or a device fp32 scalar that receives max |O| over the
+ *     whole output, taken on the real-valued O before any output scaling or
+ *     rounding (the call sets it to 0 first, on `stream`).
+ *   lse : as sdpa_fwd_ex, of the real-valued scores.
+ * P enters the P V product as E4M3 (relative rounding error <= 2^-4 per
+ * element); the row sums and the LSE use the unrounded fp32 P.
+ */
+int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o,
+                 float *lse, const float *descale_q, const float *descale_k,
+                 const float *descale_v, const float *scale_o, float *amax_o,
+                 int b, int h, int h_kv, int s_q, int s_kv, int d,
+                 float attn_scale, int mask, int window_left, int out_dtype,
+                 sdpa_stream_t stream);
+
+/* Packed FP8 forward: sdpa_varlen_fwd_ex's layout and masks with the FP8
+ * arguments of sdpa_fwd_fp8. */
+int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o,
+                        float *lse, const float *descale_q,
+                        const float *descale_k, const float *descale_v,
+                        const float *scale_o, float *amax_o,
+                        const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_kv, int num_seqs,
+                        int total_q, int total_kv, int max_seqlen_q,
+                        int max_seqlen_kv, int h, int h_kv, int d,
+                        float attn_scale, int mask, int window_left,
+                        int out_dtype, sdpa_stream_t stream);
 
 /*
  * Workspace bytes sdpa_bwd needs: an fp32 dQ accumulator [b,h,s_q,d] and

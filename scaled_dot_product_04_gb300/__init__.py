@@ -12,7 +12,8 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (SDPA_BF16, SDPA_FP16, SDPA_MASK_CAUSAL, SDPA_MASK_CAUSAL_BOTTOM_RIGHT,  # noqa: F401
+from ._lib import (SDPA_BF16, SDPA_FP16, SDPA_FP8_E4M3, sdpa_fwd_fp8, sdpa_varlen_fwd_fp8,  # noqa: F401
+                   SDPA_MASK_CAUSAL, SDPA_MASK_CAUSAL_BOTTOM_RIGHT,
                    SDPA_MASK_NONE, SdpaError, dtype_code, load, sdpa_bwd, sdpa_bwd_ex,
                    sdpa_bwd_ex_workspace_size, sdpa_bwd_noalloc, sdpa_bwd_workspace_size,
                    sdpa_check_device_error, sdpa_fwd, sdpa_fwd_ex, sdpa_last_error,
@@ -27,7 +28,8 @@ __all__ = ["attention", "attention_varlen", "attention_bwd", "attention_varlen_b
            "sdpa_bwd_ex_workspace_size", "sdpa_varlen_bwd_ex_workspace_size", "sdpa_last_error",
            "sdpa_check_device_error", "sdpa_set_forward_variant", "sdpa_set_kernel_timer",
            "sdpa_version", "SdpaError", "load", "SDPA_MASK_NONE", "SDPA_MASK_CAUSAL",
-           "SDPA_MASK_CAUSAL_BOTTOM_RIGHT"]
+           "SDPA_MASK_CAUSAL_BOTTOM_RIGHT", "SDPA_FP8_E4M3", "sdpa_fwd_fp8", "sdpa_varlen_fwd_fp8",
+           "attention_fp8"]
 
 _MASK_NAMES = {"none": SDPA_MASK_NONE, "top_left": SDPA_MASK_CAUSAL,
                "bottom_right": SDPA_MASK_CAUSAL_BOTTOM_RIGHT}
@@ -144,3 +146,23 @@ def attention_varlen_bwd(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_kv, max
                            _default_scale(d, scale), m, window_left, int(bool(deterministic)),
                            dtype_code(q), workspace, workspace.numel(), stream)
     return dq, dk, dv
+
+
+def attention_fp8(q, k, v, descale_q, descale_k, descale_v, *, scale=None, causal=False, mask=None,
+                  window_left=-1, out_dtype=None, scale_o=None, want_amax=True, stream=None):
+    """Dense FP8 forward.  q [b,h,s_q,d], k/v [b,h_kv,s_kv,d] as torch.float8_e4m3fn (or
+    uint8 codes) on the GPU; descales are 1-element fp32 CUDA tensors.  out_dtype:
+    torch.bfloat16 (default), torch.float16 or torch.float8_e4m3fn (needs scale_o).
+    -> (o, lse, amax) with amax a 1-element fp32 tensor (or None)."""
+    import torch
+    b, h, s_q, d = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    code = {torch.bfloat16: SDPA_BF16, torch.float16: SDPA_FP16}.get(out_dtype, SDPA_FP8_E4M3)
+    o = torch.empty((b, h, s_q, d), dtype=out_dtype, device=q.device)
+    lse = torch.empty((b, h, s_q), dtype=torch.float32, device=q.device)
+    amax = torch.empty(1, dtype=torch.float32, device=q.device) if want_amax else None
+    sdpa_fwd_fp8(q, k, v, o, lse, descale_q, descale_k, descale_v, scale_o, amax, b, h, h_kv, s_q,
+                 s_kv, d, _default_scale(d, scale), _mask_code(causal, mask), window_left, code,
+                 stream)
+    return o, lse, amax

@@ -22,6 +22,7 @@ SDPA_ERR_CUDA = 5
 SDPA_ERR_TIMEOUT = 6
 SDPA_BF16 = 0
 SDPA_FP16 = 1
+SDPA_FP8_E4M3 = 2
 SDPA_MASK_NONE = 0
 SDPA_MASK_CAUSAL = 1
 SDPA_MASK_CAUSAL_BOTTOM_RIGHT = 2
@@ -31,7 +32,8 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
                 6: "SDPA_ERR_TIMEOUT"}
 
 # Exported symbols, in the order include/sdpa.h declares them.
-EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_fwd_ex", "sdpa_varlen_fwd_ex",
+EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_fwd_ex", "sdpa_varlen_fwd_ex", "sdpa_fwd_fp8",
+           "sdpa_varlen_fwd_fp8",
            "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_varlen_bwd_workspace_size",
            "sdpa_varlen_bwd", "sdpa_bwd_ex_workspace_size", "sdpa_varlen_bwd_ex_workspace_size",
            "sdpa_bwd_ex", "sdpa_varlen_bwd_ex", "sdpa_bwd_noalloc", "sdpa_last_error",
@@ -75,6 +77,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sdpa_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]
         lib.sdpa_varlen_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                            _I, _F, _I, _I, _I, _P]
+        lib.sdpa_fwd_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                     _F, _I, _I, _I, _P]
+        lib.sdpa_varlen_fwd_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
+                                            _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]
         lib.sdpa_bwd_ex_workspace_size.argtypes = [_I, _I, _I, _I, _I]
         lib.sdpa_bwd_ex_workspace_size.restype = _Z
         lib.sdpa_varlen_bwd_ex_workspace_size.argtypes = [_I, _I, _I, _I]
@@ -102,6 +108,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sdpa_set_kernel_timer.restype = None
         for name in ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
                      "sdpa_fwd_ex", "sdpa_varlen_fwd_ex", "sdpa_bwd_ex", "sdpa_varlen_bwd_ex",
+                     "sdpa_fwd_fp8", "sdpa_varlen_fwd_fp8",
                      "sdpa_bwd_noalloc", "sdpa_check_device_error"):
             getattr(lib, name).restype = _I
         _lib = lib
@@ -168,6 +175,27 @@ def sdpa_varlen_fwd_ex(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, t
                                      total_kv, max_seqlen_q, max_seqlen_kv, h, h_kv, d,
                                      float(attn_scale), int(mask), int(window_left), int(dtype),
                                      _stream(stream)))
+
+
+def sdpa_fwd_fp8(q, k, v, o, lse, descale_q, descale_k, descale_v, scale_o, amax_o, b, h, h_kv,
+                 s_q, s_kv, d, attn_scale, mask, window_left, out_dtype, stream=None):
+    _check(load().sdpa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(descale_q),
+                               _ptr(descale_k), _ptr(descale_v), _ptr(scale_o), _ptr(amax_o), b,
+                               h, h_kv, s_q, s_kv, d, float(attn_scale), int(mask),
+                               int(window_left), int(out_dtype), _stream(stream)))
+
+
+def sdpa_varlen_fwd_fp8(q, k, v, o, lse, descale_q, descale_k, descale_v, scale_o, amax_o,
+                        cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv, max_seqlen_q,
+                        max_seqlen_kv, h, h_kv, d, attn_scale, mask, window_left, out_dtype,
+                        stream=None):
+    _check(load().sdpa_varlen_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      _ptr(descale_q), _ptr(descale_k), _ptr(descale_v),
+                                      _ptr(scale_o), _ptr(amax_o), _ptr(cu_seqlens_q),
+                                      _ptr(cu_seqlens_kv), num_seqs, total_q, total_kv,
+                                      max_seqlen_q, max_seqlen_kv, h, h_kv, d, float(attn_scale),
+                                      int(mask), int(window_left), int(out_dtype),
+                                      _stream(stream)))
 
 
 def sdpa_bwd_ex_workspace_size(b, h, s_q, d, deterministic=0) -> int:

@@ -106,17 +106,24 @@ int get_encoder() {
     return SDPA_OK;
 }
 
+// Element kind of a tensor map: 0 bf16, 1 fp16, 2 E4M3 (read as bytes).
+static CUtensorMapDataType map_type(int el) {
+    return el == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                   : el == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+}
+static int elem_bytes(int el) { return el == 2 ? 1 : 2; }
+
 // 3-D map over [dim2][dim1][d] with element stride 1 along d.  The box is
-// 64 elements (128 bytes, one swizzle span) x box1 x box2, 128-byte swizzle.
-int encode_map(CUtensorMap *m, const void *ptr, bool bf16, uint64_t d, uint64_t dim1,
+// 128 bytes of a row (64 16-bit or 128 8-bit elements: one swizzle span) x
+// box1 x box2, 128-byte swizzle.
+int encode_map(CUtensorMap *m, const void *ptr, int el, uint64_t d, uint64_t dim1,
                uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1,
                uint32_t box2) {
     cuuint64_t dims[3] = {d, dim1, dim2};
     cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-    cuuint32_t box[3] = {64, box1, box2};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes(el)), box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                          3, const_cast<void *>(ptr), dims, strides, box, estr,
+    CUresult r = g_encode(m, map_type(el), 3, const_cast<void *>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -124,22 +131,30 @@ int encode_map(CUtensorMap *m, const void *ptr, bool bf16, uint64_t d, uint64_t 
 }
 
 // Dense [rows_per_slice, d] slices stacked `slices` deep; tile = 128 rows of one slice.
-int dense_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int64_t rows, int64_t slices) {
+int dense_map_el(CUtensorMap *m, const void *ptr, int el, int d, int64_t rows, int64_t slices) {
     if (rows == 0 || slices == 0) {
         memset(m, 0, sizeof(*m));
         return SDPA_OK;
     }
-    return encode_map(m, ptr, bf16, d, rows, slices, (uint64_t)d * 2, (uint64_t)rows * d * 2, 128, 1);
+    const uint64_t rb = (uint64_t)d * elem_bytes(el);
+    return encode_map(m, ptr, el, d, rows, slices, rb, (uint64_t)rows * rb, 128, 1);
+}
+int dense_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int64_t rows, int64_t slices) {
+    return dense_map_el(m, ptr, bf16 ? 0 : 1, d, rows, slices);
 }
 
 // Packed [tokens, h, d]; tile = 128 tokens of one head.  The token extent is
 // the packed total, so reads past it are zero-filled.
-int packed_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int h, int64_t tokens) {
+int packed_map_el(CUtensorMap *m, const void *ptr, int el, int d, int h, int64_t tokens) {
     if (tokens == 0) {
         memset(m, 0, sizeof(*m));
         return SDPA_OK;
     }
-    return encode_map(m, ptr, bf16, d, h, tokens, (uint64_t)d * 2, (uint64_t)h * d * 2, 1, 128);
+    const uint64_t rb = (uint64_t)d * elem_bytes(el);
+    return encode_map(m, ptr, el, d, h, tokens, rb, (uint64_t)h * rb, 1, 128);
+}
+int packed_map(CUtensorMap *m, const void *ptr, bool bf16, int d, int h, int64_t tokens) {
+    return packed_map_el(m, ptr, bf16 ? 0 : 1, d, h, tokens);
 }
 
 // fp32 dQ accumulator [rows][d] as a 2-D map with 16 x 32 boxes (64-byte rows,
@@ -426,6 +441,142 @@ int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float 
     return sdpa_varlen_fwd_ex(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q,
                               total_kv, max_seqlen_q, max_seqlen_kv, h, h, d, attn_scale,
                               causal ? SDPA_MASK_CAUSAL : SDPA_MASK_NONE, -1, dtype, stream);
+}
+
+// Checks of the FP8 forward's extra arguments.
+static int check_fp8(int d, int out_dtype, float scale, const float *dq, const float *dk,
+                     const float *dv, const float *so) {
+    if (d != 128) return fail(SDPA_ERR_UNSUPPORTED, "the FP8 forward takes d = 128 (got d=%d)", d);
+    if (out_dtype != SDPA_BF16 && out_dtype != SDPA_FP16 && out_dtype != SDPA_FP8_E4M3)
+        return fail(SDPA_ERR_UNSUPPORTED, "out_dtype %d is not SDPA_BF16, SDPA_FP16 or SDPA_FP8_E4M3",
+                    out_dtype);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(SDPA_ERR_INVALID_ARG, "attn_scale must be finite and > 0 (got %g)", (double)scale);
+    if (!dq || !dk || !dv) return fail(SDPA_ERR_INVALID_ARG, "descale_q, descale_k and descale_v are required");
+    if (out_dtype == SDPA_FP8_E4M3 && !so)
+        return fail(SDPA_ERR_INVALID_ARG, "scale_o is required for an SDPA_FP8_E4M3 output");
+    return SDPA_OK;
+}
+
+int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                 const float *descale_q, const float *descale_k, const float *descale_v,
+                 const float *scale_o, float *amax_o, int b, int h, int h_kv, int s_q, int s_kv,
+                 int d, float attn_scale, int mask, int window_left, int out_dtype,
+                 sdpa_stream_t stream) {
+    int st = check_fp8(d, out_dtype, attn_scale, descale_q, descale_k, descale_v, scale_o);
+    if (st) return st;
+    if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
+    if (b < 0 || s_q < 0 || s_kv < 0)
+        return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d s_q=%d s_kv=%d)", b, s_q, s_kv);
+    const int64_t bh = (int64_t)b * h, bh_kv = (int64_t)b * h_kv;
+    if (bh == 0 || s_q == 0) return ok();
+    const int64_t q_tiles = (s_q + kTileM - 1) / kTileM;
+    if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
+        return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
+    const size_t ob = out_dtype == SDPA_FP8_E4M3 ? 1 : 2;
+    const size_t qbytes = (size_t)bh * s_q * d, kvbytes = (size_t)bh_kv * s_kv * d;
+    const Span in[7] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"},
+                        {descale_q, 4, "descale_q", 4}, {descale_k, 4, "descale_k", 4},
+                        {descale_v, 4, "descale_v", 4}, {scale_o, scale_o ? 4u : 0u, "scale_o", 4}};
+    const Span out[3] = {{o, qbytes * ob, "o"}, {lse, lse ? (size_t)bh * s_q * 4 : 0, "lse"},
+                         {amax_o, amax_o ? 4u : 0u, "amax_o", 4}};
+    if ((st = check_ptrs(in, 7, out, 3))) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev))) return st;
+    if ((st = get_encoder())) return st;
+    CUtensorMap tq, tk, tv;
+    if ((st = dense_map_el(&tq, q, 2, d, s_q, bh))) return st;
+    if ((st = dense_map_el(&tk, k, 2, d, s_kv, bh_kv))) return st;
+    if ((st = dense_map_el(&tv, v, 2, d, s_kv, bh_kv))) return st;
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.err = dev->err;
+    p.bh = (int)bh;
+    p.h = h;
+    p.h_kv = h_kv;
+    p.group = h / h_kv;
+    p.s_q = s_q;
+    p.s_kv = s_kv;
+    p.q_tiles = (int)q_tiles;
+    p.n_units = (int)(q_tiles * bh);
+    p.mask = mask;
+    p.window = window_left;
+    p.scale_log2 = attn_scale * kLog2e;
+    p.descale_q = descale_q;
+    p.descale_k = descale_k;
+    p.descale_v = descale_v;
+    p.scale_o = scale_o;
+    p.amax_o = amax_o;
+    const int grid = std::min(p.n_units, dev->sm_count);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
+        return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
+    return launch_status(launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer), "sdpa_fwd_fp8");
+}
+
+int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
+                        const float *descale_q, const float *descale_k, const float *descale_v,
+                        const float *scale_o, float *amax_o, const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_kv, int num_seqs, int total_q, int total_kv,
+                        int max_seqlen_q, int max_seqlen_kv, int h, int h_kv, int d,
+                        float attn_scale, int mask, int window_left, int out_dtype,
+                        sdpa_stream_t stream) {
+    int st = check_fp8(d, out_dtype, attn_scale, descale_q, descale_k, descale_v, scale_o);
+    if (st) return st;
+    if ((st = check_mask_heads(mask, window_left, h, h_kv))) return st;
+    if ((st = check_varlen_sizes(cu_seqlens_q, cu_seqlens_kv, num_seqs, total_q, total_kv,
+                                 max_seqlen_q, max_seqlen_kv, h)))
+        return st;
+    if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
+    const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;
+    const int64_t slices = (int64_t)num_seqs * h;
+    if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)
+        return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
+    const size_t ob = out_dtype == SDPA_FP8_E4M3 ? 1 : 2;
+    const size_t qbytes = (size_t)total_q * h * d, kvbytes = (size_t)total_kv * h_kv * d;
+    const Span in[9] = {{q, qbytes, "q"}, {k, kvbytes, "k"}, {v, kvbytes, "v"},
+                        {cu_seqlens_q, (size_t)(num_seqs + 1) * 4, "cu_seqlens_q", 4},
+                        {cu_seqlens_kv, (size_t)(num_seqs + 1) * 4, "cu_seqlens_kv", 4},
+                        {descale_q, 4, "descale_q", 4}, {descale_k, 4, "descale_k", 4},
+                        {descale_v, 4, "descale_v", 4}, {scale_o, scale_o ? 4u : 0u, "scale_o", 4}};
+    const Span out[3] = {{o, qbytes * ob, "o"}, {lse, lse ? (size_t)total_q * h * 4 : 0, "lse"},
+                         {amax_o, amax_o ? 4u : 0u, "amax_o", 4}};
+    if ((st = check_ptrs(in, 9, out, 3))) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev))) return st;
+    if ((st = get_encoder())) return st;
+    CUtensorMap tq, tk, tv;
+    if ((st = packed_map_el(&tq, q, 2, d, h, total_q))) return st;
+    if ((st = packed_map_el(&tk, k, 2, d, h_kv, total_kv))) return st;
+    if ((st = packed_map_el(&tv, v, 2, d, h_kv, total_kv))) return st;
+    FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.cu_q = cu_seqlens_q;
+    p.cu_kv = cu_seqlens_kv;
+    p.err = dev->err;
+    p.bh = (int)slices;
+    p.h = h;
+    p.h_kv = h_kv;
+    p.group = h / h_kv;
+    p.num_seqs = num_seqs;
+    p.q_tiles = (int)q_tiles;
+    p.n_units = (int)(q_tiles * slices);
+    p.mask = mask;
+    p.window = window_left;
+    p.scale_log2 = attn_scale * kLog2e;
+    p.descale_q = descale_q;
+    p.descale_k = descale_k;
+    p.descale_v = descale_v;
+    p.scale_o = scale_o;
+    p.amax_o = amax_o;
+    const int grid = std::min(p.n_units, dev->sm_count);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
+        return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
+    return launch_status(launch_fwd_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer),
+                         "sdpa_varlen_fwd_fp8");
 }
 
 static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -30,6 +30,9 @@ enum KernelTag : uint32_t {
 // one) and lo_i = max(0, i + delta - window) for window >= 0 (0 without).
 enum MaskKind : int { kMaskNone = 0, kMaskTopLeft = 1, kMaskBottomRight = 2 };
 
+// Element kinds of inputs and outputs (the values of the ABI's sdpa_dtype).
+enum ElemKind : int { kElBf16 = 0, kElFp16 = 1, kElE4m3 = 2 };
+
 struct FwdParams {
     void *o;                     // output [.. , d] in the I/O dtype
     float *lse;                  // may be null
@@ -48,6 +51,10 @@ struct FwdParams {
     int mask;                    // MaskKind
     int window;                  // window_left, -1 for none
     float scale_log2;            // attn_scale * log2(e)
+    // E4M3 inputs only: per-tensor factors in device memory (fp32 scalars)
+    const float *descale_q, *descale_k, *descale_v;
+    const float *scale_o;        // E4M3 output: O is stored as O * scale_o
+    float *amax_o;               // may be null: receives max |O| (atomic max)
 };
 
 // Key range [lo, hi) of query row i (see MaskKind), for the row order of one
@@ -107,6 +114,10 @@ cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
                        cudaStream_t stream, const KernelTimer &timer);
+// E4M3 inputs, d = 128, output kind `out` (ElemKind), one-tile kernel.
+cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const FwdParams &p, int out, bool packed, int grid, cudaStream_t stream,
+                           const KernelTimer &timer);
 // Deterministic dQ pass (bwd_dq.cu): one CTA per (query slice, query tile);
 // q_tiles = query tiles per slice.  Writes p.dq from the row terms in p.rowx.
 cudaError_t launch_bwd_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

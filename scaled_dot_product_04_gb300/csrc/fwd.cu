@@ -45,21 +45,22 @@
 namespace sdpa {
 namespace {
 
-template <int D>
+// kEb: bytes per input element (2 for bf16/fp16, 1 for E4M3).
+template <int D, int kEb = 2>
 struct FwdLayout {
-    static constexpr int kChunks = D / 64;                // 128-byte swizzle columns per row
-    static constexpr int kChunkBytes = kTileM * 128;      // 16 KiB: 128 rows x 64 elements
+    static constexpr int kChunks = D * kEb / 128;          // 128-byte swizzle columns per row
+    static constexpr int kChunkBytes = kTileM * 128;      // 16 KiB: 128 rows x 128 bytes
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     // K and V have rings of their own: a K stage is released once S = Q K^T
     // has read it, a V stage once O += P V has, so the next loads start early.
-    static constexpr int kKStages = (D == 128) ? 3 : 5;
-    static constexpr int kVStages = (D == 128) ? 2 : 4;
+    static constexpr int kKStages = (kTileBytes >= 32768) ? 3 : 5;
+    static constexpr int kVStages = (kTileBytes >= 32768) ? 2 : 4;
     // Q is double-buffered by unit parity so the next unit's Q arrives while
     // the current unit still runs.
     static constexpr int kQStages = 2;
     // cu_seqlens entries cached in shared memory (longer lists are read from
     // global memory); at d = 128 only the room left by the rings is used.
-    static constexpr int kCuCap = (D == 128) ? 192 : 2048;
+    static constexpr int kCuCap = (kTileBytes >= 32768) ? 192 : 2048;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQStages * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
@@ -157,11 +158,22 @@ SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int 
     return U;
 }
 
-template <int D, bool kBf16, bool kPacked>
+// Element kinds: kEl is the input type (kElBf16, kElFp16 or kElE4m3), kOut
+// the output type (the input type for 16-bit inputs; bf16, fp16 or E4M3 for
+// E4M3 inputs).  E4M3 inputs (cudnn-frontend PR #554, per-tensor FP8
+// forward) carry per-tensor descales read from device memory:
+// descale_q * descale_k folds into the softmax multiplier and descale_v
+// (times scale_o for an E4M3 output) into the output factor; amax_o, if
+// given, receives max |O| of the real-valued output.  P enters P V as E4M3,
+// four per TMEM column; every product is a kind::f8f6f4 MMA of K = 32.
+template <int D, int kEl, bool kPacked, int kOut>
 __global__ void __launch_bounds__(192, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using L = FwdLayout<D>;
+    constexpr bool kFp8 = kEl == kElE4m3;
+    constexpr bool kBf16 = kEl == kElBf16;
+    constexpr int kEb = kFp8 ? 1 : 2;
+    using L = FwdLayout<D, kEb>;
     using io_t = uint16_t;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
-                                bar(L::bVFull + vs), c * 64, y, z);
+                                bar(L::bVFull + vs), c * (128 / kEb), y, z);
                 ++v_it;
                 return true;
             };
@@ -263,7 +275,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kQ + qs * L::kTileBytes + c * L::kChunkBytes, &tm_q,
-                                bar(L::bQFull + qs), c * 64, qy, qz);
+                                bar(L::bQFull + qs), c * (128 / kEb), qy, qz);
                 ++units;
                 for (int j = 0; j < U.n_kv; ++j) {
                     const int k0 = (U.kt0 + j) * kTileN;
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
                         tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
-                                    bar(L::bKFull + ks), c * 64, ky, kz);
+                                    bar(L::bKFull + ks), c * (128 / kEb), ky, kz);
                     ++k_it;
                     if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
                     pv_y = ky;
@@ -299,30 +311,40 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_s = make_idesc_f16(kTileM, kTileN, kBf16, false, false);
-            constexpr uint32_t idesc_o = make_idesc_f16(kTileM, D, kBf16, false, true);
-            // S = Q K^T: both operands K-major (head dim contiguous), 16 per step.
+            constexpr uint32_t idesc_s = kFp8 ? make_idesc_e4m3(kTileM, kTileN, false, false)
+                                              : make_idesc_f16(kTileM, kTileN, kBf16, false, false);
+            constexpr uint32_t idesc_o = kFp8 ? make_idesc_e4m3(kTileM, D, false, true)
+                                              : make_idesc_f16(kTileM, D, kBf16, false, true);
+            // S = Q K^T: both operands K-major (head dim contiguous), 32 bytes
+            // (16 bf16 or 32 E4M3 elements) per step.
             int units = 0;  // live units processed by this CTA (selects the Q buffer)
             auto issue_s = [&](int ks, uint32_t col) {
                 const uint32_t qs = sbase + L::kQ + (units & 1) * L::kTileBytes;
                 const uint32_t kb = sbase + L::kK + ks * L::kTileBytes;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 0; k < D * kEb / 32; ++k) {
                     const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
-                    mma_ss(tmem + col, smem_desc_sw128(qs + off, 16, 1024),
-                           smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                    if constexpr (kFp8)
+                        mma_ss_f8(tmem + col, smem_desc_sw128(qs + off, 16, 1024),
+                                  smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                    else
+                        mma_ss(tmem + col, smem_desc_sw128(qs + off, 16, 1024),
+                               smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
                 }
             };
-            // O += P V: P from TMEM (two bf16 per column, 8 columns per 16 keys),
-            // V MN-major (head dim contiguous); 64-wide head-dim halves are
-            // 16 KiB apart (leading offset), 8-key groups 1 KiB apart.
+            // O += P V: P from TMEM (8 columns per step: 16 keys as bf16 pairs
+            // or 32 keys as E4M3 quads), V MN-major (head dim contiguous);
+            // 128-byte head-dim chunks are 16 KiB apart (leading offset),
+            // 8-key groups 1 KiB apart, so a step advances 2 or 4 KiB.
             auto issue_pv = [&](int vs, uint32_t pcol, uint32_t ocol, bool acc) {
                 const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
 #pragma unroll
-                for (int k = 0; k < kTileN / 16; ++k) {
-                    mma_ts(tmem + ocol, tmem + pcol + k * 8,
-                           smem_desc_sw128(vb + k * 2048, L::kChunkBytes, 1024), idesc_o,
-                           (acc || k > 0) ? 1u : 0u);
+                for (int k = 0; k < kTileN * kEb / 32; ++k) {
+                    const uint64_t vdesc = smem_desc_sw128(vb + k * (4096 / kEb), L::kChunkBytes, 1024);
+                    if constexpr (kFp8)
+                        mma_ts_f8(tmem + ocol, tmem + pcol + k * 8, vdesc, idesc_o, (acc || k > 0) ? 1u : 0u);
+                    else
+                        mma_ts(tmem + ocol, tmem + pcol + k * 8, vdesc, idesc_o, (acc || k > 0) ? 1u : 0u);
                 }
             };
             // S_x goes to S buffer x&1, which held P_{x-2}: it waits for that
@@ -380,7 +402,14 @@ __global__ void __launch_bounds__(192, 1)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row of the tile == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-        const float sl2 = p.scale_log2;
+        float sl2 = p.scale_log2;
+        float o_factor = 1.f;  // descale_v (times scale_o for an E4M3 output)
+        if constexpr (kFp8) {
+            sl2 *= *p.descale_q * *p.descale_k;
+            o_factor = *p.descale_v;
+        }
+        constexpr int kOb = kOut == kElE4m3 ? 1 : 2;  // output bytes per element
+        float amax = 0.f;  // max |O| over this thread's rows (E4M3 inputs)
         // A unit's epilogue (O / l, LSE) is deferred until the next unit's
         // first P is out, so the MMA warp has work while O is written.
         struct Pending {
@@ -388,14 +417,14 @@ __global__ void __launch_bounds__(192, 1)
             bool row_ok;
             int unit;
             float l, m;
-            io_t *orow;
+            uint8_t *orow;
             float *lse;
         } pend{false, false, 0, 0.f, 0.f, nullptr, nullptr};
         auto epilogue = [&]() -> bool {
             const int ob = pend.unit & 1;
             if (!warp_wait(bar(L::bOFull + ob), (pend.unit >> 1) & 1, wc, 14)) return false;
             tc_fence_after();
-            const float inv_l = (pend.l > 0.f) ? 1.f / pend.l : 0.f;
+            const float inv_l = (pend.l > 0.f) ? o_factor / pend.l : 0.f;
             const uint32_t ocol = L::kColO + ob * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -406,16 +435,37 @@ __global__ void __launch_bounds__(192, 1)
                     tc_fence_before();
                     mbar_arrive(bar(L::bOFree + ob));
                 }
-                uint32_t pk[16];
+                if constexpr (kFp8) {
+                    if (pend.row_ok) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
-                                         __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (pend.row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(pend.orow + c * 32);
+                        for (int i = 0; i < 32; ++i)
+                            amax = fmaxf(amax, fabsf(__uint_as_float(o[i]) * inv_l));
+                    }
+                }
+                if constexpr (kOut == kElE4m3) {
+                    const float so = inv_l * *p.scale_o;
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int i = 0; i < 8; ++i)
+                        pk[i] = pack_e4m3x4(__uint_as_float(o[4 * i]) * so, __uint_as_float(o[4 * i + 1]) * so,
+                                            __uint_as_float(o[4 * i + 2]) * so, __uint_as_float(o[4 * i + 3]) * so);
+                    if (pend.row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(pend.orow + c * 32 * kOb);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                } else {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack2<kOut == kElBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                                       __uint_as_float(o[2 * i + 1]) * inv_l);
+                    if (pend.row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(pend.orow + c * 32 * kOb);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
                 }
             }
             if (pend.row_ok && pend.lse)
@@ -432,14 +482,14 @@ __global__ void __launch_bounds__(192, 1)
             if (!U.live) continue;
             const int q_idx = U.row0 + r;
             const bool row_ok = q_idx < U.Lq;
-            io_t *orow = reinterpret_cast<io_t *>(p.o) + U.o_row0 + (int64_t)q_idx * U.o_rs;
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + (U.o_row0 + (int64_t)q_idx * U.o_rs) * kOb;
             float *lse_ptr = p.lse ? p.lse + U.lse_row0 + (int64_t)q_idx * U.lse_rs : nullptr;
             if (U.n_kv == 0) {
                 // No key is visible to any row of this tile: O = 0, LSE = -inf.
                 if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-                    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < D * kOb / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
                     if (lse_ptr) *lse_ptr = -INFINITY;
                 }
                 continue;
@@ -489,17 +539,36 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const float base = (m_used == -INFINITY) ? 0.f : m_used;
                 const uint64_t sl2_2 = f2_pack(sl2, sl2), nbase_2 = f2_pack(-base, -base);
-                // P = exp2(s * scale*log2e - base), pairs packed in place into s[0..64)
+                // P = exp2(s * scale*log2e - base), packed in place into s[0..64)
+                // as bf16/fp16 pairs, or into s[0..32) as E4M3 quads
                 uint64_t sum2[4] = {0, 0, 0, 0};
+                if constexpr (kFp8) {
 #pragma unroll
-                for (int i = 0; i < kTileN / 2; ++i) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
-                                     sl2_2, nbase_2),
-                              x0, x1);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
-                    s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
+                    for (int i = 0; i < kTileN / 4; ++i) {
+                        float x0, x1, x2, x3;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1])),
+                                         sl2_2, nbase_2),
+                                  x0, x1);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])),
+                                         sl2_2, nbase_2),
+                                  x2, x3);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                        sum2[(2 * i) & 3] = f2_add(sum2[(2 * i) & 3], f2_pack(p0, p1));
+                        sum2[(2 * i + 1) & 3] = f2_add(sum2[(2 * i + 1) & 3], f2_pack(p2, p3));
+                        s[i] = pack_e4m3x4(p0, p1, p2, p3);  // i <= 4i: packs in place
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kTileN / 2; ++i) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                         sl2_2, nbase_2),
+                                  x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+                        s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
+                    }
                 }
                 {
                     float a0, a1;
@@ -507,7 +576,7 @@ __global__ void __launch_bounds__(192, 1)
                     l += a0 + a1;
                 }
                 tmem_st32(t_lane + cs, s);
-                tmem_st32(t_lane + cs + 32, s + 32);
+                if constexpr (!kFp8) tmem_st32(t_lane + cs + 32, s + 32);
 
                 if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                     // O holds the unit's earlier P V products; it may be rescaled
@@ -536,6 +605,14 @@ __global__ void __launch_bounds__(192, 1)
             ++units;
         }
         if (ok && pend.on) epilogue();
+        if constexpr (kFp8) {
+            // max |O| of the CTA's rows into the caller's amax (non-negative
+            // floats order as their bit patterns)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            if (p.amax_o && lane == 0 && amax > 0.f)
+                atomicMax(reinterpret_cast<int *>(p.amax_o), __float_as_int(amax));
+        }
     }
 
     tc_fence_before();
@@ -546,12 +623,12 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int D, bool kBf16, bool kPacked>
+template <int D, int kEl, bool kPacked, int kOut>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdParams &p, int grid, cudaStream_t stream,
                          const KernelTimer &timer) {
-    using L = FwdLayout<D>;
-    auto kern = fwd_kernel<D, kBf16, kPacked>;
+    using L = FwdLayout<D, kEl == kElE4m3 ? 1 : 2>;
+    auto kern = fwd_kernel<D, kEl, kPacked, kOut>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);
     if (e != cudaSuccess) return e;
@@ -567,18 +644,34 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
                        cudaStream_t stream, const KernelTimer &timer) {
-#define SDPA_FWD_CASE(D_, BF_, PK_)                                            \
-    if (d == D_ && bf16 == BF_ && packed == PK_)                               \
-        return launch_fwd_t<D_, BF_, PK_>(tq, tk, tv, p, grid, stream, timer);
-    SDPA_FWD_CASE(64, true, false)
-    SDPA_FWD_CASE(64, true, true)
-    SDPA_FWD_CASE(64, false, false)
-    SDPA_FWD_CASE(64, false, true)
-    SDPA_FWD_CASE(128, true, false)
-    SDPA_FWD_CASE(128, true, true)
-    SDPA_FWD_CASE(128, false, false)
-    SDPA_FWD_CASE(128, false, true)
+#define SDPA_FWD_CASE(D_, EL_, PK_)                                            \
+    if (d == D_ && (bf16 ? kElBf16 : kElFp16) == EL_ && packed == PK_)         \
+        return launch_fwd_t<D_, EL_, PK_, EL_>(tq, tk, tv, p, grid, stream, timer);
+    SDPA_FWD_CASE(64, kElBf16, false)
+    SDPA_FWD_CASE(64, kElBf16, true)
+    SDPA_FWD_CASE(64, kElFp16, false)
+    SDPA_FWD_CASE(64, kElFp16, true)
+    SDPA_FWD_CASE(128, kElBf16, false)
+    SDPA_FWD_CASE(128, kElBf16, true)
+    SDPA_FWD_CASE(128, kElFp16, false)
+    SDPA_FWD_CASE(128, kElFp16, true)
 #undef SDPA_FWD_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const FwdParams &p, int out, bool packed, int grid, cudaStream_t stream,
+                           const KernelTimer &timer) {
+#define SDPA_FP8_CASE(OUT_, PK_)                                               \
+    if (out == OUT_ && packed == PK_)                                          \
+        return launch_fwd_t<128, kElE4m3, PK_, OUT_>(tq, tk, tv, p, grid, stream, timer);
+    SDPA_FP8_CASE(kElBf16, false)
+    SDPA_FP8_CASE(kElBf16, true)
+    SDPA_FP8_CASE(kElFp16, false)
+    SDPA_FP8_CASE(kElFp16, true)
+    SDPA_FP8_CASE(kElE4m3, false)
+    SDPA_FP8_CASE(kElE4m3, true)
+#undef SDPA_FP8_CASE
     return cudaErrorInvalidValue;
 }
 

@@ -108,3 +108,27 @@ def make(w: Workload, dtype: torch.dtype = torch.bfloat16):
     q, k, v, do, cu_q, cu_kv = packed(lens, lens, w.h, w.d, w.seed, dtype, w.qk_mult)
     return dict(q=q, k=k, v=v, do=do, cu_q=cu_q, cu_kv=cu_kv, lengths=lens)
 
+
+
+def fp8_quantize(x: torch.Tensor):
+    """Per-tensor E4M3 encoding of a synthetic tensor: codes (uint8) of x * s
+    with s = 448 / max|x| (the largest code maps to the largest magnitude),
+    and the descale 1 / s as a float.  Input generation only."""
+    amax = float(x.abs().max())
+    s = 448.0 / amax if amax > 0 else 1.0
+    codes = (x.float() * s).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, 1.0 / s
+
+
+def fp8_dense(b: int, h: int, s_q: int, s_kv: int, d: int, seed: int, h_kv: int | None = None):
+    """E4M3 codes of Q [b,h,s_q,d], K/V [b,h_kv,s_kv,d] drawn N(0,1), with their descales."""
+    q, k, v, _ = dense(b, h, s_q, s_kv, d, seed, torch.float32, h_kv=h_kv)
+    (qc, dq), (kc, dk), (vc, dv) = fp8_quantize(q), fp8_quantize(k), fp8_quantize(v)
+    return qc, kc, vc, dq, dk, dv
+
+
+def fp8_packed(lengths_q, lengths_kv, h: int, d: int, seed: int, h_kv: int | None = None):
+    """E4M3 codes of packed Q/K/V, their descales and the two cu_seqlens."""
+    q, k, v, _, cu_q, cu_kv = packed(lengths_q, lengths_kv, h, d, seed, torch.float32, h_kv=h_kv)
+    (qc, dq), (kc, dk), (vc, dv) = fp8_quantize(q), fp8_quantize(k), fp8_quantize(v)
+    return qc, kc, vc, dq, dk, dv, cu_q, cu_kv
