@@ -16,6 +16,12 @@ so the scaling is weak; the time is the maximum over ranks.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead, on
 a bounded sample of the same workload (rank 0 only).
+
+``--variant`` measures the widened rows on the same workload (the headline
+line is the default, bf16): ``deterministic`` runs the backward with its
+deterministic dQ pass (the backward timer then spans the main kernel and the
+dQ pass), ``fp8`` times the E4M3 forward alone (bf16 output) against the FP8
+tensor peak (the measured bf16 peak x 2, the nominal FP8/BF16 ratio).
 """
 from __future__ import annotations
 
@@ -62,6 +68,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--variant", choices=["bf16", "deterministic", "fp8"], default="bf16",
+                    help="bf16 (default, the headline), deterministic backward, or FP8 forward")
     return ap.parse_args()
 
 
@@ -226,24 +234,43 @@ def run_ours(args):
     t = sdpa_inputs.make(w)
     b, h, s, d = w.b, w.h, w.s, w.d
     scale, causal = w.scale, int(w.causal)
+    variant = args.variant
+    fp8 = variant == "fp8"
+    det = 1 if variant == "deterministic" else 0
+    if fp8:
+        # E4M3 codes of the workload's own Q, K, V with per-tensor descales
+        enc = [sdpa_inputs.fp8_quantize(t[x].float()) for x in ("q", "k", "v")]
+        t = dict(t, q=enc[0][0], k=enc[1][0], v=enc[2][0])
+        descales = [torch.tensor([e[1]], dtype=torch.float32, device=dev) for e in enc]
     q, k, v, do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((b, h, s), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(sdpa.sdpa_bwd_workspace_size(b, h, s, d), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(do), torch.empty_like(do), torch.empty_like(do)
+    ws = torch.empty(max(1, sdpa.sdpa_bwd_ex_workspace_size(b, h, s, d, det)), dtype=torch.uint8,
+                     device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     f_fwd = fwd_flops(w)
-    f_step = f_fwd * (1.0 + BWD_FACTOR)
+    f_step = f_fwd if fp8 else f_fwd * (1.0 + BWD_FACTOR)
 
     def step(ev_f=None, ev_b=None):
         if ev_f:
             sdpa.sdpa_set_kernel_timer(*ev_f)
+        if fp8:
+            sdpa.sdpa_fwd_fp8(q, k, v, o, lse, *descales, None, amax, b, h, h, s, s, d, scale,
+                              causal, -1, 0, stream)
+            sdpa.sdpa_set_kernel_timer(None, None)
+            return
         sdpa.sdpa_fwd(q, k, v, o, lse, b, h, s, s, d, scale, causal, 0, stream)
         if ev_b:
             sdpa.sdpa_set_kernel_timer(*ev_b)
-        sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, b, h, s, s, d, scale, causal, 0, ws,
-                      ws.numel(), stream)
+        if det:
+            sdpa.sdpa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, b, h, h, s, s, d, scale, causal, -1,
+                             1, 0, ws, ws.numel(), stream)
+        else:
+            sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, b, h, s, s, d, scale, causal, 0, ws,
+                          ws.numel(), stream)
         sdpa.sdpa_set_kernel_timer(None, None)
 
     for _ in range(args.warmup):
@@ -282,7 +309,7 @@ def run_ours(args):
 
     step_ms = [a.elapsed_time(bb) for a, bb, _, _ in ev]
     fwd_ms = [f[0].elapsed_time(f[1]) for _, _, f, _ in ev]
-    bwd_ms = [g[0].elapsed_time(g[1]) for _, _, _, g in ev]
+    bwd_ms = [0.0 if fp8 else g[0].elapsed_time(g[1]) for _, _, _, g in ev]
     total_ms = sum(step_ms)
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
@@ -294,18 +321,20 @@ def run_ours(args):
     # ------------------------------------------------------------ end to end
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv, hdo = (t[x].pin_memory() for x in ("q", "k", "v", "do"))
-        ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-                             for x in (o, dq, dk, dv))
-        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        ins = [(t[x].pin_memory(), dv_) for x, dv_ in (("q", q), ("k", k), ("v", v), ("do", do))
+               if not (fp8 and x == "do")]
+        outs = [(torch.empty(x.shape, dtype=x.dtype, pin_memory=True), x)
+                for x in ((o, lse) if fp8 else (o, lse, dq, dk, dv))]
+        hq, hk, hv = ins[0][0], ins[1][0], ins[2][0]
+        hdo = ins[3][0] if len(ins) > 3 else None
+        ho, hlse = outs[0][0], outs[1][0]
+        hdq, hdk, hdv = (x[0] for x in outs[2:]) if not fp8 else (None, None, None)
 
         def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            do.copy_(hdo, non_blocking=True)
+            for src, dst in ins:
+                dst.copy_(src, non_blocking=True)
             step()
-            for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            for dst, src in outs:
                 dst.copy_(src, non_blocking=True)
 
         n_e2e = max(3, min(args.steps, 10))
@@ -318,8 +347,8 @@ def run_ours(args):
         z.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = a.elapsed_time(z) / n_e2e
-        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
-        d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+        h2d = sum(x.numel() * x.element_size() for x, _ in ins)
+        d2h = sum(x.numel() * x.element_size() for x, _ in outs)
         e2e = {"value": world * f_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
@@ -327,31 +356,36 @@ def run_ours(args):
     peaks, peak_src = read_peaks()
     mean_f, mean_b = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
     kern = "bwd_main" if sum(bwd_ms) >= sum(fwd_ms) else "fwd"
-    k_flops = f_fwd * BWD_FACTOR if kern == "bwd_main" else f_fwd
-    k_ms = mean_b if kern == "bwd_main" else mean_f
+    if det and kern == "bwd_main":
+        kern = "bwd_main+dq"
+    k_flops = f_fwd * BWD_FACTOR if kern.startswith("bwd") else f_fwd
+    k_ms = mean_b if kern.startswith("bwd") else mean_f
     achieved = k_flops / (k_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops_sustained"])
+    ratio = 2.0 if fp8 else 1.0  # nominal FP8 / BF16 dense tensor rate
+    peak = float(peaks["bf16_tflops_sustained"]) * ratio
     version = sdpa.sdpa_version()
     tr = TRAFFIC.get((kern, version))
+    src = (f"{peak_src} sustained bf16 (MEASURED_PEAKS.json)" if peak_src == "measured"
+           else "fallback sustained bf16")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": tr, "kernel": kern,
-                "peak_source": f"{peak_src} sustained bf16 (MEASURED_PEAKS.json)"
-                if peak_src == "measured" else "fallback sustained bf16"}
-    burst = float(peaks["bf16_tflops"])
+                "peak_source": src + (" x 2 (nominal FP8/BF16 ratio)" if fp8 else "")}
+    burst = float(peaks["bf16_tflops"]) * ratio
     phases = {
         "fwd_kernel": {"ms": mean_f, "tflops": f_fwd / (mean_f * 1e-3) / 1e12,
                        "frac_sustained": f_fwd / (mean_f * 1e-3) / 1e12 / peak,
                        "frac_burst": f_fwd / (mean_f * 1e-3) / 1e12 / burst},
-        "bwd_main_kernel": {"ms": mean_b,
-                            "tflops": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12,
-                            "frac_sustained": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12 / peak,
-                            "frac_burst": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12 / burst},
+        "bwd_main_kernel": None if fp8 else {
+            "ms": mean_b, "tflops": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12,
+            "frac_sustained": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12 / peak,
+            "frac_burst": f_fwd * BWD_FACTOR / (mean_b * 1e-3) / 1e12 / burst,
+            "kernels": "main + deterministic dQ pass" if det else "main"},
         "bwd_pre_and_convert_ms": statistics.mean(
             sm - fm - bm for sm, fm, bm in zip(step_ms, fwd_ms, bwd_ms)),
     }
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         rate, spent, n, threads = oracle_sample_rate(w, t, min_s=10.0, max_s=30.0)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} heads of {w.name}, each cut to its first "
@@ -361,17 +395,21 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) bf16" + (", Q and K x2)" if w.qk_mult != 1 else ")"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if fp8 else "bf16",
+            "data": "synthetic (seeded N(0,1) bf16" + (", Q and K x2" if w.qk_mult != 1 else "")
+                    + (", encoded as E4M3 with per-tensor descales)" if fp8 else ")"),
             "config": {"workload": w.name, "b": b, "h": h, "s_q": s, "s_kv": s, "d": d,
-                       "causal": bool(causal), "layout": "bhsd",
-                       "step": "fwd (O, LSE) + bwd (dQ, dK, dV)",
+                       "causal": bool(causal), "layout": "bhsd", "variant": variant,
+                       "step": ("FP8 fwd (O bf16, LSE, amax)" if fp8 else
+                                "fwd (O, LSE) + bwd (dQ, dK, dV)"
+                                + (", deterministic dQ pass" if det else "")),
                        "flops_per_step": f_step, "pct_of_peak": 100.0 * value / world / peak,
                        "l2": "a 512 MiB buffer (> L2) is written between timed steps; "
                              "inputs+outputs total %d MiB" % ((4 * q.numel() + 2 * k.numel() * 2)
                                                               * 2 >> 20),
                        "parallelism": f"replicas x{world}"},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": 4 * args.steps,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": (1 if fp8 else 4) * args.steps,
             "roofline": roofline, "phases": phases, "cpu_baseline": cpu,
             "library": version,
         }

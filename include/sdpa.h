@@ -326,7 +326,8 @@ int sdpa_check_device_error(sdpa_stream_t stream);
  * Measurement hook (no counterpart on the pages).  While both events are
  * non-NULL, every later call on this host thread records `start_event` on
  * its stream immediately before launching its main kernel (the forward
- * kernel, or the backward's main kernel) and `stop_event` immediately after,
+ * kernel, or the backward's main kernel, followed in deterministic mode by
+ * its dQ pass) and `stop_event` immediately after,
  * so a caller can time that kernel alone with cudaEventElapsedTime.  The
  * events are cudaEvent_t handles owned by the caller; pass NULL, NULL to
  * stop.  Recording adds no synchronisation.

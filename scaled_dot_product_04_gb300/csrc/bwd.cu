@@ -713,9 +713,14 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     if (timer.start) cudaEventRecord(timer.start, stream);
     kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, trx, p);
     e = cudaGetLastError();
+    if (p.deterministic) {
+        // the timed span covers the main kernel and the dQ pass
+        if (e == cudaSuccess) e = launch_bwd_dq(tq, tk, tv, tdo, p, p.q_tiles, D, kBf16, kPacked, stream);
+        if (timer.stop) cudaEventRecord(timer.stop, stream);
+        return e;
+    }
     if (timer.stop) cudaEventRecord(timer.stop, stream);
     if (e != cudaSuccess) return e;
-    if (p.deterministic) return launch_bwd_dq(tq, tk, tv, tdo, p, p.q_tiles, D, kBf16, kPacked, stream);
     bwd_dq_convert_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(p, rows);
     return cudaGetLastError();
 }
