@@ -319,38 +319,88 @@ def run_ours(args):
     clocks = sampler.summary(t0, t1)
 
     # ------------------------------------------------------------ end to end
+    # Each step copies its inputs from pinned host memory, runs the path and
+    # copies its results back.  Two device buffer sets and two copy streams
+    # (host->device and device->host, one copy engine each) let step i's
+    # copies overlap the compute of steps i-1 and i+1; every step's own
+    # copies stay inside the timed region.
     e2e = None
     if not args.no_e2e:
-        ins = [(t[x].pin_memory(), dv_) for x, dv_ in (("q", q), ("k", k), ("v", v), ("do", do))
-               if not (fp8 and x == "do")]
-        outs = [(torch.empty(x.shape, dtype=x.dtype, pin_memory=True), x)
-                for x in ((o, lse) if fp8 else (o, lse, dq, dk, dv))]
-        hq, hk, hv = ins[0][0], ins[1][0], ins[2][0]
-        hdo = ins[3][0] if len(ins) > 3 else None
-        ho, hlse = outs[0][0], outs[1][0]
-        hdq, hdk, hdv = (x[0] for x in outs[2:]) if not fp8 else (None, None, None)
+        names_in = ["q", "k", "v"] + ([] if fp8 else ["do"])
+        host_in = [t[x].pin_memory() for x in names_in]
 
-        def e2e_step():
-            for src, dst in ins:
-                dst.copy_(src, non_blocking=True)
-            step()
-            for dst, src in outs:
-                dst.copy_(src, non_blocking=True)
+        def dev_set():
+            ins = [torch.empty(x.shape, dtype=x.dtype, device=dev) for x in host_in]
+            outs = [torch.empty_like(o), torch.empty_like(lse)]
+            if not fp8:
+                outs += [torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)]
+            return ins, outs
+
+        sets = [dev_set(), dev_set()]
+        host_out = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in sets[0][1]]
+                    for _ in range(2)]
+        ws2 = [ws, torch.empty_like(ws)]
+        h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def run_step(i):
+            ins, outs = sets[i & 1]
+            qq, kk, vv = ins[0], ins[1], ins[2]
+            oo, ll = outs[0], outs[1]
+            if fp8:
+                sdpa.sdpa_fwd_fp8(qq, kk, vv, oo, ll, *descales, None, amax, b, h, h, s, s, d,
+                                  scale, causal, -1, 0, stream)
+                return
+            ddo = ins[3]
+            gq, gk, gv = outs[2], outs[3], outs[4]
+            sdpa.sdpa_fwd(qq, kk, vv, oo, ll, b, h, s, s, d, scale, causal, 0, stream)
+            wsi = ws2[i & 1]
+            if det:
+                sdpa.sdpa_bwd_ex(qq, kk, vv, oo, ddo, ll, gq, gk, gv, b, h, h, s, s, d, scale,
+                                 causal, -1, 1, 0, wsi, wsi.numel(), stream)
+            else:
+                sdpa.sdpa_bwd(qq, kk, vv, oo, ddo, ll, gq, gk, gv, b, h, s, s, d, scale, causal, 0,
+                              wsi, wsi.numel(), stream)
+
+        def pipeline(n):
+            free = [None, None]  # device->host copy of the set's last results done
+            for i in range(n):
+                st = i & 1
+                ins, outs = sets[st]
+                with torch.cuda.stream(h2d):
+                    if free[st] is not None:
+                        h2d.wait_event(free[st])
+                    for dst, src in zip(ins, host_in):
+                        dst.copy_(src, non_blocking=True)
+                    ready = torch.cuda.Event()
+                    ready.record(h2d)
+                stream.wait_event(ready)
+                run_step(i)
+                done = torch.cuda.Event()
+                done.record(stream)
+                with torch.cuda.stream(d2h):
+                    d2h.wait_event(done)
+                    for dst, src in zip(host_out[st], outs):
+                        dst.copy_(src, non_blocking=True)
+                    free[st] = torch.cuda.Event()
+                    free[st].record(d2h)
 
         n_e2e = max(3, min(args.steps, 10))
-        e2e_step()
+        pipeline(2)
         torch.cuda.synchronize(dev)
-        a, z = new_ev(), new_ev()
-        a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        z.record(stream)
+        ev_a, ev_z = new_ev(), new_ev()
+        ev_a.record(h2d)             # before the first step's first copy
+        pipeline(n_e2e)
+        ev_z.record(d2h)             # after the last step's last copy
         torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(z) / n_e2e
-        h2d = sum(x.numel() * x.element_size() for x, _ in ins)
-        d2h = sum(x.numel() * x.element_size() for x, _ in outs)
+        e_ms = ev_a.elapsed_time(ev_z) / n_e2e
+        h2d_bytes = sum(x.numel() * x.element_size() for x in host_in)
+        d2h_bytes = sum(x.numel() * x.element_size() for x in host_out[0])
         e2e = {"value": world * f_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "ms_per_step": e_ms,
+               "copies": "pinned host buffers; two copy streams overlap each step's copies "
+                         "with the neighbouring steps' compute; CUDA events before the first "
+                         "copy and after the last"}
 
     # ------------------------------------------------------------ roofline
     peaks, peak_src = read_peaks()
