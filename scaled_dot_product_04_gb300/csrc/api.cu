@@ -470,7 +470,9 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
         return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d s_q=%d s_kv=%d)", b, s_q, s_kv);
     const int64_t bh = (int64_t)b * h, bh_kv = (int64_t)b * h_kv;
     if (bh == 0 || s_q == 0) return ok();
-    const int64_t q_tiles = (s_q + kTileM - 1) / kTileM;
+    const bool pair = window_left < 0 && use_pair_kernel(false, d, s_q, s_kv);
+    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
+    const int64_t q_tiles = (s_q + unit_rows - 1) / unit_rows;
     if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
     const size_t ob = out_dtype == SDPA_FP8_E4M3 ? 1 : 2;
@@ -512,7 +514,9 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
-    return launch_status(launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer), "sdpa_fwd_fp8");
+    return launch_status(pair ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer)
+                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer),
+                         "sdpa_fwd_fp8");
 }
 
 int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -529,7 +533,9 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;
+    const bool pair = window_left < 0 && use_pair_kernel(true, d, max_seqlen_q, max_seqlen_kv);
+    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
+    const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
     const int64_t slices = (int64_t)num_seqs * h;
     if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
@@ -575,7 +581,8 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
-    return launch_status(launch_fwd_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer),
+    return launch_status(pair ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer)
+                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer),
                          "sdpa_varlen_fwd_fp8");
 }
 

@@ -114,7 +114,10 @@ cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
                        cudaStream_t stream, const KernelTimer &timer);
-// E4M3 inputs, d = 128, output kind `out` (ElemKind), one-tile kernel.
+// E4M3 inputs, d = 128, output kind `out` (ElemKind): one-tile and two-tile kernels.
+cudaError_t launch_fwd_pair_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                const FwdParams &p, int out, bool packed, int grid,
+                                cudaStream_t stream, const KernelTimer &timer);
 cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const FwdParams &p, int out, bool packed, int grid, cudaStream_t stream,
                            const KernelTimer &timer);

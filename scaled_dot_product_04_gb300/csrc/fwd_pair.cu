@@ -35,14 +35,15 @@ namespace {
 constexpr int kPairThreads = 384;
 constexpr int kPairRows = 2 * kTileM;  // query rows per work unit
 
-template <int D>
+// kEb: bytes per input element (2 for bf16/fp16, 1 for E4M3).
+template <int D, int kEb = 2>
 struct PairLayout {
-    static constexpr int kChunks = D / 64;            // 128-byte swizzle columns per row
-    static constexpr int kChunkBytes = kTileM * 128;  // 16 KiB: 128 rows x 64 elements
+    static constexpr int kChunks = D * kEb / 128;     // 128-byte swizzle columns per row
+    static constexpr int kChunkBytes = kTileM * 128;  // 16 KiB: 128 rows x 128 bytes
     static constexpr int kTileBytes = kChunks * kChunkBytes;
-    static constexpr int kKStages = (D == 128) ? 3 : 5;
-    static constexpr int kVStages = (D == 128) ? 2 : 4;
-    static constexpr int kCuCap = (D == 128) ? 192 : 2048;  // cu_seqlens entries cached
+    static constexpr int kKStages = (kTileBytes >= 32768) ? 3 : 5;
+    static constexpr int kVStages = (kTileBytes >= 32768) ? 2 : 4;
+    static constexpr int kCuCap = (kTileBytes >= 32768) ? 192 : 2048;  // cu_seqlens entries cached
     static constexpr int kQ = 0;                             // Q_A, Q_B
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
@@ -139,12 +140,17 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
     return U;
 }
 
-template <int D, bool kBf16, bool kPacked>
+// kEl / kOut: input and output element kinds as in fwd.cu (E4M3 inputs with
+// device descales, P as E4M3 quads, kind::f8f6f4 products; amax of O).
+template <int D, int kEl, bool kPacked, int kOut>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using L = PairLayout<D>;
-    using io_t = uint16_t;
+    constexpr bool kFp8 = kEl == kElE4m3;
+    constexpr bool kBf16 = kEl == kElBf16;
+    constexpr int kEb = kFp8 ? 1 : 2;
+    constexpr int kOb = kOut == kElE4m3 ? 1 : 2;
+    using L = PairLayout<D, kEb>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
-                                bar(L::bVFull + vs), c * 64, y, z);
+                                bar(L::bVFull + vs), c * (128 / kEb), y, z);
                 ++v_it;
                 return true;
             };
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
                         tma_load_3d(sbase + L::kQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q,
-                                    bar(L::bQFull), c * 64, qy, qz);
+                                    bar(L::bQFull), c * (128 / kEb), qy, qz);
                 }
                 ++units;
                 for (int j = 0; j < nmax; ++j) {
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
                         tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
-                                    bar(L::bKFull + ks), c * 64, ky, kz);
+                                    bar(L::bKFull + ks), c * (128 / kEb), ky, kz);
                     ++k_it;
                     if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
                     pv_y = ky;
@@ -277,29 +283,41 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_s = make_idesc_f16(kTileM, kTileN, kBf16, false, false);
-            constexpr uint32_t idesc_o = make_idesc_f16(kTileM, D, kBf16, false, true);
-            // S_X = Q_X K^T: both operands K-major (head dim contiguous), 16 per step.
+            constexpr uint32_t idesc_s = kFp8 ? make_idesc_e4m3(kTileM, kTileN, false, false)
+                                              : make_idesc_f16(kTileM, kTileN, kBf16, false, false);
+            constexpr uint32_t idesc_o = kFp8 ? make_idesc_e4m3(kTileM, D, false, true)
+                                              : make_idesc_f16(kTileM, D, kBf16, false, true);
+            // S_X = Q_X K^T: both operands K-major (head dim contiguous), 32
+            // bytes (16 bf16 or 32 E4M3 elements) per step.
             auto issue_s = [&](int x, int ks) {
                 const uint32_t qb = sbase + L::kQ + x * L::kTileBytes;
                 const uint32_t kb = sbase + L::kK + ks * L::kTileBytes;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 0; k < D * kEb / 32; ++k) {
                     const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
-                    mma_ss(tmem + L::kColS + x * 128, smem_desc_sw128(qb + off, 16, 1024),
-                           smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                    if constexpr (kFp8)
+                        mma_ss_f8(tmem + L::kColS + x * 128, smem_desc_sw128(qb + off, 16, 1024),
+                                  smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                    else
+                        mma_ss(tmem + L::kColS + x * 128, smem_desc_sw128(qb + off, 16, 1024),
+                               smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
                 }
             };
-            // O_X += P_X V: P from TMEM (two bf16 per column, 8 columns per 16
-            // keys), V MN-major (head dim contiguous); 64-wide head-dim halves
-            // are 16 KiB apart (leading offset), 8-key groups 1 KiB apart.
+            // O_X += P_X V: P from TMEM (8 columns per step: 16 keys as bf16
+            // pairs or 32 keys as E4M3 quads), V MN-major (head dim
+            // contiguous); 128-byte head-dim chunks are 16 KiB apart (leading
+            // offset), 8-key groups 1 KiB apart.
             auto issue_pv = [&](int x, int vs, bool acc) {
                 const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
 #pragma unroll
-                for (int k = 0; k < kTileN / 16; ++k) {
-                    mma_ts(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8,
-                           smem_desc_sw128(vb + k * 2048, L::kChunkBytes, 1024), idesc_o,
-                           (acc || k > 0) ? 1u : 0u);
+                for (int k = 0; k < kTileN * kEb / 32; ++k) {
+                    const uint64_t vdesc = smem_desc_sw128(vb + k * (4096 / kEb), L::kChunkBytes, 1024);
+                    if constexpr (kFp8)
+                        mma_ts_f8(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8, vdesc,
+                                  idesc_o, (acc || k > 0) ? 1u : 0u);
+                    else
+                        mma_ts(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8, vdesc,
+                               idesc_o, (acc || k > 0) ? 1u : 0u);
                 }
             };
             // cnt[x]: products P_X V issued so far (one per tile of X); uo[x]:
@@ -386,7 +404,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int r = quad * 32 + lane;  // row of the tile == TMEM lane
         const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
         const uint32_t scol = L::kColS + x * 128, ocol = L::kColO + x * D;
-        const float sl2 = p.scale_log2;
+        float sl2 = p.scale_log2;
+        float o_factor = 1.f;  // descale_v (E4M3 inputs)
+        if constexpr (kFp8) {
+            sl2 *= *p.descale_q * *p.descale_k;
+            o_factor = *p.descale_v;
+        }
+        float amax = 0.f;  // max |O| over this thread's rows (E4M3 inputs)
         int cnt = 0, uo = 0;  // tiles and units of this tile's chain
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -397,7 +421,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             if (!U.live || row0 >= U.Lq) continue;  // no row of this tile
             const int q_idx = row0 + r;
             const bool row_ok = q_idx < U.Lq;
-            io_t *orow = reinterpret_cast<io_t *>(p.o) + U.o_row0 + (int64_t)q_idx * U.o_rs;
+            uint8_t *orow = static_cast<uint8_t *>(p.o) + (U.o_row0 + (int64_t)q_idx * U.o_rs) * kOb;
             float *lse_ptr = p.lse ? p.lse + U.lse_row0 + (int64_t)q_idx * U.lse_rs : nullptr;
             const int n_kv = U.n_kv[x];
             if (n_kv == 0) {
@@ -405,7 +429,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-                    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < D * kOb / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
                     if (lse_ptr) *lse_ptr = -INFINITY;
                 }
                 continue;
@@ -453,17 +477,36 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
                 const float base = (m_used == -INFINITY) ? 0.f : m_used;
                 const uint64_t sl2_2 = f2_pack(sl2, sl2), nbase_2 = f2_pack(-base, -base);
-                // P = exp2(s * scale*log2e - base), pairs packed in place into s[0..64)
+                // P = exp2(s * scale*log2e - base), packed in place into s[0..64)
+                // as bf16/fp16 pairs, or into s[0..32) as E4M3 quads
                 uint64_t sum2[4] = {0, 0, 0, 0};
+                if constexpr (kFp8) {
 #pragma unroll
-                for (int i = 0; i < kTileN / 2; ++i) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
-                                     sl2_2, nbase_2),
-                              x0, x1);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
-                    s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
+                    for (int i = 0; i < kTileN / 4; ++i) {
+                        float x0, x1, x2, x3;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1])),
+                                         sl2_2, nbase_2),
+                                  x0, x1);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])),
+                                         sl2_2, nbase_2),
+                                  x2, x3);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                        sum2[(2 * i) & 3] = f2_add(sum2[(2 * i) & 3], f2_pack(p0, p1));
+                        sum2[(2 * i + 1) & 3] = f2_add(sum2[(2 * i + 1) & 3], f2_pack(p2, p3));
+                        s[i] = pack_e4m3x4(p0, p1, p2, p3);  // i <= 4i: packs in place
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kTileN / 2; ++i) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                                         sl2_2, nbase_2),
+                                  x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+                        s[i] = pack2<kBf16>(p0, p1);  // i <= 2i: packs in place
+                    }
                 }
                 {
                     float a0, a1;
@@ -471,7 +514,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     l += a0 + a1;
                 }
                 tmem_st32(t_lane + scol, s);
-                tmem_st32(t_lane + scol + 32, s + 32);
+                if constexpr (!kFp8) tmem_st32(t_lane + scol + 32, s + 32);
 
                 if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                     // S_X(j) was issued after O_X += P_X(j-1) V retired, so O_X
@@ -495,7 +538,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             ok = warp_wait(bar(L::bOFull + x), uo & 1, wc, 14);
             if (!ok) break;
             tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            const float inv_l = (l > 0.f) ? o_factor / l : 0.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -505,20 +548,48 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     tc_fence_before();
                     mbar_arrive(bar(L::bOFree + x));
                 }
-                uint32_t pk[16];
+                if constexpr (kFp8) {
+                    if (row_ok) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
-                                         __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                        for (int i = 0; i < 32; ++i)
+                            amax = fmaxf(amax, fabsf(__uint_as_float(o[i]) * inv_l));
+                    }
+                }
+                if constexpr (kOut == kElE4m3) {
+                    const float so = inv_l * *p.scale_o;
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int i = 0; i < 8; ++i)
+                        pk[i] = pack_e4m3x4(__uint_as_float(o[4 * i]) * so, __uint_as_float(o[4 * i + 1]) * so,
+                                            __uint_as_float(o[4 * i + 2]) * so, __uint_as_float(o[4 * i + 3]) * so);
+                    if (row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32 * kOb);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                } else {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack2<kOut == kElBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                                       __uint_as_float(o[2 * i + 1]) * inv_l);
+                    if (row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32 * kOb);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
                 }
             }
             if (row_ok && lse_ptr) *lse_ptr = (l > 0.f) ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
             ++uo;
+        }
+        if constexpr (kFp8) {
+            // max |O| of the tile chain's rows into the caller's amax
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            if (p.amax_o && lane == 0 && amax > 0.f)
+                atomicMax(reinterpret_cast<int *>(p.amax_o), __float_as_int(amax));
         }
     }
 
@@ -530,12 +601,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
 }
 
-template <int D, bool kBf16, bool kPacked>
+template <int D, int kEl, bool kPacked, int kOut>
 cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const FwdParams &p, int grid, cudaStream_t stream,
                           const KernelTimer &timer) {
-    using L = PairLayout<D>;
-    auto kern = fwd_pair_kernel<D, kBf16, kPacked>;
+    using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2>;
+    auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);
     if (e != cudaSuccess) return e;
@@ -553,18 +624,34 @@ int fwd_pair_rows() { return kPairRows; }
 cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const FwdParams &p, int d, bool bf16, bool packed, int grid,
                             cudaStream_t stream, const KernelTimer &timer) {
-#define SDPA_PAIR_CASE(D_, BF_, PK_)                                           \
-    if (d == D_ && bf16 == BF_ && packed == PK_)                               \
-        return launch_pair_t<D_, BF_, PK_>(tq, tk, tv, p, grid, stream, timer);
-    SDPA_PAIR_CASE(64, true, false)
-    SDPA_PAIR_CASE(64, true, true)
-    SDPA_PAIR_CASE(64, false, false)
-    SDPA_PAIR_CASE(64, false, true)
-    SDPA_PAIR_CASE(128, true, false)
-    SDPA_PAIR_CASE(128, true, true)
-    SDPA_PAIR_CASE(128, false, false)
-    SDPA_PAIR_CASE(128, false, true)
+#define SDPA_PAIR_CASE(D_, EL_, PK_)                                           \
+    if (d == D_ && (bf16 ? kElBf16 : kElFp16) == EL_ && packed == PK_)         \
+        return launch_pair_t<D_, EL_, PK_, EL_>(tq, tk, tv, p, grid, stream, timer);
+    SDPA_PAIR_CASE(64, kElBf16, false)
+    SDPA_PAIR_CASE(64, kElBf16, true)
+    SDPA_PAIR_CASE(64, kElFp16, false)
+    SDPA_PAIR_CASE(64, kElFp16, true)
+    SDPA_PAIR_CASE(128, kElBf16, false)
+    SDPA_PAIR_CASE(128, kElBf16, true)
+    SDPA_PAIR_CASE(128, kElFp16, false)
+    SDPA_PAIR_CASE(128, kElFp16, true)
 #undef SDPA_PAIR_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_pair_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                const FwdParams &p, int out, bool packed, int grid,
+                                cudaStream_t stream, const KernelTimer &timer) {
+#define SDPA_PAIR_FP8_CASE(OUT_, PK_)                                          \
+    if (out == OUT_ && packed == PK_)                                          \
+        return launch_pair_t<128, kElE4m3, PK_, OUT_>(tq, tk, tv, p, grid, stream, timer);
+    SDPA_PAIR_FP8_CASE(kElBf16, false)
+    SDPA_PAIR_FP8_CASE(kElBf16, true)
+    SDPA_PAIR_FP8_CASE(kElFp16, false)
+    SDPA_PAIR_FP8_CASE(kElFp16, true)
+    SDPA_PAIR_FP8_CASE(kElE4m3, false)
+    SDPA_PAIR_FP8_CASE(kElE4m3, true)
+#undef SDPA_PAIR_FP8_CASE
     return cudaErrorInvalidValue;
 }
 

@@ -30,6 +30,13 @@ def sdpa():
     return m
 
 
+@pytest.fixture(params=[1, 2], ids=["one_tile", "two_tile"])
+def variant(request, sdpa):
+    sdpa.sdpa_set_forward_variant(request.param)
+    yield request.param
+    sdpa.sdpa_set_forward_variant(0)
+
+
 def _scalar(x):
     return torch.tensor([x], dtype=torch.float32, device="cuda")
 
@@ -49,7 +56,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"b{c[0]}h{c[1]}kv{c[2]}s{c[3]}x{c[4]}_{c[5]}_w{c[6]}")
-def test_fp8_dense_bf16_out(sdpa, case):
+def test_fp8_dense_bf16_out(sdpa, variant, case):
     b, h, h_kv, s_q, s_kv, mask, window = case
     d = 128
     qc, kc, vc, dq, dk, dv = sdpa_inputs.fp8_dense(b, h, s_q, s_kv, d, seed=9000 + s_q, h_kv=h_kv)
@@ -68,7 +75,7 @@ def test_fp8_dense_bf16_out(sdpa, case):
     assert abs(float(amax) - omax) <= 2.0 ** -8 * omax + 1e-12
 
 
-def test_fp8_e4m3_output_and_amax(sdpa):
+def test_fp8_e4m3_output_and_amax(sdpa, variant):
     b, h, s, d = 1, 4, 600, 128
     qc, kc, vc, dq, dk, dv = sdpa_inputs.fp8_dense(b, h, s, s, d, seed=91)
     args = (qc.cuda(), kc.cuda(), vc.cuda(), _scalar(dq), _scalar(dk), _scalar(dv))
@@ -87,7 +94,7 @@ def test_fp8_e4m3_output_and_amax(sdpa):
     check_lse(lse8, rlse)
 
 
-def test_fp8_fp16_output(sdpa):
+def test_fp8_fp16_output(sdpa, variant):
     b, h, s, d = 1, 2, 333, 128
     qc, kc, vc, dq, dk, dv = sdpa_inputs.fp8_dense(b, h, s, s, d, seed=92)
     scale = 1.0 / math.sqrt(d)
@@ -101,7 +108,7 @@ def test_fp8_fp16_output(sdpa):
     check_lse(lse, rlse)
 
 
-def test_fp8_packed(sdpa):
+def test_fp8_packed(sdpa, variant):
     lq = [130, 7, 300, 64, 0]
     lk = [130, 40, 300, 64, 9]
     h, h_kv, d = 4, 2, 128
@@ -121,7 +128,7 @@ def test_fp8_packed(sdpa):
     check_lse(lse, rlse)
 
 
-def test_fp8_rms_error_within_the_statistical_bound(sdpa):
+def test_fp8_rms_error_within_the_statistical_bound(sdpa, variant):
     # Round-to-nearest errors of P are independent with RMS <= 2^-4 / sqrt(3)
     # (uniform within half an E4M3 step), so E[dO_i^2] <= (2^-4/sqrt(3))^2 *
     # sum_j (p_j/l)^2 v_j^2 <= (2^-4/sqrt(3))^2 * max_j v_j^2-weighted mean:
