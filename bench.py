@@ -80,6 +80,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest x over all ranks: the job takes as long as its slowest rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(flops_per_step: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job TFLOP/s: the steps of every rank (each a full replica of the
+    workload) over the slowest rank's time, i.e. weak scaling."""
+    return world * flops_per_step * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -310,12 +327,8 @@ def run_ours(args):
     step_ms = [a.elapsed_time(bb) for a, bb, _, _ in ev]
     fwd_ms = [f[0].elapsed_time(f[1]) for _, _, f, _ in ev]
     bwd_ms = [0.0 if fp8 else g[0].elapsed_time(g[1]) for _, _, _, g in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    value = world * f_step * args.steps / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_rate(f_step, args.steps, world, total_ms)
     clocks = sampler.summary(t0, t1)
 
     # ------------------------------------------------------------ end to end
@@ -392,7 +405,7 @@ def run_ours(args):
         pipeline(n_e2e)
         ev_z.record(d2h)             # after the last step's last copy
         torch.cuda.synchronize(dev)
-        e_ms = ev_a.elapsed_time(ev_z) / n_e2e
+        e_ms = max_over_ranks(ev_a.elapsed_time(ev_z) / n_e2e, world, dev)
         h2d_bytes = sum(x.numel() * x.element_size() for x in host_in)
         d2h_bytes = sum(x.numel() * x.element_size() for x in host_out[0])
         e2e = {"value": world * f_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
