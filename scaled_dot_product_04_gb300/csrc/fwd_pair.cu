@@ -22,10 +22,12 @@
 //                the exponent unit at the same time);
 //   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B (thread r
 //                owns row r = TMEM lane r), as in fwd.cu.
-// TMEM columns: S_A 0, S_B 128, O_A 256, O_B 256 + d.  S_X(j+1) is issued only
-// after O_X += P_X(j) V_j has retired (P_X lives in the S_X columns), so when
-// the softmax sees S_X(j+1), O_X holds every earlier product and may be
-// rescaled without further waiting.
+// TMEM columns: S_A 0, S_B 128, O_A 256, O_B 256 + d.  S_X(j+1) is issued right
+// behind O_X += P_X(j) V_j although P_X lives in the S_X columns: tcgen05.mma
+// instructions of one thread execute in issue order, so the earlier product
+// has read P_X before the later one writes S_X (the same ordering every
+// chained accumulation relies on).  When the softmax sees S_X(j+1) complete,
+// O_X therefore holds every earlier product and may be rescaled at once.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -58,8 +60,7 @@ struct PairLayout {
     // per tile X in {A, B}: index + X
     static constexpr int bSFull = bVEmpty + kVStages;
     static constexpr int bPReady = bSFull + 2;
-    static constexpr int bPVDone = bPReady + 2;
-    static constexpr int bOFull = bPVDone + 2;
+    static constexpr int bOFull = bPReady + 2;
     static constexpr int bOFree = bOFull + 2;
     static constexpr int bMmaIdle = bOFree + 2;
     static constexpr int kNumBars = bMmaIdle + 1;
@@ -189,7 +190,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(L::bSFull + x), 1);
             mbar_init(bar(L::bPReady + x), kTileM);
-            mbar_init(bar(L::bPVDone + x), 1);
             mbar_init(bar(L::bOFull + x), 1);
             mbar_init(bar(L::bOFree + x), kTileM);
         }
@@ -287,31 +287,34 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                               : make_idesc_f16(kTileM, kTileN, kBf16, false, false);
             constexpr uint32_t idesc_o = kFp8 ? make_idesc_e4m3(kTileM, D, false, true)
                                               : make_idesc_f16(kTileM, D, kBf16, false, true);
+            // Operand descriptors, built once and advanced by constant offsets
+            // (a descriptor's low 14 bits are the address / 16).
+            constexpr uint32_t kChunk16 = L::kChunkBytes >> 4, kTile16 = L::kTileBytes >> 4;
+            const uint64_t dQ_k = smem_desc_sw128(sbase + L::kQ, 16, 1024);
+            const uint64_t dK_k = smem_desc_sw128(sbase + L::kK, 16, 1024);
+            const uint64_t dV_mn = smem_desc_sw128(sbase + L::kV, L::kChunkBytes, 1024);
             // S_X = Q_X K^T: both operands K-major (head dim contiguous), 32
             // bytes (16 bf16 or 32 E4M3 elements) per step.
             auto issue_s = [&](int x, int ks) {
-                const uint32_t qb = sbase + L::kQ + x * L::kTileBytes;
-                const uint32_t kb = sbase + L::kK + ks * L::kTileBytes;
+                const uint64_t a = dQ_k + x * kTile16, b = dK_k + ks * kTile16;
 #pragma unroll
                 for (int k = 0; k < D * kEb / 32; ++k) {
-                    const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
+                    const uint32_t off = (k / 4) * kChunk16 + (k % 4) * 2;
                     if constexpr (kFp8)
-                        mma_ss_f8(tmem + L::kColS + x * 128, smem_desc_sw128(qb + off, 16, 1024),
-                                  smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                        mma_ss_f8(tmem + L::kColS + x * 128, a + off, b + off, idesc_s, k > 0);
                     else
-                        mma_ss(tmem + L::kColS + x * 128, smem_desc_sw128(qb + off, 16, 1024),
-                               smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                        mma_ss(tmem + L::kColS + x * 128, a + off, b + off, idesc_s, k > 0);
                 }
             };
             // O_X += P_X V: P from TMEM (8 columns per step: 16 keys as bf16
             // pairs or 32 keys as E4M3 quads), V MN-major (head dim
             // contiguous); 128-byte head-dim chunks are 16 KiB apart (leading
-            // offset), 8-key groups 1 KiB apart.
+            // offset), 8-key groups 1 KiB apart, so a step advances 2 or 4 KiB.
             auto issue_pv = [&](int x, int vs, bool acc) {
-                const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
+                const uint64_t b = dV_mn + vs * kTile16;
 #pragma unroll
                 for (int k = 0; k < kTileN * kEb / 32; ++k) {
-                    const uint64_t vdesc = smem_desc_sw128(vb + k * (4096 / kEb), L::kChunkBytes, 1024);
+                    const uint64_t vdesc = b + k * ((4096 / kEb) >> 4);
                     if constexpr (kFp8)
                         mma_ts_f8(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8, vdesc,
                                   idesc_o, (acc || k > 0) ? 1u : 0u);
@@ -321,8 +324,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
             };
             // cnt[x]: products P_X V issued so far (one per tile of X); uo[x]:
-            // units in which tile X took part.  Every phase of bPVDone + x is
-            // waited here, in order, before S_X reuses its columns.
+            // units in which tile X took part.
             int t = 0, units = 0, cnt[2] = {0, 0}, uo[2] = {0, 0};
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -336,8 +338,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     if (!ok || U.n_kv[x] == 0) continue;
-                    if (cnt[x] > 0) ok = mbar_wait(bar(L::bPVDone + x), (cnt[x] - 1) & 1, wc, 6);
-                    if (!ok) continue;
                     tc_fence_after();
                     issue_s(x, t % L::kKStages);
                     mma_commit(bar(L::bSFull + x));
@@ -361,7 +361,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         if (!ok) continue;
                         tc_fence_after();
                         issue_pv(x, t % L::kVStages, j > 0);
-                        mma_commit(bar(L::bPVDone + x));
                         ++cnt[x];
                         if (j + 1 >= U.n_kv[x]) continue;
                         if (!k_next) {
@@ -369,8 +368,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                            wc, 10);
                             k_next = true;
                         }
-                        // S_X(j+1) overwrites the P_X(j) that O_X += P_X V reads
-                        if (ok) ok = mbar_wait(bar(L::bPVDone + x), (cnt[x] - 1) & 1, wc, 11);
+                        // S_X(j+1) overwrites the P_X(j) that O_X += P_X V
+                        // reads; issue order keeps them apart (see the header)
                         if (!ok) continue;
                         tc_fence_after();
                         issue_s(x, t1 % L::kKStages);
@@ -517,8 +516,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if constexpr (!kFp8) tmem_st32(t_lane + scol + 32, s + 32);
 
                 if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-                    // S_X(j) was issued after O_X += P_X(j-1) V retired, so O_X
-                    // holds every earlier product and nothing writes it now.
+                    // The commit behind S_X(j) completed only once every earlier
+                    // product had, O_X += P_X(j-1) V included, so O_X holds all
+                    // of them and nothing writes it now.
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
