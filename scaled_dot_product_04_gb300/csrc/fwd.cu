@@ -315,21 +315,24 @@ __global__ void __launch_bounds__(192, 1)
                                               : make_idesc_f16(kTileM, kTileN, kBf16, false, false);
             constexpr uint32_t idesc_o = kFp8 ? make_idesc_e4m3(kTileM, D, false, true)
                                               : make_idesc_f16(kTileM, D, kBf16, false, true);
+            // Operand descriptors, built once and advanced by constant offsets
+            // (a descriptor's low 14 bits are the address / 16).
+            constexpr uint32_t kChunk16 = L::kChunkBytes >> 4, kTile16 = L::kTileBytes >> 4;
+            const uint64_t dQ_k = smem_desc_sw128(sbase + L::kQ, 16, 1024);
+            const uint64_t dK_k = smem_desc_sw128(sbase + L::kK, 16, 1024);
+            const uint64_t dV_mn = smem_desc_sw128(sbase + L::kV, L::kChunkBytes, 1024);
             // S = Q K^T: both operands K-major (head dim contiguous), 32 bytes
             // (16 bf16 or 32 E4M3 elements) per step.
             int units = 0;  // live units processed by this CTA (selects the Q buffer)
             auto issue_s = [&](int ks, uint32_t col) {
-                const uint32_t qs = sbase + L::kQ + (units & 1) * L::kTileBytes;
-                const uint32_t kb = sbase + L::kK + ks * L::kTileBytes;
+                const uint64_t a = dQ_k + (units & 1) * kTile16, b = dK_k + ks * kTile16;
 #pragma unroll
                 for (int k = 0; k < D * kEb / 32; ++k) {
-                    const uint32_t off = (k / 4) * L::kChunkBytes + (k % 4) * 32;
+                    const uint32_t off = (k / 4) * kChunk16 + (k % 4) * 2;
                     if constexpr (kFp8)
-                        mma_ss_f8(tmem + col, smem_desc_sw128(qs + off, 16, 1024),
-                                  smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                        mma_ss_f8(tmem + col, a + off, b + off, idesc_s, k > 0);
                     else
-                        mma_ss(tmem + col, smem_desc_sw128(qs + off, 16, 1024),
-                               smem_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
+                        mma_ss(tmem + col, a + off, b + off, idesc_s, k > 0);
                 }
             };
             // O += P V: P from TMEM (8 columns per step: 16 keys as bf16 pairs
@@ -337,10 +340,10 @@ __global__ void __launch_bounds__(192, 1)
             // 128-byte head-dim chunks are 16 KiB apart (leading offset),
             // 8-key groups 1 KiB apart, so a step advances 2 or 4 KiB.
             auto issue_pv = [&](int vs, uint32_t pcol, uint32_t ocol, bool acc) {
-                const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
+                const uint64_t vb = dV_mn + vs * kTile16;
 #pragma unroll
                 for (int k = 0; k < kTileN * kEb / 32; ++k) {
-                    const uint64_t vdesc = smem_desc_sw128(vb + k * (4096 / kEb), L::kChunkBytes, 1024);
+                    const uint64_t vdesc = vb + k * ((4096 / kEb) >> 4);
                     if constexpr (kFp8)
                         mma_ts_f8(tmem + ocol, tmem + pcol + k * 8, vdesc, idesc_o, (acc || k > 0) ? 1u : 0u);
                     else
