@@ -47,7 +47,7 @@ namespace {
 SDPA_DEV float tf32_hi(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
 
 SDPA_DEV bool warp_wait_b(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
-    bool ok = mbar_wait(bar, parity, w, site);
+    bool ok = mbar_wait_lean(bar, parity, w, site);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -415,12 +415,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss(tmem + col, a + kstep(k), b + kstep(k), id_sq, k > 0);
                 mma_ss_tf32(tmem + col, a_ex, dRX + st * kRowX16, id_rx, 1u);
             };
-            bool ok = mbar_wait(bar(L::bKVFull), 0, wc, 2) && mbar_wait(bar(L::bQFull), 0, wc, 3);
+            bool ok = mbar_wait_lean(bar(L::bKVFull), 0, wc, 2) && mbar_wait_lean(bar(L::bQFull), 0, wc, 3);
             if (ok) {
                 tc_fence_after();
                 issue_kmajor(dK_k, dQ_k, dAS, 0, L::kColS);  // S'^T_0
                 mma_commit(bar(L::bSFull));
-                ok = mbar_wait(bar(L::bDOFull), 0, wc, 4);
+                ok = mbar_wait_lean(bar(L::bDOFull), 0, wc, 4);
             }
             if (ok) {
                 tc_fence_after();
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int dst = L::kDOStages == 1 ? 0 : (i & 1);
                 // dV += P^T dO.  P^T is packed two per column into the first 32
                 // columns of each compute group's 64 S^T columns.
-                ok = mbar_wait(bar(L::bPReady), i & 1, wc, 5);
+                ok = mbar_wait_lean(bar(L::bPReady), i & 1, wc, 5);
                 if (!ok) break;
                 tc_fence_after();
                 {
@@ -447,8 +447,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // S'^T_{i+1}, once the dV product has finished reading P^T_i
                 if (i + 1 < n_it) {
                     const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
-                    ok = mbar_wait(bar(L::bQFull + st1), use1 & 1, wc, 6) &&
-                         mbar_wait(bar(L::bDVDone), i & 1, wc, 7);
+                    ok = mbar_wait_lean(bar(L::bQFull + st1), use1 & 1, wc, 6) &&
+                         mbar_wait_lean(bar(L::bDVDone), i & 1, wc, 7);
                     if (!ok) break;
                     tc_fence_after();
                     issue_kmajor(dK_k, dQ_k + st1 * kTile16, dAS, st1, L::kColS);
@@ -457,9 +457,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dQ_i = dS' K (unless the deterministic dQ pass computes dQ),
                 // then dK += dS'^T Q (last reader of Q_i)
                 const bool do_dq = !p.deterministic;
-                ok = mbar_wait(bar(L::bDSReady), i & 1, wc, 8);
+                ok = mbar_wait_lean(bar(L::bDSReady), i & 1, wc, 8);
                 if (ok && do_dq && !L::kDQAliasDP && i > 0)
-                    ok = mbar_wait(bar(L::bDQFree), (i - 1) & 1, wc, 9);
+                    ok = mbar_wait_lean(bar(L::bDQFree), (i - 1) & 1, wc, 9);
                 if (!ok) break;
                 tc_fence_after();
                 if (do_dq) {
@@ -481,8 +481,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (i + 1 < n_it) {
                     const int dst1 = L::kDOStages == 1 ? 0 : ((i + 1) & 1);
                     const int duse1 = (i + 1) / L::kDOStages;
-                    ok = mbar_wait(bar(L::bDOFull + dst1), duse1 & 1, wc, 10);
-                    if (ok && do_dq && L::kDQAliasDP) ok = mbar_wait(bar(L::bDQFree), i & 1, wc, 11);
+                    ok = mbar_wait_lean(bar(L::bDOFull + dst1), duse1 & 1, wc, 10);
+                    if (ok && do_dq && L::kDQAliasDP) ok = mbar_wait_lean(bar(L::bDQFree), i & 1, wc, 11);
                     if (!ok) break;
                     tc_fence_after();
                     issue_kmajor(dV_k, dDO_k + dst1 * kTile16, dAD, (i + 1) & 1, L::kColDP);

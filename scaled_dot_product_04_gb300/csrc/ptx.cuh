@@ -62,11 +62,8 @@ struct WaitCtx {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // two seconds
 
-// Wait until phase `parity` of `bar` has completed.  Returns false (after
-// recording the failure) when the limit expires or another role of the CTA
-// has already given up.
-SDPA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The polling part of the bounded wait.
+SDPA_DEV bool mbar_poll(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
     uint64_t t0 = global_timer_ns();
     // The abort flag and the clock are looked at every 16th poll only: each
     // look is a shared-memory read that competes with the operand traffic.
@@ -80,6 +77,27 @@ SDPA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_
             return false;
         }
     }
+}
+
+// Wait until phase `parity` of `bar` has completed.  Returns false (after
+// recording the failure) when the limit expires or another role of the CTA
+// has already given up.
+SDPA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_poll(bar, parity, w, site);
+}
+
+// The same wait with the polling loop out of line, so that only one
+// try_wait is inlined per wait site.  That shortens the code of a kernel
+// with many wait sites whose waits are mostly satisfied on the first try
+// (the backward: its issuing thread runs faster); where waits routinely
+// poll (the forward's softmax), the call costs more than it saves.
+static __device__ __noinline__ bool mbar_poll_ol(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
+    return mbar_poll(bar, parity, w, site);
+}
+SDPA_DEV bool mbar_wait_lean(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_poll_ol(bar, parity, w, site);
 }
 
 // Teardown wait: ignores the abort flag, gives up silently after the limit.
