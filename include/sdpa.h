@@ -323,6 +323,17 @@ const char *sdpa_last_error(void);
 int sdpa_check_device_error(sdpa_stream_t stream);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages).  Enqueues on
+ * `stream` one small kernel whose bounded wait -- the same code every kernel
+ * waits with, here with a limit of `limit_us` microseconds (1 .. 2,000,000)
+ * instead of two seconds -- polls a barrier phase that nothing completes.
+ * The wait expires, records its kernel ("selftest") and site in the error
+ * word, and the kernel exits: the next sdpa_check_device_error returns
+ * SDPA_ERR_TIMEOUT and clears the word.  Nothing faults or hangs.
+ */
+int sdpa_selftest_wait_timeout(int limit_us, sdpa_stream_t stream);
+
+/*
  * Measurement hook (no counterpart on the pages).  While both events are
  * non-NULL, every later call on this host thread records `start_event` on
  * its stream immediately before launching its main kernel (the forward

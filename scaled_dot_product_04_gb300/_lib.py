@@ -37,7 +37,8 @@ EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_fwd_ex", "sdpa_varlen_fwd_ex", "
            "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_varlen_bwd_workspace_size",
            "sdpa_varlen_bwd", "sdpa_bwd_ex_workspace_size", "sdpa_varlen_bwd_ex_workspace_size",
            "sdpa_bwd_ex", "sdpa_varlen_bwd_ex", "sdpa_bwd_noalloc", "sdpa_last_error",
-           "sdpa_check_device_error", "sdpa_set_forward_variant", "sdpa_set_kernel_timer",
+           "sdpa_check_device_error", "sdpa_selftest_wait_timeout", "sdpa_set_forward_variant",
+           "sdpa_set_kernel_timer",
            "sdpa_version")
 
 
@@ -101,6 +102,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                          _F, _I, _I, _P]
         lib.sdpa_last_error.restype = ctypes.c_char_p
         lib.sdpa_check_device_error.argtypes = [_P]
+        lib.sdpa_selftest_wait_timeout.argtypes = [_I, _P]
+        lib.sdpa_selftest_wait_timeout.restype = _I
         lib.sdpa_version.restype = ctypes.c_char_p
         lib.sdpa_set_forward_variant.argtypes = [_I]
         lib.sdpa_set_forward_variant.restype = _I
@@ -265,6 +268,11 @@ def sdpa_last_error() -> str:
 
 def sdpa_check_device_error(stream=None) -> None:
     _check(load().sdpa_check_device_error(_stream(stream)))
+
+
+def sdpa_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (see include/sdpa.h)."""
+    _check(load().sdpa_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def sdpa_set_kernel_timer(start_event=None, stop_event=None) -> None:

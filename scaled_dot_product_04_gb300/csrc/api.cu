@@ -294,10 +294,22 @@ int sdpa_check_device_error(sdpa_stream_t stream) {
     if (word == 0) return ok();
     const uint32_t zero = 0;
     cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
-    static const char *names[] = {"?", "fwd", "bwd_preprocess", "bwd_main", "bwd_dq_convert", "bwd_dq"};
+    static const char *names[] = {"?", "fwd", "bwd_preprocess", "bwd_main", "bwd_dq_convert", "bwd_dq",
+                                  "selftest"};
     const uint32_t tag = word >> 16;
     return fail(SDPA_ERR_TIMEOUT, "kernel %s gave up on a bounded wait (site %u)",
-                tag < 6 ? names[tag] : "?", word & 0xffffu);
+                tag < 7 ? names[tag] : "?", word & 0xffffu);
+}
+
+int sdpa_selftest_wait_timeout(int limit_us, sdpa_stream_t stream) {
+    if (limit_us < 1 || limit_us > 2000000)
+        return fail(SDPA_ERR_INVALID_ARG, "limit_us must be in [1, 2000000] (got %d)", limit_us);
+    DeviceState *dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    return launch_status(launch_wait_selftest(dev->err, (uint64_t)limit_us * 1000ull,
+                                              static_cast<cudaStream_t>(stream)),
+                         "sdpa_selftest_wait_timeout");
 }
 
 int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int b, int h,

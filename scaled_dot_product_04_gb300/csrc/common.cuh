@@ -17,6 +17,7 @@ enum KernelTag : uint32_t {
     kTagBwdMain = 3,
     kTagBwdConvert = 4,
     kTagBwdDq = 5,
+    kTagSelftest = 6,
 };
 
 // Where a tile lives: dense tensors are [b*h, s, d] (row stride d), packed
@@ -97,6 +98,11 @@ struct BwdParams {
     int q_tiles;                 // query tiles per slice: dense ceil(s_q/128), packed
                                  // ceil(max_seqlen_q/128) (the dQ pass's grid)
 };
+
+// Failure-detection self-test (selftest.cu): one CTA waits, with the bounded
+// wait of every kernel and the given limit, on a barrier phase that nothing
+// completes, and so records a timeout in the error word.
+cudaError_t launch_wait_selftest(uint32_t *err, uint64_t limit_ns, cudaStream_t stream);
 
 // Host launchers (one translation unit each).
 // Optional measurement events recorded on `stream` right before and right

@@ -54,13 +54,14 @@ SDPA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded-wait bookkeeping shared by all roles of one CTA.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // two seconds
+
 struct WaitCtx {
     volatile uint32_t *abort_flag;  // shared memory: set once any wait expires
     uint32_t *err_word;             // global: first error code recorded here
     uint32_t kernel_tag;            // identifies kernel for the error message
+    uint64_t limit_ns = kWaitLimitNs;  // how long one wait may take
 };
-
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // two seconds
 
 // The polling part of the bounded wait.
 SDPA_DEV bool mbar_poll(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
@@ -71,7 +72,7 @@ SDPA_DEV bool mbar_poll(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 15u) != 0u) continue;
         if (*w.abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > w.limit_ns) {
             *w.abort_flag = 1u;
             atomicCAS(w.err_word, 0u, (w.kernel_tag << 16) | (site & 0xffffu));
             return false;
