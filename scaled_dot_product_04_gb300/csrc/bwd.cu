@@ -200,6 +200,8 @@ struct BwdLayout {
 // warps: 0 TMA, 1 MMA, 2-5 compute (queries 0-63 of a tile), 6-9 compute
 // (queries 64-127), 10-13 dQ epilogue
 constexpr int kBwdThreads = 448;
+// slices whose key tiles are interleaved in the CTA order
+constexpr int kSliceGroup = 4;
 
 template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -215,13 +217,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // A CTA owns one key tile of one key/value slice ((batch, kv head) or
     // (sequence, kv head)) and walks every query tile that can see it, for
     // each of the group's h / h_kv query heads in turn, so dK and dV sum over
-    // the group in TMEM.  Head-major order: all key tiles of one slice run
-    // back to back, ascending (under a causal mask the first key tiles see
-    // the most query tiles, so each slice's heaviest units start first).  The
-    // CTAs resident at any time then share a slice or two, whose fp32 dQ
-    // accumulator, Q and dO stay in L2 instead of every head's at once.
-    const int slice = blockIdx.x / p.kv_tiles;  // key/value slice
-    const int kt = blockIdx.x % p.kv_tiles;
+    // the group in TMEM.  Order: slices in groups of kSliceGroup, key tile
+    // major within a group (under a causal mask the first key tiles see the
+    // most query tiles, so the heaviest units of a group start first).  The
+    // CTAs resident at any time then share a few slices, whose fp32 dQ
+    // accumulator, Q and dO stay in L2 instead of every head's at once; and
+    // the heaviest unit of the last group starts early enough not to run
+    // alone at the end, as the last slice's first key tile would in plain
+    // slice-major order.
+    const int per_group = kSliceGroup * p.kv_tiles;
+    const int group_i = blockIdx.x / per_group;
+    const int in_group = blockIdx.x - group_i * per_group;
+    const int group_n = min(kSliceGroup, p.kv_slices - group_i * kSliceGroup);
+    const int slice = group_i * kSliceGroup + in_group % group_n;  // key/value slice
+    const int kt = in_group / group_n;
     const int hk = slice % p.h_kv;              // key/value head
     int Lq, Lkv, tok_q0 = 0, tok_kv0 = 0;
     int q_slice0;                               // dense: query slice of the group's first head
