@@ -27,6 +27,11 @@ thread_local std::string t_last_error;
 thread_local KernelTimer t_timer;
 thread_local int t_fwd_variant = 0;  // 0 auto, 1 one-tile, 2 two-tile
 
+// K + V bytes above which the one-tile forward orders its units slice group by
+// slice group: with the latest-tile-first order over all slices, the units in
+// flight would each stream another slice's K and V from HBM.
+constexpr size_t kSliceMajorKVBytes = size_t(64) << 20;
+
 // Forward kernel choice.  The two-tile kernel (256 query rows per unit, two
 // softmax warpgroups) wins when every unit visits many key tiles; short or
 // packed problems do better with the one-tile kernel's 128-row units.
@@ -270,7 +275,7 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.5 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.6 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)
@@ -351,13 +356,14 @@ int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     p.s_kv = s_kv;
     p.q_tiles = (int)q_tiles;
     p.n_units = (int)(q_tiles * bh);
+    const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
     const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer)
-                              : launch_fwd(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer),
+                              : launch_fwd(tq, tk, tv, p, d, bf16, false, grid, slice_major, cs, t_timer),
                          "sdpa_fwd");
 }
 
@@ -434,13 +440,14 @@ int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o, flo
     p.num_seqs = num_seqs;
     p.q_tiles = (int)q_tiles;
     p.n_units = (int)(q_tiles * slices);
+    const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
     const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer)
-                              : launch_fwd(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer),
+                              : launch_fwd(tq, tk, tv, p, d, bf16, true, grid, slice_major, cs, t_timer),
                          "sdpa_varlen_fwd");
 }
 
@@ -514,6 +521,7 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     p.s_kv = s_kv;
     p.q_tiles = (int)q_tiles;
     p.n_units = (int)(q_tiles * bh);
+    const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
@@ -527,7 +535,7 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
     return launch_status(pair ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer)
-                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer),
+                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, slice_major, cs, t_timer),
                          "sdpa_fwd_fp8");
 }
 
@@ -581,6 +589,7 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
     p.num_seqs = num_seqs;
     p.q_tiles = (int)q_tiles;
     p.n_units = (int)(q_tiles * slices);
+    const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
@@ -594,7 +603,7 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
     if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
     return launch_status(pair ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer)
-                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer),
+                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, true, grid, slice_major, cs, t_timer),
                          "sdpa_varlen_fwd_fp8");
 }
 

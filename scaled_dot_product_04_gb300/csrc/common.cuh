@@ -117,16 +117,18 @@ int fwd_pair_rows();
 cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const FwdParams &p, int d, bool bf16, bool packed, int grid,
                             cudaStream_t stream, const KernelTimer &timer);
+// slice_major: order the units slice group by slice group (K and V too large
+// for L2), else latest query tile first over all slices.
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
-                       cudaStream_t stream, const KernelTimer &timer);
+                       bool slice_major, cudaStream_t stream, const KernelTimer &timer);
 // E4M3 inputs, d = 128, output kind `out` (ElemKind): one-tile and two-tile kernels.
 cudaError_t launch_fwd_pair_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const FwdParams &p, int out, bool packed, int grid,
                                 cudaStream_t stream, const KernelTimer &timer);
 cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const FwdParams &p, int out, bool packed, int grid, cudaStream_t stream,
-                           const KernelTimer &timer);
+                           const FwdParams &p, int out, bool packed, int grid, bool slice_major,
+                           cudaStream_t stream, const KernelTimer &timer);
 // Deterministic dQ pass (bwd_dq.cu): one CTA per (query slice, query tile);
 // q_tiles = query tiles per slice.  Writes p.dq from the row terms in p.rowx.
 cudaError_t launch_bwd_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

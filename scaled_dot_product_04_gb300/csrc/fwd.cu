@@ -17,7 +17,11 @@
 // LPT scheduler notes): the grid is capped at one CTA per SM; CTA c walks
 // the units c, c + grid, c + 2*grid, ... of a list ordered latest query tile
 // first, which under the causal mask is heaviest first.  A unit is one
-// 128-row query tile of one (batch, head) or (sequence, head).  Packed
+// 128-row query tile of one (batch, head) or (sequence, head).  When K and V
+// outgrow L2 the list runs slice group by slice group instead (dense: the
+// heads of one batch; packed: one sequence, longest first), latest tile
+// first within a group, so the units in flight share a few slices' K and V
+// in L2 rather than streaming a different slice each from HBM.  Packed
 // sequences are found from cu_seqlens on the device (cached in shared
 // memory); a unit past its sequence's end costs a few instructions.
 //
@@ -58,14 +62,18 @@ struct FwdLayout {
     // Q is double-buffered by unit parity so the next unit's Q arrives while
     // the current unit still runs.
     static constexpr int kQStages = 2;
-    // cu_seqlens entries cached in shared memory (longer lists are read from
-    // global memory); at d = 128 only the room left by the rings is used.
-    static constexpr int kCuCap = (kTileBytes >= 32768) ? 192 : 2048;
+    // cu_seqlens entries cached in shared memory, with the packed unit list's
+    // sequence order and unit offsets (longer lists are read from global
+    // memory in the envelope order); at d = 128 only the room left by the
+    // rings is used.
+    static constexpr int kCuCap = (kTileBytes >= 32768) ? 96 : 1024;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kQStages * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
-    static constexpr int kCu = kV + kVStages * kTileBytes;  // int32 cu_q[kCuCap], cu_kv[kCuCap]
-    static constexpr int kBar = kCu + 2 * kCuCap * 4;
+    // int32 cu_q[kCuCap], cu_kv[kCuCap], order[kCuCap], first_unit[kCuCap]
+    static constexpr int kCu = kV + kVStages * kTileBytes;
+    static constexpr int kScan = kCu + 4 * kCuCap * 4;  // 8 int32: per-warp sums
+    static constexpr int kBar = kScan + 32;
     static constexpr int bQFull = 0;   // two
     static constexpr int bQEmpty = 2;  // two
     static constexpr int bKFull = 4;
@@ -116,11 +124,45 @@ struct Unit {
     int64_t o_row0, o_rs, lse_row0, lse_rs;
 };
 
+// Packed units in sequence-major order: `order` lists the sequences by
+// query-tile count, most first, and sequence order[i] owns units
+// [first_unit[i], first_unit[i + 1]), its query tiles latest first with the
+// heads innermost.  The CTAs running at any time then share one or two
+// sequences, whose K and V stay in L2 while every head's units stream them.
+SDPA_DEV void packed_slot(const FwdParams &p, int u, const int *cu_q, const int *order,
+                          const int *first_unit, int &qt, int &slice) {
+    int lo = 0, hi = p.num_seqs;  // first_unit[lo] <= u < first_unit[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (first_unit[mid] <= u) lo = mid;
+        else hi = mid;
+    }
+    const int n = order[lo], local = u - first_unit[lo];
+    const int tiles = (cu_q[n + 1] - cu_q[n] + kTileM - 1) / kTileM;
+    qt = tiles - 1 - local / p.h;
+    slice = n * p.h + local % p.h;
+}
+
+// Unit u.  With slice_major, dense units run batch by batch (the h
+// slices of one batch, latest query tile first, heads innermost) and packed
+// ones sequence by sequence (order != nullptr, see packed_slot); otherwise,
+// and for packed lists too long for the shared table, latest query tile
+// first over all slices (heaviest first, which balances small problems best).
 template <int D, bool kPacked>
-SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int *cu_kv) {
+SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int *cu_kv,
+                          bool slice_major, const int *order, const int *first_unit) {
     Unit U;
-    const int qt = p.q_tiles - 1 - u / p.bh;  // latest (heaviest) query tiles first
-    U.slice = u % p.bh;
+    int qt;
+    if (kPacked && order) {
+        packed_slot(p, u, cu_q, order, first_unit, qt, U.slice);
+    } else {
+        // slice groups of gs slices (all of them unless slice-major dense)
+        const int gs = (!kPacked && slice_major) ? p.h : p.bh;
+        const int per_group = gs * p.q_tiles;
+        const int g = u / per_group, local = u - g * per_group;
+        qt = p.q_tiles - 1 - local / gs;
+        U.slice = g * gs + local % gs;
+    }
     if constexpr (!kPacked) {
         U.head = 0;
         U.kv_head = 0;
@@ -169,7 +211,7 @@ SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int 
 template <int D, int kEl, bool kPacked, int kOut>
 __global__ void __launch_bounds__(192, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int slice_major) {
     constexpr bool kFp8 = kEl == kElE4m3;
     constexpr bool kBf16 = kEl == kElBf16;
     constexpr int kEb = kFp8 ? 1 : 2;
@@ -184,18 +226,70 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
 
-    // cu_seqlens of packed inputs, cached when they fit
+    // cu_seqlens of packed inputs, cached when they fit, and then the
+    // sequence-major unit list (see packed_slot)
     int *cu_q_s = reinterpret_cast<int *>(smem + L::kCu);
     int *cu_kv_s = cu_q_s + L::kCuCap;
+    int *order_s = cu_kv_s + L::kCuCap;
+    int *first_s = order_s + L::kCuCap;
     const int *cu_q = p.cu_q, *cu_kv = p.cu_kv;
+    const int *order = nullptr;
+    int n_units = p.n_units;
     if constexpr (kPacked) {
         if (p.num_seqs + 1 <= L::kCuCap) {
-            for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) {
+            const int ns = p.num_seqs;
+            for (int i = threadIdx.x; i <= ns; i += blockDim.x) {
                 cu_q_s[i] = p.cu_q[i];
                 cu_kv_s[i] = p.cu_kv[i];
             }
             cu_q = cu_q_s;
             cu_kv = cu_kv_s;
+        }
+        if (p.num_seqs + 1 <= L::kCuCap && slice_major) {
+            const int ns = p.num_seqs;
+            __syncthreads();
+            auto tiles = [&](int n) { return (cu_q_s[n + 1] - cu_q_s[n] + kTileM - 1) / kTileM; };
+            // most query tiles first, ties in sequence order (a rank count;
+            // long lists keep their own order)
+            for (int n = threadIdx.x; n < ns; n += blockDim.x) {
+                int rank = n;
+                if (ns <= 256) {
+                    const int tn = tiles(n);
+                    rank = 0;
+                    for (int m = 0; m < ns; ++m) {
+                        const int tm = tiles(m);
+                        rank += (tm > tn || (tm == tn && m < n)) ? 1 : 0;
+                    }
+                }
+                order_s[rank] = n;
+            }
+            __syncthreads();
+            // first_unit = exclusive prefix sum of tiles(order[i]) * h: each
+            // thread sums a chunk, the chunk sums are scanned in the warp and
+            // across the warps
+            int *scan = reinterpret_cast<int *>(smem + L::kScan);
+            const int per = (ns + blockDim.x - 1) / blockDim.x;
+            const int b0 = min(ns, (int)threadIdx.x * per), b1 = min(ns, b0 + per);
+            int csum = 0;
+            for (int i = b0; i < b1; ++i) csum += tiles(order_s[i]) * p.h;
+            int incl = csum;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if ((int)lane >= off) incl += y;
+            }
+            if (lane == 31) scan[warp] = incl;
+            __syncthreads();
+            int run = incl - csum;
+            for (int w = 0; w < (int)warp; ++w) run += scan[w];
+            for (int i = b0; i < b1; ++i) {
+                first_s[i] = run;
+                run += tiles(order_s[i]) * p.h;
+            }
+            if (threadIdx.x == blockDim.x - 1) first_s[ns] = run;  // the last chunk ends the list
+            __syncthreads();
+            order = order_s;
+            n_units = first_s[ns];
         }
     }
 
@@ -235,7 +329,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const WaitCtx wc{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.err, kTagFwd};
-    const int first = blockIdx.x, step = gridDim.x, n_units = p.n_units;
+    const int first = blockIdx.x, step = gridDim.x;
 
     if (warp == 0) {
         // ============================================================ producer
@@ -262,7 +356,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int k = 0; ok; ++k) {
                 const int u = unit_of(k, first, step);
                 if (u >= n_units) break;
-                const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv);
+                const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
                 if (U.n_kv == 0) continue;
                 // the previous unit's last V goes out before waiting for Q's slot
                 if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
@@ -369,7 +463,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int k = 0; ok; ++k) {
                 const int u = unit_of(k, first, step);
                 if (u >= n_units) break;
-                const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv);
+                const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
                 if (U.n_kv == 0) continue;
                 ok = mbar_wait(bar(L::bQFull + (units & 1)), (units >> 1) & 1, wc, 4) && issue_s_tile(t);
                 if (!ok) break;
@@ -481,7 +575,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int k = 0; ok; ++k) {
             const int u = unit_of(k, first, step);
             if (u >= n_units) break;
-            const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv);
+            const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
             if (!U.live) continue;
             const int q_idx = U.row0 + r;
             const bool row_ok = q_idx < U.Lq;
@@ -628,7 +722,7 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int D, int kEl, bool kPacked, int kOut>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const FwdParams &p, int grid, cudaStream_t stream,
+                         const FwdParams &p, int grid, bool slice_major, cudaStream_t stream,
                          const KernelTimer &timer) {
     using L = FwdLayout<D, kEl == kElE4m3 ? 1 : 2>;
     auto kern = fwd_kernel<D, kEl, kPacked, kOut>;
@@ -636,7 +730,7 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
                                          L::kSmemAlloc);
     if (e != cudaSuccess) return e;
     if (timer.start) cudaEventRecord(timer.start, stream);
-    kern<<<grid, 192, L::kSmemAlloc, stream>>>(tq, tk, tv, p);
+    kern<<<grid, 192, L::kSmemAlloc, stream>>>(tq, tk, tv, p, slice_major ? 1 : 0);
     e = cudaGetLastError();
     if (timer.stop) cudaEventRecord(timer.stop, stream);
     return e;
@@ -646,10 +740,10 @@ cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdParams &p, int d, bool bf16, bool packed, int grid,
-                       cudaStream_t stream, const KernelTimer &timer) {
+                       bool slice_major, cudaStream_t stream, const KernelTimer &timer) {
 #define SDPA_FWD_CASE(D_, EL_, PK_)                                            \
     if (d == D_ && (bf16 ? kElBf16 : kElFp16) == EL_ && packed == PK_)         \
-        return launch_fwd_t<D_, EL_, PK_, EL_>(tq, tk, tv, p, grid, stream, timer);
+        return launch_fwd_t<D_, EL_, PK_, EL_>(tq, tk, tv, p, grid, slice_major, stream, timer);
     SDPA_FWD_CASE(64, kElBf16, false)
     SDPA_FWD_CASE(64, kElBf16, true)
     SDPA_FWD_CASE(64, kElFp16, false)
@@ -663,11 +757,11 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const FwdParams &p, int out, bool packed, int grid, cudaStream_t stream,
-                           const KernelTimer &timer) {
+                           const FwdParams &p, int out, bool packed, int grid, bool slice_major,
+                           cudaStream_t stream, const KernelTimer &timer) {
 #define SDPA_FP8_CASE(OUT_, PK_)                                               \
     if (out == OUT_ && packed == PK_)                                          \
-        return launch_fwd_t<128, kElE4m3, PK_, OUT_>(tq, tk, tv, p, grid, stream, timer);
+        return launch_fwd_t<128, kElE4m3, PK_, OUT_>(tq, tk, tv, p, grid, slice_major, stream, timer);
     SDPA_FP8_CASE(kElBf16, false)
     SDPA_FP8_CASE(kElBf16, true)
     SDPA_FP8_CASE(kElFp16, false)

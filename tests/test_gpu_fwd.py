@@ -300,3 +300,69 @@ def test_many_short_units_varlen_deterministic(sdpa):
     b = sdpa.attention_varlen(q, k, v, cu, cu, max(lens), max(lens), scale=0.088, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("d,n", [(128, 90), (128, 120), (64, 300)])
+def test_many_sequences_unit_orders(sdpa, d, n):
+    """Packed unit lists of the one-tile forward: length-sorted sequence-major
+    (sequence table cached in shared memory), sequence-major in the given order
+    (over 256 sequences), and latest-tile-first over all slices (table not
+    cached: more than 95 sequences at d = 128); with empty sequences."""
+    g = np.random.default_rng(n)
+    lens = g.integers(0, 300, n).tolist()
+    lens[3] = 0
+    lens[7] = 513
+    _varlen_case(sdpa, lens, lens, 2, d, True, seed=45 + n)
+
+
+# ------------------------------------- unit orders of problems larger than L2
+# K + V above 64 MiB switch the one-tile forward to slice-group order (dense:
+# batch by batch; packed: sequence by sequence, longest first when the
+# sequence table fits in shared memory).  Sampled rows against the oracle.
+def _sampled_rows(n, salt):
+    return np.unique(np.array([0, n - 1, n // 2, (salt * 13) % n, (salt * 29 + 5) % n], np.int32))
+
+
+def test_slice_major_dense_one_tile(sdpa):
+    b, h, s, d = 8, 32, 1024, 128  # K + V = 134 MB
+    q, k, v, _ = sdpa_inputs.dense(b, h, s, s, d, seed=61)
+    sdpa.sdpa_set_forward_variant(1)
+    try:
+        o, lse = sdpa.attention(q.cuda(), k.cuda(), v.cuda(), scale=0.088, causal=True)
+        torch.cuda.synchronize()
+    finally:
+        sdpa.sdpa_set_forward_variant(0)
+    o, lse = o.cpu(), lse.cpu()
+    for bb, hh in [(0, 0), (3, 17), (7, 31)]:
+        rows = _sampled_rows(s, bb * 32 + hh)
+        ro, rl = oracle.attn_fwd_rows(q[bb, hh], k[bb, hh], v[bb, hh], rows, 0.088, True)
+        check_rel(o[bb, hh][rows], ro, O_TOL[torch.bfloat16], f"o[{bb},{hh}]")
+        check_lse(lse[bb, hh][rows], rl)
+
+
+@pytest.mark.parametrize("d,n,lo,hi", [(128, 40, 1, 400),     # sorted sequence-major
+                                        (64, 300, 0, 60),      # sequence-major, given order
+                                        (128, 120, 0, 120)])   # table not cached
+def test_slice_major_packed_one_tile(sdpa, d, n, lo, hi):
+    h = 32
+    g = np.random.default_rng(n + d)
+    lens = g.integers(lo, hi, n).tolist()
+    lens[1] = 0
+    lens[2] = hi + 200
+    q, k, v, _, cu, _ = sdpa_inputs.packed(lens, lens, h, d, seed=62 + n)
+    assert 2 * k.numel() * 2 > (64 << 20)
+    o, lse = sdpa.attention_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), cu.cuda(), max(lens),
+                                   max(lens), scale=1.0 / math.sqrt(d), causal=True)
+    torch.cuda.synchronize()
+    o, lse = o.cpu(), lse.cpu()
+    cl = cu.tolist()
+    for i, L in enumerate(lens):
+        if L == 0:
+            continue
+        hh = (i * 7) % h
+        a, e = cl[i], cl[i + 1]
+        rows = _sampled_rows(L, i)
+        ro, rl = oracle.attn_fwd_rows(q[a:e, hh], k[a:e, hh], v[a:e, hh], rows, 1.0 / math.sqrt(d),
+                                      True)
+        check_rel(o[a:e, hh][rows], ro, O_TOL[torch.bfloat16], f"o seq {i}")
+        check_lse(lse[a:e, hh][rows], rl, f"lse seq {i}")
