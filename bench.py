@@ -49,7 +49,8 @@ REF_PREFIX = 2048         # tokens of one head per oracle sample
 # full workload (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel
 # and the library version the capture was taken with; any other version
 # reports null.  Source: profiles/bwd_main_dram_c5_b1h32s16384d128.md.
-TRAFFIC = {("bwd_main", "sdpa_gb300 0.4 sm_103a"): 0.81430e9 + 0.49046e9}
+TRAFFIC = {("bwd_main", "sdpa_gb300 0.4 sm_103a"): 0.81430e9 + 0.49046e9,
+           ("bwd_main", "sdpa_gb300 0.6 sm_103a"): 0.83157e9 + 0.50512e9}
 
 
 def fwd_flops(w) -> float:
