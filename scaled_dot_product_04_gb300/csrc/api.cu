@@ -33,12 +33,15 @@ thread_local int t_fwd_variant = 0;  // 0 auto, 1 one-tile, 2 two-tile
 constexpr size_t kSliceMajorKVBytes = size_t(64) << 20;
 
 // Forward kernel choice.  The two-tile kernel (256 query rows per unit, two
-// softmax warpgroups) wins when every unit visits many key tiles; short or
-// packed problems do better with the one-tile kernel's 128-row units.
+// softmax warpgroups) wins when every unit visits many key tiles; short
+// problems do better with the one-tile kernel's 128-row units.  rows_*: the
+// dense lengths, or the packed totals over the sequence count (the mean
+// length, which must be longer: a packed list also holds short sequences).
 bool use_pair_kernel(bool packed, int d, int64_t rows_q, int64_t rows_kv) {
     if (t_fwd_variant == 1) return false;
     if (t_fwd_variant == 2) return true;
-    return !packed && d == 128 && rows_q >= 2048 && rows_kv >= 2048;
+    const int64_t min_rows = packed ? 4096 : 2048;
+    return d == 128 && rows_q >= min_rows && rows_kv >= min_rows;
 }
 
 int fail(int status, const char *fmt, ...) {
@@ -275,7 +278,7 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.6 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.7 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)
@@ -407,7 +410,8 @@ int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o, flo
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const bool pair = window_left < 0 && use_pair_kernel(true, d, max_seqlen_q, max_seqlen_kv);
+    const bool pair = window_left < 0 && use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
+                                                         (int64_t)total_kv / num_seqs);
     const int unit_rows = pair ? fwd_pair_rows() : kTileM;
     const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
     const int64_t slices = (int64_t)num_seqs * h;
@@ -553,7 +557,8 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const bool pair = window_left < 0 && use_pair_kernel(true, d, max_seqlen_q, max_seqlen_kv);
+    const bool pair = window_left < 0 && use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
+                                                         (int64_t)total_kv / num_seqs);
     const int unit_rows = pair ? fwd_pair_rows() : kTileM;
     const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
     const int64_t slices = (int64_t)num_seqs * h;

@@ -37,20 +37,26 @@ namespace {
 constexpr int kPairThreads = 384;
 constexpr int kPairRows = 2 * kTileM;  // query rows per work unit
 
-// kEb: bytes per input element (2 for bf16/fp16, 1 for E4M3).
-template <int D, int kEb = 2>
+// kEb: bytes per input element (2 for bf16/fp16, 1 for E4M3).  kPk: packed
+// inputs, whose cu_seqlens cache also holds the sequence table of the unit
+// list (order, first unit) and a scan scratch.
+template <int D, int kEb = 2, bool kPk = false>
 struct PairLayout {
     static constexpr int kChunks = D * kEb / 128;     // 128-byte swizzle columns per row
     static constexpr int kChunkBytes = kTileM * 128;  // 16 KiB: 128 rows x 128 bytes
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     static constexpr int kKStages = (kTileBytes >= 32768) ? 3 : 5;
     static constexpr int kVStages = (kTileBytes >= 32768) ? 2 : 4;
-    static constexpr int kCuCap = (kTileBytes >= 32768) ? 192 : 2048;  // cu_seqlens entries cached
+    // cu_seqlens entries cached (packed: with the unit list's sequence table)
+    static constexpr int kCuCap = kPk ? ((kTileBytes >= 32768) ? 96 : 1024) : ((kTileBytes >= 32768) ? 192 : 2048);
+    static constexpr int kCuArrays = kPk ? 4 : 2;
     static constexpr int kQ = 0;                             // Q_A, Q_B
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
-    static constexpr int kCu = kV + kVStages * kTileBytes;  // int32 cu_q[kCuCap], cu_kv[kCuCap]
-    static constexpr int kBar = kCu + 2 * kCuCap * 4;
+    // int32 cu_q[kCuCap], cu_kv[kCuCap] (packed: then order[kCuCap], first_unit[kCuCap])
+    static constexpr int kCu = kV + kVStages * kTileBytes;
+    static constexpr int kScan = kCu + kCuArrays * kCuCap * 4;  // packed: 16 int32, per-warp sums
+    static constexpr int kBar = kScan + (kPk ? 64 : 0);
     static constexpr int bQFull = 0;
     static constexpr int bQEmpty = 1;
     static constexpr int bKFull = 2;
@@ -95,11 +101,35 @@ struct PairUnit {
     int64_t o_row0, o_rs, lse_row0, lse_rs;
 };
 
+// Unit u: latest (heaviest) rows first over all slices; packed units with a
+// cached sequence table (order != nullptr) run sequence by sequence instead,
+// longest first: sequence order[i] owns units [first_unit[i], first_unit[i+1]),
+// its 256-row blocks latest first with the heads innermost, so the CTAs in
+// flight share one or two sequences' K and V in L2.
 template <int D, bool kPacked>
-SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const int *cu_kv) {
+SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const int *cu_kv,
+                              const int *order, const int *first_unit) {
     PairUnit U;
-    const int qp = p.q_tiles - 1 - u / p.bh;  // latest (heaviest) rows first
-    U.slice = u % p.bh;
+    int qp;
+    if constexpr (kPacked) {
+        if (order) {
+            int lo = 0, hi = p.num_seqs;  // first_unit[lo] <= u < first_unit[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (first_unit[mid] <= u) lo = mid;
+                else hi = mid;
+            }
+            const int n = order[lo], local = u - first_unit[lo];
+            qp = (cu_q[n + 1] - cu_q[n] + kPairRows - 1) / kPairRows - 1 - local / p.h;
+            U.slice = n * p.h + local % p.h;
+        } else {
+            qp = p.q_tiles - 1 - u / p.bh;
+            U.slice = u % p.bh;
+        }
+    } else {
+        qp = p.q_tiles - 1 - u / p.bh;  // latest (heaviest) rows first
+        U.slice = u % p.bh;
+    }
     if constexpr (!kPacked) {
         U.head = 0;
         U.kv_head = 0;
@@ -151,7 +181,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     constexpr bool kBf16 = kEl == kElBf16;
     constexpr int kEb = kFp8 ? 1 : 2;
     constexpr int kOb = kOut == kElE4m3 ? 1 : 2;
-    using L = PairLayout<D, kEb>;
+    using L = PairLayout<D, kEb, kPacked>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -161,18 +191,66 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
 
-    // cu_seqlens of packed inputs, cached when they fit
+    // cu_seqlens of packed inputs, cached when they fit, and then the
+    // sequence table of the unit list (see decode_pair)
     int *cu_q_s = reinterpret_cast<int *>(smem + L::kCu);
     int *cu_kv_s = cu_q_s + L::kCuCap;
+    int *order_s = cu_kv_s + L::kCuCap;  // packed layout only
+    int *first_s = order_s + L::kCuCap;
     const int *cu_q = p.cu_q, *cu_kv = p.cu_kv;
+    const int *order = nullptr;
+    int n_units = p.n_units;
     if constexpr (kPacked) {
         if (p.num_seqs + 1 <= L::kCuCap) {
-            for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) {
+            const int ns = p.num_seqs;
+            for (int i = threadIdx.x; i <= ns; i += blockDim.x) {
                 cu_q_s[i] = p.cu_q[i];
                 cu_kv_s[i] = p.cu_kv[i];
             }
             cu_q = cu_q_s;
             cu_kv = cu_kv_s;
+            __syncthreads();
+            auto blocks = [&](int n) { return (cu_q_s[n + 1] - cu_q_s[n] + kPairRows - 1) / kPairRows; };
+            // most 256-row blocks first, ties in sequence order (a rank count;
+            // long lists keep their own order)
+            for (int n = threadIdx.x; n < ns; n += blockDim.x) {
+                int rank = n;
+                if (ns <= 256) {
+                    const int bn = blocks(n);
+                    rank = 0;
+                    for (int m = 0; m < ns; ++m) {
+                        const int bm = blocks(m);
+                        rank += (bm > bn || (bm == bn && m < n)) ? 1 : 0;
+                    }
+                }
+                order_s[rank] = n;
+            }
+            __syncthreads();
+            // first_unit = exclusive prefix sum of blocks(order[i]) * h: chunk
+            // sums per thread, scanned in the warp and across the warps
+            int *scan = reinterpret_cast<int *>(smem + L::kScan);
+            const int per = (ns + blockDim.x - 1) / blockDim.x;
+            const int b0 = min(ns, (int)threadIdx.x * per), b1 = min(ns, b0 + per);
+            int csum = 0;
+            for (int i = b0; i < b1; ++i) csum += blocks(order_s[i]) * p.h;
+            int incl = csum;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if ((int)lane >= off) incl += y;
+            }
+            if (lane == 31) scan[warp] = incl;
+            __syncthreads();
+            int run = incl - csum;
+            for (int w = 0; w < (int)warp; ++w) run += scan[w];
+            for (int i = b0; i < b1; ++i) {
+                first_s[i] = run;
+                run += blocks(order_s[i]) * p.h;
+            }
+            if (threadIdx.x == blockDim.x - 1) first_s[ns] = run;  // the last chunk ends the list
+            __syncthreads();
+            order = order_s;
+            n_units = first_s[ns];
         }
     }
 
@@ -206,7 +284,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const WaitCtx wc{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.err, kTagFwd};
-    const int first = blockIdx.x, step = gridDim.x, n_units = p.n_units;
+    const int first = blockIdx.x, step = gridDim.x;
 
     if (warp == 0) {
         // ============================================================ producer
@@ -233,7 +311,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int u = unit_of(k, first, step);
                 if (u >= n_units) break;
-                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv);
+                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
                 const int nmax = max(U.n_kv[0], U.n_kv[1]);
                 if (nmax == 0) continue;
                 // the previous unit's last V goes out before waiting for Q's slot
@@ -330,7 +408,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int u = unit_of(k, first, step);
                 if (u >= n_units) break;
-                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv);
+                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
                 const int nmax = max(U.n_kv[0], U.n_kv[1]);
                 if (nmax == 0) continue;
                 ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) &&
@@ -415,7 +493,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int k = 0; ok; ++k) {
             const int u = unit_of(k, first, step);
             if (u >= n_units) break;
-            const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv);
+            const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
             const int row0 = U.row0 + x * kTileM;
             if (!U.live || row0 >= U.Lq) continue;  // no row of this tile
             const int q_idx = row0 + r;
@@ -605,7 +683,7 @@ template <int D, int kEl, bool kPacked, int kOut>
 cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const FwdParams &p, int grid, cudaStream_t stream,
                           const KernelTimer &timer) {
-    using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2>;
+    using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2, kPacked>;
     auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);

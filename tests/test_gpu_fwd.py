@@ -366,3 +366,32 @@ def test_slice_major_packed_one_tile(sdpa, d, n, lo, hi):
                                       True)
         check_rel(o[a:e, hh][rows], ro, O_TOL[torch.bfloat16], f"o seq {i}")
         check_lse(lse[a:e, hh][rows], rl, f"lse seq {i}")
+
+
+def test_packed_long_sequences_two_tile(sdpa):
+    """A packed problem whose mean sequence length reaches 4096 runs the
+    two-tile kernel by default (longest sequence first); sampled rows against
+    the oracle, and the same bits as the two-tile kernel forced."""
+    lens, h, d = [4200, 4500, 3000, 5000, 100], 4, 128
+    assert sum(lens) // len(lens) < 4096  # the short one keeps the mean below: one-tile
+    for ls in (lens, lens[:4]):
+        q, k, v, _, cu, _ = sdpa_inputs.packed(ls, ls, h, d, seed=71 + len(ls))
+        args = (q.cuda(), k.cuda(), v.cuda(), cu.cuda(), cu.cuda(), max(ls), max(ls))
+        o, lse = sdpa.attention_varlen(*args, scale=0.088, causal=True)
+        sdpa.sdpa_set_forward_variant(2)
+        try:
+            o2, lse2 = sdpa.attention_varlen(*args, scale=0.088, causal=True)
+        finally:
+            sdpa.sdpa_set_forward_variant(0)
+        torch.cuda.synchronize()
+        if len(ls) == 4:
+            assert torch.equal(o, o2) and torch.equal(lse, lse2)
+        o, lse = o.cpu(), lse.cpu()
+        cl = cu.tolist()
+        for i, L in enumerate(ls):
+            hh = i % h
+            a, e = cl[i], cl[i + 1]
+            rows = _sampled_rows(L, i + 3)
+            ro, rl = oracle.attn_fwd_rows(q[a:e, hh], k[a:e, hh], v[a:e, hh], rows, 0.088, True)
+            check_rel(o[a:e, hh][rows], ro, O_TOL[torch.bfloat16], f"o seq {i}")
+            check_lse(lse[a:e, hh][rows], rl, f"lse seq {i}")
