@@ -22,6 +22,9 @@
 //                the exponent unit at the same time);
 //   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B (thread r
 //                owns row r = TMEM lane r), as in fwd.cu.
+// Warps 0..3 (TMA, MMA and two idle warps) form warpgroup 0, which gives up
+// registers with setmaxnreg to the two softmax warpgroups, whose row of S
+// (128 fp32 values) and running state then fit without spilling.
 // TMEM columns: S_A 0, S_B 128, O_A 256, O_B 256 + d.  S_X(j+1) is issued right
 // behind O_X += P_X(j) V_j although P_X lives in the S_X columns: tcgen05.mma
 // instructions of one thread execute in issue order, so the earlier product
@@ -285,196 +288,201 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint32_t tmem = misc[0];
     const WaitCtx wc{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.err, kTagFwd};
     const int first = blockIdx.x, step = gridDim.x;
-
-    if (warp == 0) {
-        // ============================================================ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            // V_x goes out one tile after K_x, so a wait for a free V stage
-            // never holds back the K load the next S products need first.
-            int k_it = 0, v_it = 0, units = 0;
-            int pv_y = 0, pv_z = 0;
-            bool v_pending = false, ok = true;
-            auto issue_v = [&](int y, int z) -> bool {
-                const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
-                if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) return false;
-                mbar_arrive_expect_tx(bar(L::bVFull + vs), L::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
-                                bar(L::bVFull + vs), c * (128 / kEb), y, z);
-                ++v_it;
-                return true;
-            };
-            for (int k = 0; ok; ++k) {
-                const int u = unit_of(k, first, step);
-                if (u >= n_units) break;
-                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
-                const int nmax = max(U.n_kv[0], U.n_kv[1]);
-                if (nmax == 0) continue;
-                // the previous unit's last V goes out before waiting for Q's slot
-                if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
-                v_pending = false;
-                if (units > 0 && !mbar_wait(bar(L::bQEmpty), (units - 1) & 1, wc, 1)) break;
-                mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTileBytes);
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int qy = kPacked ? U.head : U.row0 + x * kTileM;
-                    const int qz = kPacked ? U.tok_q0 + U.row0 + x * kTileM : U.slice;
-#pragma unroll
+    // Registers: warpgroup 0 (TMA, MMA, two idle warps) hands 64 per thread
+    // to the two softmax warpgroups: 128 x 104 + 256 x 200 = 384 x 168.
+    if (warp < 4) {
+        setmaxnreg_dec<104>();
+        if (warp == 0) {
+            // ============================================================ producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                // V_x goes out one tile after K_x, so a wait for a free V stage
+                // never holds back the K load the next S products need first.
+                int k_it = 0, v_it = 0, units = 0;
+                int pv_y = 0, pv_z = 0;
+                bool v_pending = false, ok = true;
+                auto issue_v = [&](int y, int z) -> bool {
+                    const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
+                    if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) return false;
+                    mbar_arrive_expect_tx(bar(L::bVFull + vs), L::kTileBytes);
+    #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sbase + L::kQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q,
-                                    bar(L::bQFull), c * (128 / kEb), qy, qz);
-                }
-                ++units;
-                for (int j = 0; j < nmax; ++j) {
-                    const int ky = kPacked ? U.kv_head : j * kTileN;
-                    const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.kv_slice;
-                    const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
-                    if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(L::bKFull + ks), L::kTileBytes);
-#pragma unroll
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
-                                    bar(L::bKFull + ks), c * (128 / kEb), ky, kz);
-                    ++k_it;
+                        tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
+                                    bar(L::bVFull + vs), c * (128 / kEb), y, z);
+                    ++v_it;
+                    return true;
+                };
+                for (int k = 0; ok; ++k) {
+                    const int u = unit_of(k, first, step);
+                    if (u >= n_units) break;
+                    const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
+                    const int nmax = max(U.n_kv[0], U.n_kv[1]);
+                    if (nmax == 0) continue;
+                    // the previous unit's last V goes out before waiting for Q's slot
                     if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
-                    pv_y = ky;
-                    pv_z = kz;
-                    v_pending = true;
-                }
-            }
-            if (ok && v_pending) issue_v(pv_y, pv_z);
-            // Every load issued must land before the CTA may exit.
-            if (units > 0) mbar_wait_drain(bar(L::bQFull), (units - 1) & 1);
-            for (int i = max(0, k_it - L::kKStages); i < k_it; ++i)
-                mbar_wait_drain(bar(L::bKFull + i % L::kKStages), (i / L::kKStages) & 1);
-            for (int i = max(0, v_it - L::kVStages); i < v_it; ++i)
-                mbar_wait_drain(bar(L::bVFull + i % L::kVStages), (i / L::kVStages) & 1);
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ============================================================ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = kFp8 ? make_idesc_e4m3(kTileM, kTileN, false, false)
-                                              : make_idesc_f16(kTileM, kTileN, kBf16, false, false);
-            constexpr uint32_t idesc_o = kFp8 ? make_idesc_e4m3(kTileM, D, false, true)
-                                              : make_idesc_f16(kTileM, D, kBf16, false, true);
-            // Operand descriptors, built once and advanced by constant offsets
-            // (a descriptor's low 14 bits are the address / 16).
-            constexpr uint32_t kChunk16 = L::kChunkBytes >> 4, kTile16 = L::kTileBytes >> 4;
-            const uint64_t dQ_k = smem_desc_sw128(sbase + L::kQ, 16, 1024);
-            const uint64_t dK_k = smem_desc_sw128(sbase + L::kK, 16, 1024);
-            const uint64_t dV_mn = smem_desc_sw128(sbase + L::kV, L::kChunkBytes, 1024);
-            // S_X = Q_X K^T: both operands K-major (head dim contiguous), 32
-            // bytes (16 bf16 or 32 E4M3 elements) per step.
-            auto issue_s = [&](int x, int ks) {
-                const uint64_t a = dQ_k + x * kTile16, b = dK_k + ks * kTile16;
-#pragma unroll
-                for (int k = 0; k < D * kEb / 32; ++k) {
-                    const uint32_t off = (k / 4) * kChunk16 + (k % 4) * 2;
-                    if constexpr (kFp8)
-                        mma_ss_f8(tmem + L::kColS + x * 128, a + off, b + off, idesc_s, k > 0);
-                    else
-                        mma_ss(tmem + L::kColS + x * 128, a + off, b + off, idesc_s, k > 0);
-                }
-            };
-            // O_X += P_X V: P from TMEM (8 columns per step: 16 keys as bf16
-            // pairs or 32 keys as E4M3 quads), V MN-major (head dim
-            // contiguous); 128-byte head-dim chunks are 16 KiB apart (leading
-            // offset), 8-key groups 1 KiB apart, so a step advances 2 or 4 KiB.
-            auto issue_pv = [&](int x, int vs, bool acc) {
-                const uint64_t b = dV_mn + vs * kTile16;
-#pragma unroll
-                for (int k = 0; k < kTileN * kEb / 32; ++k) {
-                    const uint64_t vdesc = b + k * ((4096 / kEb) >> 4);
-                    if constexpr (kFp8)
-                        mma_ts_f8(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8, vdesc,
-                                  idesc_o, (acc || k > 0) ? 1u : 0u);
-                    else
-                        mma_ts(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8, vdesc,
-                               idesc_o, (acc || k > 0) ? 1u : 0u);
-                }
-            };
-            // cnt[x]: products P_X V issued so far (one per tile of X); uo[x]:
-            // units in which tile X took part.
-            int t = 0, units = 0, cnt[2] = {0, 0}, uo[2] = {0, 0};
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
-                const int u = unit_of(k, first, step);
-                if (u >= n_units) break;
-                const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
-                const int nmax = max(U.n_kv[0], U.n_kv[1]);
-                if (nmax == 0) continue;
-                ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) &&
-                     mbar_wait(bar(L::bKFull + t % L::kKStages), (t / L::kKStages) & 1, wc, 5);
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    if (!ok || U.n_kv[x] == 0) continue;
-                    tc_fence_after();
-                    issue_s(x, t % L::kKStages);
-                    mma_commit(bar(L::bSFull + x));
-                }
-                if (!ok) break;
-                mma_commit(bar(L::bKEmpty + t % L::kKStages));
-                if (nmax == 1) mma_commit(bar(L::bQEmpty));
-                // Per key tile j: O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1).
-                for (int j = 0; j < nmax; ++j, ++t) {
-                    const int t1 = t + 1;
-                    bool k_next = false;  // K_{j+1} seen to have landed
-                    ok = mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 7);
-#pragma unroll
+                    v_pending = false;
+                    if (units > 0 && !mbar_wait(bar(L::bQEmpty), (units - 1) & 1, wc, 1)) break;
+                    mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTileBytes);
+    #pragma unroll
                     for (int x = 0; x < 2; ++x) {
-                        if (!ok || j >= U.n_kv[x]) continue;
-                        ok = mbar_wait(bar(L::bPReady + x), cnt[x] & 1, wc, 8);
-                        // the unit's first P V overwrites O_X: its previous
-                        // epilogue must have read it out
-                        if (ok && j == 0 && uo[x] > 0)
-                            ok = mbar_wait(bar(L::bOFree + x), (uo[x] - 1) & 1, wc, 9);
-                        if (!ok) continue;
-                        tc_fence_after();
-                        issue_pv(x, t % L::kVStages, j > 0);
-                        ++cnt[x];
-                        if (j + 1 >= U.n_kv[x]) continue;
-                        if (!k_next) {
-                            ok = mbar_wait(bar(L::bKFull + t1 % L::kKStages), (t1 / L::kKStages) & 1,
-                                           wc, 10);
-                            k_next = true;
+                        const int qy = kPacked ? U.head : U.row0 + x * kTileM;
+                        const int qz = kPacked ? U.tok_q0 + U.row0 + x * kTileM : U.slice;
+    #pragma unroll
+                        for (int c = 0; c < L::kChunks; ++c)
+                            tma_load_3d(sbase + L::kQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q,
+                                        bar(L::bQFull), c * (128 / kEb), qy, qz);
+                    }
+                    ++units;
+                    for (int j = 0; j < nmax; ++j) {
+                        const int ky = kPacked ? U.kv_head : j * kTileN;
+                        const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.kv_slice;
+                        const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
+                        if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
+                            ok = false;
+                            break;
                         }
-                        // S_X(j+1) overwrites the P_X(j) that O_X += P_X V
-                        // reads; issue order keeps them apart (see the header)
-                        if (!ok) continue;
+                        mbar_arrive_expect_tx(bar(L::bKFull + ks), L::kTileBytes);
+    #pragma unroll
+                        for (int c = 0; c < L::kChunks; ++c)
+                            tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
+                                        bar(L::bKFull + ks), c * (128 / kEb), ky, kz);
+                        ++k_it;
+                        if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
+                        pv_y = ky;
+                        pv_z = kz;
+                        v_pending = true;
+                    }
+                }
+                if (ok && v_pending) issue_v(pv_y, pv_z);
+                // Every load issued must land before the CTA may exit.
+                if (units > 0) mbar_wait_drain(bar(L::bQFull), (units - 1) & 1);
+                for (int i = max(0, k_it - L::kKStages); i < k_it; ++i)
+                    mbar_wait_drain(bar(L::bKFull + i % L::kKStages), (i / L::kKStages) & 1);
+                for (int i = max(0, v_it - L::kVStages); i < v_it; ++i)
+                    mbar_wait_drain(bar(L::bVFull + i % L::kVStages), (i / L::kVStages) & 1);
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            // ============================================================ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idesc_s = kFp8 ? make_idesc_e4m3(kTileM, kTileN, false, false)
+                                                  : make_idesc_f16(kTileM, kTileN, kBf16, false, false);
+                constexpr uint32_t idesc_o = kFp8 ? make_idesc_e4m3(kTileM, D, false, true)
+                                                  : make_idesc_f16(kTileM, D, kBf16, false, true);
+                // Operand descriptors, built once and advanced by constant offsets
+                // (a descriptor's low 14 bits are the address / 16).
+                constexpr uint32_t kChunk16 = L::kChunkBytes >> 4, kTile16 = L::kTileBytes >> 4;
+                const uint64_t dQ_k = smem_desc_sw128(sbase + L::kQ, 16, 1024);
+                const uint64_t dK_k = smem_desc_sw128(sbase + L::kK, 16, 1024);
+                const uint64_t dV_mn = smem_desc_sw128(sbase + L::kV, L::kChunkBytes, 1024);
+                // S_X = Q_X K^T: both operands K-major (head dim contiguous), 32
+                // bytes (16 bf16 or 32 E4M3 elements) per step.
+                auto issue_s = [&](int x, int ks) {
+                    const uint64_t a = dQ_k + x * kTile16, b = dK_k + ks * kTile16;
+    #pragma unroll
+                    for (int k = 0; k < D * kEb / 32; ++k) {
+                        const uint32_t off = (k / 4) * kChunk16 + (k % 4) * 2;
+                        if constexpr (kFp8)
+                            mma_ss_f8(tmem + L::kColS + x * 128, a + off, b + off, idesc_s, k > 0);
+                        else
+                            mma_ss(tmem + L::kColS + x * 128, a + off, b + off, idesc_s, k > 0);
+                    }
+                };
+                // O_X += P_X V: P from TMEM (8 columns per step: 16 keys as bf16
+                // pairs or 32 keys as E4M3 quads), V MN-major (head dim
+                // contiguous); 128-byte head-dim chunks are 16 KiB apart (leading
+                // offset), 8-key groups 1 KiB apart, so a step advances 2 or 4 KiB.
+                auto issue_pv = [&](int x, int vs, bool acc) {
+                    const uint64_t b = dV_mn + vs * kTile16;
+    #pragma unroll
+                    for (int k = 0; k < kTileN * kEb / 32; ++k) {
+                        const uint64_t vdesc = b + k * ((4096 / kEb) >> 4);
+                        if constexpr (kFp8)
+                            mma_ts_f8(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8, vdesc,
+                                      idesc_o, (acc || k > 0) ? 1u : 0u);
+                        else
+                            mma_ts(tmem + L::kColO + x * D, tmem + L::kColS + x * 128 + k * 8, vdesc,
+                                   idesc_o, (acc || k > 0) ? 1u : 0u);
+                    }
+                };
+                // cnt[x]: products P_X V issued so far (one per tile of X); uo[x]:
+                // units in which tile X took part.
+                int t = 0, units = 0, cnt[2] = {0, 0}, uo[2] = {0, 0};
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int u = unit_of(k, first, step);
+                    if (u >= n_units) break;
+                    const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
+                    const int nmax = max(U.n_kv[0], U.n_kv[1]);
+                    if (nmax == 0) continue;
+                    ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) &&
+                         mbar_wait(bar(L::bKFull + t % L::kKStages), (t / L::kKStages) & 1, wc, 5);
+    #pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (!ok || U.n_kv[x] == 0) continue;
                         tc_fence_after();
-                        issue_s(x, t1 % L::kKStages);
+                        issue_s(x, t % L::kKStages);
                         mma_commit(bar(L::bSFull + x));
                     }
                     if (!ok) break;
-                    mma_commit(bar(L::bVEmpty + t % L::kVStages));
-                    if (j + 1 < nmax) {
-                        mma_commit(bar(L::bKEmpty + t1 % L::kKStages));
-                        if (j + 2 == nmax) mma_commit(bar(L::bQEmpty));  // last reader of Q
+                    mma_commit(bar(L::bKEmpty + t % L::kKStages));
+                    if (nmax == 1) mma_commit(bar(L::bQEmpty));
+                    // Per key tile j: O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1).
+                    for (int j = 0; j < nmax; ++j, ++t) {
+                        const int t1 = t + 1;
+                        bool k_next = false;  // K_{j+1} seen to have landed
+                        ok = mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 7);
+    #pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            if (!ok || j >= U.n_kv[x]) continue;
+                            ok = mbar_wait(bar(L::bPReady + x), cnt[x] & 1, wc, 8);
+                            // the unit's first P V overwrites O_X: its previous
+                            // epilogue must have read it out
+                            if (ok && j == 0 && uo[x] > 0)
+                                ok = mbar_wait(bar(L::bOFree + x), (uo[x] - 1) & 1, wc, 9);
+                            if (!ok) continue;
+                            tc_fence_after();
+                            issue_pv(x, t % L::kVStages, j > 0);
+                            ++cnt[x];
+                            if (j + 1 >= U.n_kv[x]) continue;
+                            if (!k_next) {
+                                ok = mbar_wait(bar(L::bKFull + t1 % L::kKStages), (t1 / L::kKStages) & 1,
+                                               wc, 10);
+                                k_next = true;
+                            }
+                            // S_X(j+1) overwrites the P_X(j) that O_X += P_X V
+                            // reads; issue order keeps them apart (see the header)
+                            if (!ok) continue;
+                            tc_fence_after();
+                            issue_s(x, t1 % L::kKStages);
+                            mma_commit(bar(L::bSFull + x));
+                        }
+                        if (!ok) break;
+                        mma_commit(bar(L::bVEmpty + t % L::kVStages));
+                        if (j + 1 < nmax) {
+                            mma_commit(bar(L::bKEmpty + t1 % L::kKStages));
+                            if (j + 2 == nmax) mma_commit(bar(L::bQEmpty));  // last reader of Q
+                        }
                     }
+                    if (!ok) break;
+    #pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (U.n_kv[x] == 0) continue;
+                        mma_commit(bar(L::bOFull + x));
+                        ++uo[x];
+                    }
+                    ++units;
                 }
-                if (!ok) break;
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    if (U.n_kv[x] == 0) continue;
-                    mma_commit(bar(L::bOFull + x));
-                    ++uo[x];
-                }
-                ++units;
+                // Let every MMA issued above retire before TMEM is released.
+                mma_commit(bar(L::bMmaIdle));
+                mbar_wait_drain(bar(L::bMmaIdle), 0);
             }
-            // Let every MMA issued above retire before TMEM is released.
-            mma_commit(bar(L::bMmaIdle));
-            mbar_wait_drain(bar(L::bMmaIdle), 0);
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp >= 4) {
+    } else {
+        setmaxnreg_inc<200>();
         // ============================================================ softmax
         const int x = (warp - 4) >> 2;  // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
         const int quad = warp & 3;

@@ -53,6 +53,16 @@ SDPA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Per-warpgroup register budgets (all four warps of a warpgroup execute it).
+template <uint32_t N>
+SDPA_DEV void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+SDPA_DEV void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Bounded-wait bookkeeping shared by all roles of one CTA.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // two seconds
 
