@@ -356,7 +356,7 @@ void sdpa_set_kernel_timer(void *start_event, void *stop_event);
  */
 int sdpa_set_forward_variant(int variant);
 
-/* Library version string, e.g. "sdpa_gb300 0.7 sm_103a"; the
+/* Library version string, e.g. "sdpa_gb300 0.8 sm_103a"; the
  * minor number changes whenever a kernel changes. */
 const char *sdpa_version(void);
 
