@@ -21,7 +21,14 @@ a bounded sample of the same workload (rank 0 only).
 line is the default, bf16): ``deterministic`` runs the backward with its
 deterministic dQ pass (the backward timer then spans the main kernel and the
 dQ pass), ``fp8`` times the E4M3 forward alone (bf16 output) against the FP8
-tensor peak (the measured bf16 peak x 2, the nominal FP8/BF16 ratio).
+tensor peak (the measured bf16 peak x 2, the nominal FP8/BF16 ratio).  The
+mask and head-sharing rows run the forward + backward step through the
+extended calls: ``gqa`` with 8 key/value heads for the 32 query heads,
+``window`` with the causal mask and window_left = 2048, ``bottom_right`` with
+4096 queries against the 16384 keys under the bottom-right causal mask.  Their
+FLOPs count the visible (query, key) pairs exactly (4*d per pair forward,
+2.5x that backward), since the pages' halving applies to the plain causal
+square only.
 """
 from __future__ import annotations
 
@@ -60,6 +67,26 @@ def fwd_flops(w) -> float:
     return 4.0 * w.b * w.h * w.s * w.s * w.d * (0.5 if w.causal else 1.0)
 
 
+# Extended-call variants on the default workload: key/value heads, query
+# length, mask (0 none, 1 top-left causal, 2 bottom-right causal), window_left.
+EXT_VARIANTS = {"gqa": dict(h_kv=8, s_q=None, mask=1, window=-1),
+                "window": dict(h_kv=None, s_q=None, mask=1, window=2048),
+                "bottom_right": dict(h_kv=None, s_q=4096, mask=2, window=-1)}
+
+
+def visible_pairs(s_q: int, s_kv: int, mask: int, window: int) -> int:
+    """(query, key) pairs the mask leaves visible in one (b, h) slice: row i
+    sees keys [max(0, i + delta - window), min(s_kv, i + delta + 1)) with
+    delta = s_kv - s_q for the bottom-right mask and 0 otherwise (no upper
+    bound without a causal mask, no lower bound without a window)."""
+    import numpy as np
+    i = np.arange(s_q, dtype=np.int64)
+    delta = s_kv - s_q if mask == 2 else 0
+    hi = np.minimum(s_kv, i + delta + 1) if mask != 0 else np.full(s_q, s_kv, np.int64)
+    lo = np.maximum(0, i + delta - window) if window >= 0 else np.zeros(s_q, np.int64)
+    return int(np.maximum(hi - lo, 0).sum())
+
+
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -72,8 +99,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--variant", choices=["bf16", "deterministic", "fp8"], default="bf16",
-                    help="bf16 (default, the headline), deterministic backward, or FP8 forward")
+    ap.add_argument("--variant", choices=["bf16", "deterministic", "fp8"] + list(EXT_VARIANTS),
+                    default="bf16",
+                    help="bf16 (default, the headline), deterministic backward, FP8 forward, or "
+                         "an extended-call row (gqa, window, bottom_right)")
     return ap.parse_args()
 
 
@@ -258,6 +287,14 @@ def run_ours(args):
     variant = args.variant
     fp8 = variant == "fp8"
     det = 1 if variant == "deterministic" else 0
+    ext = EXT_VARIANTS.get(variant)
+    hk, s_q, mask, window = h, s, causal, -1
+    if ext:
+        hk = ext["h_kv"] or h
+        s_q = ext["s_q"] or s
+        mask, window = ext["mask"], ext["window"]
+        qq, kk, vv, dd = sdpa_inputs.dense(b, h, s_q, s, d, w.seed, qk_mult=w.qk_mult, h_kv=hk)
+        t = dict(t, q=qq, k=kk, v=vv, do=dd)
     if fp8:
         # E4M3 codes of the workload's own Q, K, V with per-tensor descales
         enc = [sdpa_inputs.fp8_quantize(t[x].float()) for x in ("q", "k", "v")]
@@ -265,14 +302,14 @@ def run_ours(args):
         descales = [torch.tensor([e[1]], dtype=torch.float32, device=dev) for e in enc]
     q, k, v, do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((b, h, s), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(do), torch.empty_like(do), torch.empty_like(do)
-    ws = torch.empty(max(1, sdpa.sdpa_bwd_ex_workspace_size(b, h, s, d, det)), dtype=torch.uint8,
-                     device=dev)
+    lse = torch.empty((b, h, s_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(do), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(1, sdpa.sdpa_bwd_ex_workspace_size(b, h, s_q, d, det)),
+                     dtype=torch.uint8, device=dev)
     amax = torch.empty(1, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    f_fwd = fwd_flops(w)
+    f_fwd = 4.0 * b * h * d * visible_pairs(s_q, s, mask, window) if ext else fwd_flops(w)
     f_step = f_fwd if fp8 else f_fwd * (1.0 + BWD_FACTOR)
 
     def step(ev_f=None, ev_b=None):
@@ -283,10 +320,16 @@ def run_ours(args):
                               causal, -1, 0, stream)
             sdpa.sdpa_set_kernel_timer(None, None)
             return
-        sdpa.sdpa_fwd(q, k, v, o, lse, b, h, s, s, d, scale, causal, 0, stream)
+        if ext:
+            sdpa.sdpa_fwd_ex(q, k, v, o, lse, b, h, hk, s_q, s, d, scale, mask, window, 0, stream)
+        else:
+            sdpa.sdpa_fwd(q, k, v, o, lse, b, h, s, s, d, scale, causal, 0, stream)
         if ev_b:
             sdpa.sdpa_set_kernel_timer(*ev_b)
-        if det:
+        if ext:
+            sdpa.sdpa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, b, h, hk, s_q, s, d, scale, mask,
+                             window, 0, 0, ws, ws.numel(), stream)
+        elif det:
             sdpa.sdpa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, b, h, h, s, s, d, scale, causal, -1,
                              1, 0, ws, ws.numel(), stream)
         else:
@@ -369,8 +412,14 @@ def run_ours(args):
                 return
             ddo = ins[3]
             gq, gk, gv = outs[2], outs[3], outs[4]
-            sdpa.sdpa_fwd(qq, kk, vv, oo, ll, b, h, s, s, d, scale, causal, 0, stream)
             wsi = ws2[i & 1]
+            if ext:
+                sdpa.sdpa_fwd_ex(qq, kk, vv, oo, ll, b, h, hk, s_q, s, d, scale, mask, window, 0,
+                                 stream)
+                sdpa.sdpa_bwd_ex(qq, kk, vv, oo, ddo, ll, gq, gk, gv, b, h, hk, s_q, s, d, scale,
+                                 mask, window, 0, 0, wsi, wsi.numel(), stream)
+                return
+            sdpa.sdpa_fwd(qq, kk, vv, oo, ll, b, h, s, s, d, scale, causal, 0, stream)
             if det:
                 sdpa.sdpa_bwd_ex(qq, kk, vv, oo, ddo, ll, gq, gk, gv, b, h, h, s, s, d, scale,
                                  causal, -1, 1, 0, wsi, wsi.numel(), stream)
@@ -431,7 +480,8 @@ def run_ours(args):
     ratio = 2.0 if fp8 else 1.0  # nominal FP8 / BF16 dense tensor rate
     peak = float(peaks["bf16_tflops_sustained"]) * ratio
     version = sdpa.sdpa_version()
-    tr = TRAFFIC.get((kern, version))
+    # the captures are of the default workload and variant
+    tr = TRAFFIC.get((kern, version)) if variant == "bf16" and w.name == WORKLOAD else None
     src = (f"{peak_src} sustained bf16 (MEASURED_PEAKS.json)" if peak_src == "measured"
            else "fallback sustained bf16")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -452,7 +502,7 @@ def run_ours(args):
     }
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8 and not ext:
         rate, spent, n, threads = oracle_sample_rate(w, t, min_s=10.0, max_s=30.0)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} heads of {w.name}, each cut to its first "
@@ -466,8 +516,11 @@ def run_ours(args):
             "dtype": "e4m3" if fp8 else "bf16",
             "data": "synthetic (seeded N(0,1) bf16" + (", Q and K x2" if w.qk_mult != 1 else "")
                     + (", encoded as E4M3 with per-tensor descales)" if fp8 else ")"),
-            "config": {"workload": w.name, "b": b, "h": h, "s_q": s, "s_kv": s, "d": d,
+            "config": {"workload": w.name, "b": b, "h": h, "s_q": s_q, "s_kv": s, "d": d,
                        "causal": bool(causal), "layout": "bhsd", "variant": variant,
+                       **({"h_kv": hk, "mask": ["none", "causal", "causal_bottom_right"][mask],
+                           "window_left": window,
+                           "flops": "4*d*(visible pairs) fwd, 2.5x bwd"} if ext else {}),
                        "step": ("FP8 fwd (O bf16, LSE, amax)" if fp8 else
                                 "fwd (O, LSE) + bwd (dQ, dK, dV)"
                                 + (", deterministic dQ pass" if det else "")),

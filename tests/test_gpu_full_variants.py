@@ -82,3 +82,44 @@ def test_full_size_fp8_fwd_sampled(sdpa):
         bound = 2.0 ** -4 * float(np.abs(vd).max()) + 2.0 ** -8 * float(np.abs(ro).max()) + 1e-6
         assert err <= bound, f"head {hh}: max|dO| {err:.3e} > bound {bound:.3e}"
         check_lse(lse[0, hh][rows], rlse, f"lse[{hh}]")
+
+
+# The extended-call rows as bench.py runs them on the long workload: 8
+# key/value heads; causal with window_left = 2048; 4096 queries against the
+# 16384 keys under the bottom-right mask.  Sampled rows of O, LSE, dQ, dK, dV
+# against the oracle's extended definitions (GQA: a key/value head's dK and dV
+# sum over its group's query heads).
+EXT = {"gqa": (8, 16384, "top_left", -1),
+       "window": (32, 16384, "top_left", 2048),
+       "bottom_right": (32, 4096, "bottom_right", -1)}
+
+
+@pytest.mark.parametrize("name", list(EXT))
+def test_full_size_extended_rows_sampled(sdpa, name):
+    from helpers import O_TOL
+    w = sdpa_inputs.WORKLOADS[NAME]
+    h_kv, s_q, mask, window = EXT[name]
+    q, k, v, do = sdpa_inputs.dense(w.b, w.h, s_q, w.s, w.d, w.seed, qk_mult=w.qk_mult,
+                                    h_kv=h_kv)
+    qg, kg, vg, dog = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = sdpa.attention(qg, kg, vg, scale=w.scale, mask=mask, window_left=window)
+    dq, dk, dv = sdpa.attention_bwd(qg, kg, vg, o, dog, lse, scale=w.scale, mask=mask,
+                                    window_left=window)
+    torch.cuda.synchronize()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    del qg, kg, vg, dog
+    group = w.h // h_kv
+    hk = min(1, h_kv - 1)
+    heads = [hk * group + g for g in range(group)]
+    qr, kr = _rows(s_q, 7), _rows(w.s, 8)
+    r_dk = r_dv = 0
+    for hh in heads:
+        ro, rl = oracle.attn_fwd_rows_ex(q[0, hh], k[0, hk], v[0, hk], qr, w.scale, mask, window)
+        check_rel(o[0, hh][qr], ro, O_TOL[torch.bfloat16], f"o[{hh}]")
+        check_lse(lse[0, hh][qr], rl, f"lse[{hh}]")
+        g_dq, g_dk, g_dv = oracle.attn_bwd_rows_ex(q[0, hh], k[0, hk], v[0, hk], do[0, hh], qr,
+                                                   kr, w.scale, mask, window)
+        check_rel(dq[0, hh][qr], g_dq, GRAD_TOL, f"dq[{hh}]")
+        r_dk, r_dv = r_dk + g_dk, r_dv + g_dv
+    check_rel(dk[0, hk][kr], r_dk, GRAD_TOL, f"dk[{hk}]")
+    check_rel(dv[0, hk][kr], r_dv, GRAD_TOL, f"dv[{hk}]")
