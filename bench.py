@@ -99,6 +99,13 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--configs", action="store_true",
+                    help="instead of the benchmark line: time the forward and the backward "
+                         "chain of every configured workload, one JSON line each")
+    ap.add_argument("--only", default=None, help="with --configs: this workload only")
+    ap.add_argument("--probe", action="store_true",
+                    help="with --configs --only: run the forward and backward three times "
+                         "and print nothing else (a launch set for a profiler)")
     ap.add_argument("--variant", choices=["bf16", "deterministic", "fp8"] + list(EXT_VARIANTS),
                     default="bf16",
                     help="bf16 (default, the headline), deterministic backward, FP8 forward, or "
@@ -539,8 +546,91 @@ def run_ours(args):
     return 0
 
 
+def run_configs(args):
+    """Forward and backward chain of every configured workload (dense and
+    packed): CUDA events around each call with a 512 MiB L2 flush before it,
+    median of 15; the main kernels alone through the kernel timer, median of 11."""
+    import torch
+
+    import sdpa_inputs
+    import scaled_dot_product_04_gb300 as sdpa
+    sdpa.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    names = [args.only] if args.only else list(sdpa_inputs.WORKLOADS)
+    for name in names:
+        w = sdpa_inputs.WORKLOADS[name]
+        t = sdpa_inputs.make(w)
+        q, k, v, do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
+        if w.layout == "bhsd":
+            def fwd():
+                return sdpa.attention(q, k, v, scale=w.scale, causal=w.causal)
+            o, lse = fwd()
+
+            def bwd():
+                return sdpa.attention_bwd(q, k, v, o, do, lse, scale=w.scale, causal=w.causal)
+            flops = fwd_flops(w)
+        else:
+            lens, cu = t["lengths"], t["cu_q"].to(dev)
+
+            def fwd():
+                return sdpa.attention_varlen(q, k, v, cu, cu, max(lens), max(lens),
+                                             scale=w.scale, causal=w.causal)
+            o, lse = fwd()
+
+            def bwd():
+                return sdpa.attention_varlen_bwd(q, k, v, o, do, lse, cu, cu, max(lens),
+                                                 max(lens), scale=w.scale, causal=w.causal)
+            flops = sum(4.0 * w.h * n * n * w.d * (0.5 if w.causal else 1.0) for n in lens)
+        if args.probe:
+            for _ in range(3):
+                fwd()
+                bwd()
+            torch.cuda.synchronize(dev)
+            continue
+
+        def call_ms(fn, iters=15):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(iters):
+                flush.zero_()
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                z.record()
+                torch.cuda.synchronize(dev)
+                ts.append(a.elapsed_time(z))
+            return statistics.median(ts)
+
+        def kernel_ms(fn, iters=11):
+            ts = []
+            for _ in range(iters):
+                flush.zero_()
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                sdpa.sdpa_set_kernel_timer(a, z)
+                fn()
+                sdpa.sdpa_set_kernel_timer(None, None)
+                torch.cuda.synchronize(dev)
+                ts.append(a.elapsed_time(z))
+            return statistics.median(ts)
+
+        f_ms, fk_ms, b_ms, bk_ms = call_ms(fwd), kernel_ms(fwd), call_ms(bwd), kernel_ms(bwd)
+        sdpa.sdpa_check_device_error()
+        print(json.dumps({
+            "workload": name, "fwd_flops": flops, "bwd_flops": BWD_FACTOR * flops,
+            "fwd_ms": f_ms, "fwd_kernel_ms": fk_ms, "fwd_tflops": flops / f_ms / 1e9,
+            "bwd_chain_ms": b_ms, "bwd_main_ms": bk_ms,
+            "bwd_chain_tflops": BWD_FACTOR * flops / b_ms / 1e9,
+            "bwd_main_tflops": BWD_FACTOR * flops / bk_ms / 1e9,
+            "library": sdpa.sdpa_version()}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.configs:
+        return run_configs(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
