@@ -278,7 +278,7 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.8 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.9 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)
@@ -330,7 +330,8 @@ int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
         return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d s_q=%d s_kv=%d)", b, s_q, s_kv);
     const int64_t bh = (int64_t)b * h, bh_kv = (int64_t)b * h_kv;
     if (bh == 0 || s_q == 0) return ok();
-    const bool pair = window_left < 0 && use_pair_kernel(false, d, s_q, s_kv);
+    // left windows take the two-tile kernel at d = 128 only (its walking instantiations)
+    const bool pair = use_pair_kernel(false, d, s_q, s_kv) && (window_left < 0 || d == 128);
     const int unit_rows = pair ? fwd_pair_rows() : kTileM;
     const int64_t q_tiles = (s_q + unit_rows - 1) / unit_rows;
     if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
@@ -410,8 +411,9 @@ int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o, flo
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const bool pair = window_left < 0 && use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
-                                                         (int64_t)total_kv / num_seqs);
+    const bool pair = use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
+                                      (int64_t)total_kv / num_seqs) &&
+                      (window_left < 0 || d == 128);
     const int unit_rows = pair ? fwd_pair_rows() : kTileM;
     const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
     const int64_t slices = (int64_t)num_seqs * h;
@@ -493,6 +495,7 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
         return fail(SDPA_ERR_INVALID_ARG, "negative size (b=%d s_q=%d s_kv=%d)", b, s_q, s_kv);
     const int64_t bh = (int64_t)b * h, bh_kv = (int64_t)b * h_kv;
     if (bh == 0 || s_q == 0) return ok();
+    // FP8 with a left window runs the one-tile kernel
     const bool pair = window_left < 0 && use_pair_kernel(false, d, s_q, s_kv);
     const int unit_rows = pair ? fwd_pair_rows() : kTileM;
     const int64_t q_tiles = (s_q + unit_rows - 1) / unit_rows;

@@ -5,10 +5,13 @@
 // fwd.cu ("Inside NVIDIA's cuDNN Graph API" (tradepoint.io), section 5;
 // cudnn-frontend PR #554 notes on scale_softmax_log2, LSE layouts, the `sdpa`
 // op's masks and GQA, persistent scheduling and the packed total clamp); the
-// host picks this kernel for long dense d = 128 problems without a window,
-// where every unit visits many key tiles.  Both tiles walk key tiles from 0
-// (a window is still honoured, by the mask, at the cost of the tiles it
-// hides).
+// host picks this kernel for long d = 128 problems, where every unit visits
+// many key tiles.  Without a left window both tiles walk the key tiles from 0
+// (tile A leaves one key tile before B under a causal mask).  The kWin
+// instantiations, for left windows, walk from the first key tile tile A can
+// see (kt0); tile X takes part in steps [first[X], n_kv[X]) of that walk, so
+// tile B joins one key tile after A.  They are separate instantiations so
+// that the unwindowed loop compiles exactly as it would without them.
 //
 // Roles inside a CTA (12 warps):
 //   warp 0       TMA producer: Q_A, Q_B of each unit, then K_j and V_j into
@@ -99,7 +102,9 @@ SDPA_DEV int unit_of(int k, int first, int step) {
 // 128 rows, tile B the next 128.
 struct PairUnit {
     int slice, head, kv_slice, kv_head, Lq, Lkv, tok_q0, tok_kv0, row0, delta;
-    int n_kv[2];  // key tiles tile A / tile B visits (0: no row, or no key)
+    int n_kv[2];   // walk steps tile A / tile B takes part in, up to (0: no row or key)
+    int kt0;       // kWin: first key tile of the walk (else 0)
+    int first[2];  // kWin: first walk step of tile A / B (else 0)
     bool live;    // tile A holds at least one query row
     int64_t o_row0, o_rs, lse_row0, lse_rs;
 };
@@ -109,7 +114,7 @@ struct PairUnit {
 // longest first: sequence order[i] owns units [first_unit[i], first_unit[i+1]),
 // its 256-row blocks latest first with the heads innermost, so the CTAs in
 // flight share one or two sequences' K and V in L2.
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kWin>
 SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const int *cu_kv,
                               const int *order, const int *first_unit) {
     PairUnit U;
@@ -161,22 +166,51 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
     U.row0 = qp * kPairRows;
     U.live = U.row0 < U.Lq;
     U.delta = mask_delta(p.mask, U.Lq, U.Lkv);
+    U.kt0 = 0;
+    U.first[0] = U.first[1] = 0;
+    if constexpr (!kWin) {
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-        const int r0 = U.row0 + x * kTileM;
-        int n = 0;
-        if (r0 < U.Lq) {
-            const int hi = key_range(p.mask, p.window, min(r0 + kTileM, U.Lq) - 1, U.delta, U.Lkv).hi;
-            n = hi > 0 ? (hi + kTileN - 1) / kTileN : 0;
+        for (int x = 0; x < 2; ++x) {
+            const int r0 = U.row0 + x * kTileM;
+            int n = 0;
+            if (r0 < U.Lq) {
+                const int hi = key_range(p.mask, p.window, min(r0 + kTileM, U.Lq) - 1, U.delta, U.Lkv).hi;
+                n = hi > 0 ? (hi + kTileN - 1) / kTileN : 0;
+            }
+            U.n_kv[x] = n;
         }
-        U.n_kv[x] = n;
+    } else {
+        // absolute key-tile range [f, e) of each tile: from its first row's
+        // window start to its last row's causal end
+        int f[2], e[2];
+        U.kt0 = 1 << 30;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int r0 = U.row0 + x * kTileM;
+            f[x] = e[x] = 0;
+            if (r0 < U.Lq) {
+                const int lo = max(0, key_range(p.mask, p.window, r0, U.delta, U.Lkv).lo);
+                const int hi = key_range(p.mask, p.window, min(r0 + kTileM, U.Lq) - 1, U.delta, U.Lkv).hi;
+                if (hi > lo) {
+                    f[x] = lo / kTileN;
+                    e[x] = (hi + kTileN - 1) / kTileN;
+                    U.kt0 = min(U.kt0, f[x]);
+                }
+            }
+        }
+        if (U.kt0 == (1 << 30)) U.kt0 = 0;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            U.first[x] = e[x] > f[x] ? f[x] - U.kt0 : 0;
+            U.n_kv[x] = e[x] > f[x] ? e[x] - U.kt0 : 0;
+        }
     }
     return U;
 }
 
 // kEl / kOut: input and output element kinds as in fwd.cu (E4M3 inputs with
 // device descales, P as E4M3 quads, kind::f8f6f4 products; amax of O).
-template <int D, int kEl, bool kPacked, int kOut>
+template <int D, int kEl, bool kPacked, int kOut, bool kWin>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -289,9 +323,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const WaitCtx wc{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.err, kTagFwd};
     const int first = blockIdx.x, step = gridDim.x;
     // Registers: warpgroup 0 (TMA, MMA, two idle warps) hands 64 per thread
-    // to the two softmax warpgroups: 128 x 104 + 256 x 200 = 384 x 168.
+    // to the two softmax warpgroups: 128 x 104 + 256 x 200 = 384 x 168 (the
+    // kWin walk's bookkeeping takes 48: 128 x 120 + 256 x 192).
+    constexpr uint32_t kRegsWg0 = kWin ? 120 : 104, kRegsSoftmax = kWin ? 192 : 200;
+    static_assert(128 * kRegsWg0 + 256 * kRegsSoftmax == kPairThreads * 168,
+                  "register split must hand out exactly the launch's registers");
     if (warp < 4) {
-        setmaxnreg_dec<104>();
+        setmaxnreg_dec<kRegsWg0>();
         if (warp == 0) {
             // ============================================================ producer
             if (lane == 0) {
@@ -317,7 +355,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int u = unit_of(k, first, step);
                     if (u >= n_units) break;
-                    const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
+                    const PairUnit U = decode_pair<D, kPacked, kWin>(p, u, cu_q, cu_kv, order, first_s);
                     const int nmax = max(U.n_kv[0], U.n_kv[1]);
                     if (nmax == 0) continue;
                     // the previous unit's last V goes out before waiting for Q's slot
@@ -336,8 +374,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     }
                     ++units;
                     for (int j = 0; j < nmax; ++j) {
-                        const int ky = kPacked ? U.kv_head : j * kTileN;
-                        const int kz = kPacked ? U.tok_kv0 + j * kTileN : U.kv_slice;
+                        const int kj = kWin ? U.kt0 + j : j;  // absolute key tile
+                        const int ky = kPacked ? U.kv_head : kj * kTileN;
+                        const int kz = kPacked ? U.tok_kv0 + kj * kTileN : U.kv_slice;
                         const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
                         if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
                             ok = false;
@@ -414,7 +453,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int u = unit_of(k, first, step);
                     if (u >= n_units) break;
-                    const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
+                    const PairUnit U = decode_pair<D, kPacked, kWin>(p, u, cu_q, cu_kv, order, first_s);
                     const int nmax = max(U.n_kv[0], U.n_kv[1]);
                     if (nmax == 0) continue;
                     ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) &&
@@ -422,6 +461,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         if (!ok || U.n_kv[x] == 0) continue;
+                        if constexpr (kWin) {
+                            if (U.first[x] != 0) continue;  // joins the walk later
+                        }
                         tc_fence_after();
                         issue_s(x, t % L::kKStages);
                         mma_commit(bar(L::bSFull + x));
@@ -436,17 +478,28 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         ok = mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 7);
     #pragma unroll
                         for (int x = 0; x < 2; ++x) {
-                            if (!ok || j >= U.n_kv[x]) continue;
-                            ok = mbar_wait(bar(L::bPReady + x), cnt[x] & 1, wc, 8);
-                            // the unit's first P V overwrites O_X: its previous
-                            // epilogue must have read it out
-                            if (ok && j == 0 && uo[x] > 0)
-                                ok = mbar_wait(bar(L::bOFree + x), (uo[x] - 1) & 1, wc, 9);
-                            if (!ok) continue;
-                            tc_fence_after();
-                            issue_pv(x, t % L::kVStages, j > 0);
-                            ++cnt[x];
+                            if constexpr (!kWin) {
+                                if (!ok || j >= U.n_kv[x]) continue;
+                            } else {
+                                if (!ok) continue;
+                            }
+                            // kWin: tile X takes part in steps [first, n_kv); S_X(j+1)
+                            // below also opens its walk when it joins at step j + 1
+                            if (!kWin || (j >= U.first[x] && j < U.n_kv[x])) {
+                                ok = mbar_wait(bar(L::bPReady + x), cnt[x] & 1, wc, 8);
+                                // the unit's first P V overwrites O_X: its previous
+                                // epilogue must have read it out
+                                if (ok && j == U.first[x] && uo[x] > 0)
+                                    ok = mbar_wait(bar(L::bOFree + x), (uo[x] - 1) & 1, wc, 9);
+                                if (!ok) continue;
+                                tc_fence_after();
+                                issue_pv(x, t % L::kVStages, j > U.first[x]);
+                                ++cnt[x];
+                            }
                             if (j + 1 >= U.n_kv[x]) continue;
+                            if constexpr (kWin) {
+                                if (j + 1 < U.first[x]) continue;
+                            }
                             if (!k_next) {
                                 ok = mbar_wait(bar(L::bKFull + t1 % L::kKStages), (t1 / L::kKStages) & 1,
                                                wc, 10);
@@ -469,7 +522,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     if (!ok) break;
     #pragma unroll
                     for (int x = 0; x < 2; ++x) {
-                        if (U.n_kv[x] == 0) continue;
+                        if (U.n_kv[x] == U.first[x]) continue;
                         mma_commit(bar(L::bOFull + x));
                         ++uo[x];
                     }
@@ -482,7 +535,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             __syncwarp();
         }
     } else {
-        setmaxnreg_inc<200>();
+        setmaxnreg_inc<kRegsSoftmax>();
         // ============================================================ softmax
         const int x = (warp - 4) >> 2;  // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
         const int quad = warp & 3;
@@ -501,14 +554,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int k = 0; ok; ++k) {
             const int u = unit_of(k, first, step);
             if (u >= n_units) break;
-            const PairUnit U = decode_pair<D, kPacked>(p, u, cu_q, cu_kv, order, first_s);
+            const PairUnit U = decode_pair<D, kPacked, kWin>(p, u, cu_q, cu_kv, order, first_s);
             const int row0 = U.row0 + x * kTileM;
             if (!U.live || row0 >= U.Lq) continue;  // no row of this tile
             const int q_idx = row0 + r;
             const bool row_ok = q_idx < U.Lq;
             uint8_t *orow = static_cast<uint8_t *>(p.o) + (U.o_row0 + (int64_t)q_idx * U.o_rs) * kOb;
             float *lse_ptr = p.lse ? p.lse + U.lse_row0 + (int64_t)q_idx * U.lse_rs : nullptr;
-            const int n_kv = U.n_kv[x];
+            const int n_kv = U.n_kv[x] - U.first[x];  // key tiles of this tile's walk
+            const int kt_x = U.kt0 + U.first[x];       // its first key tile
             if (n_kv == 0) {
                 // No key is visible to any row of this tile: O = 0, LSE = -inf.
                 if (row_ok) {
@@ -530,7 +584,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(t_lane + scol + c * 32, s + c * 32);
                 tmem_ld_wait_regs<kTileN>(s);
 
-                const int k0 = j * kTileN;
+                const int k0 = (kt_x + j) * kTileN;
                 // the tile needs a mask unless every row sees all of its keys
                 if ((k0 + kTileN > U.Lkv) ||
                     (p.mask != kMaskNone && k0 + kTileN - 1 > row0 + U.delta) ||
@@ -687,12 +741,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
 }
 
-template <int D, int kEl, bool kPacked, int kOut>
+template <int D, int kEl, bool kPacked, int kOut, bool kWin = false>
 cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const FwdParams &p, int grid, cudaStream_t stream,
                           const KernelTimer &timer) {
     using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2, kPacked>;
-    auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut>;
+    auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut, kWin>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);
     if (e != cudaSuccess) return e;
@@ -710,6 +764,16 @@ int fwd_pair_rows() { return kPairRows; }
 cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const FwdParams &p, int d, bool bf16, bool packed, int grid,
                             cudaStream_t stream, const KernelTimer &timer) {
+    // left windows: the walking instantiations, bf16 / fp16 at d = 128 only
+    // (the host sends every other windowed problem to the one-tile kernel)
+    if (p.window >= 0) {
+        if (d != 128) return cudaErrorInvalidValue;
+        if (bf16)
+            return packed ? launch_pair_t<128, kElBf16, true, kElBf16, true>(tq, tk, tv, p, grid, stream, timer)
+                          : launch_pair_t<128, kElBf16, false, kElBf16, true>(tq, tk, tv, p, grid, stream, timer);
+        return packed ? launch_pair_t<128, kElFp16, true, kElFp16, true>(tq, tk, tv, p, grid, stream, timer)
+                      : launch_pair_t<128, kElFp16, false, kElFp16, true>(tq, tk, tv, p, grid, stream, timer);
+    }
 #define SDPA_PAIR_CASE(D_, EL_, PK_)                                           \
     if (d == D_ && (bf16 ? kElBf16 : kElFp16) == EL_ && packed == PK_)         \
         return launch_pair_t<D_, EL_, PK_, EL_>(tq, tk, tv, p, grid, stream, timer);
@@ -728,6 +792,7 @@ cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const 
 cudaError_t launch_fwd_pair_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const FwdParams &p, int out, bool packed, int grid,
                                 cudaStream_t stream, const KernelTimer &timer) {
+    if (p.window >= 0) return cudaErrorInvalidValue;  // the host keeps windows on the one-tile kernel
 #define SDPA_PAIR_FP8_CASE(OUT_, PK_)                                          \
     if (out == OUT_ && packed == PK_)                                          \
         return launch_pair_t<128, kElE4m3, PK_, OUT_>(tq, tk, tv, p, grid, stream, timer);
