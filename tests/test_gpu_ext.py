@@ -57,6 +57,7 @@ DENSE_CASES = [
     (1, 4, 4, 333, 777, 64, "bottom_right", 200),
     (1, 2, 1, 520, 400, 128, "none", 70),              # left bound only
     (1, 8, 2, 2100, 2100, 128, "bottom_right", -1),    # long enough for the two-tile choice
+    (1, 4, 2, 640, 900, 128, "bottom_right", 300),     # band of a bottom-right window, GQA
 ]
 
 
@@ -94,6 +95,7 @@ PACKED_CASES = [
     ([300, 129, 257], [300, 129, 257], 6, 3, 128, "top_left", 100),
     ([200, 513], [450, 300], 4, 2, 64, "bottom_right", 64),
     ([70, 260], [0, 260], 2, 2, 128, "top_left", 5),                 # a sequence without keys
+    ([520, 333], [700, 333], 4, 4, 128, "bottom_right", 150),
 ]
 
 
@@ -135,7 +137,7 @@ def test_ext_packed_bwd(sdpa, case):
     _grads_ok(got, ref)
 
 
-def test_ext_fp16_gqa_window(sdpa):
+def test_ext_fp16_gqa_window(sdpa, variant):
     b, h, h_kv, s, d = 1, 4, 2, 500, 128
     q, k, v, do = sdpa_inputs.dense(b, h, s, s, d, seed=77, dtype=torch.float16, h_kv=h_kv)
     scale = 1.0 / math.sqrt(d)
@@ -239,3 +241,17 @@ def test_deterministic_packed_bwd(sdpa, case):
 def test_deterministic_workspace_is_the_row_terms(sdpa):
     assert sdpa.sdpa_bwd_ex_workspace_size(2, 3, 100, 128, 1) == 2 * 3 * 100 * 16 + 256 - (2 * 3 * 100 * 16) % 256
     assert sdpa.sdpa_bwd_ex_workspace_size(2, 3, 100, 128, 0) == sdpa.sdpa_bwd_workspace_size(2, 3, 100, 128)
+
+
+def test_ext_fp16_packed_window(sdpa, variant):
+    """fp16 packed with a left window on both forward kernels."""
+    lens, h, h_kv, d = [333, 600, 90], 4, 2, 128
+    q, k, v, do, cu, _ = sdpa_inputs.packed(lens, lens, h, d, seed=78, dtype=torch.float16,
+                                           h_kv=h_kv)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = sdpa.attention_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), cu.cuda(), max(lens),
+                                   max(lens), scale=scale, causal=True, window_left=130)
+    torch.cuda.synchronize()
+    ro, rlse = oracle.sdpa_varlen_fwd_ex(q, k, v, cu, cu, scale, "top_left", 130)
+    check_rel(o, ro, O_TOL[torch.float16], "o")
+    check_lse(lse, rlse)
