@@ -92,3 +92,39 @@ def test_workspace_sizes(lib):
     assert ws >= 2 * 3 * 100 * (128 + 1) * 4 and ws % 256 == 0
     assert L.sdpa_varlen_bwd_workspace_size(200, 3, 128) == ws
     assert L.sdpa_bwd_workspace_size(1, 1, 1, 96) == ctypes.c_size_t(-1).value
+
+
+def test_extended_validation_before_any_cuda_call(lib):
+    """The extended, FP8 and self-test entry points reject bad arguments on
+    the host, before any CUDA call (so this runs without a GPU)."""
+    from scaled_dot_product_04_gb300 import _lib as L
+
+    def fwd_ex(h=4, h_kv=2, mask=1, window=-1, d=64, dtype=0, b=1):
+        return lib.sdpa_fwd_ex(0x10000, 0x20000, 0x30000, 0x40000, None, b, h, h_kv, 128, 128, d,
+                               0.125, mask, window, dtype, None)
+
+    assert fwd_ex(h_kv=3) == L.SDPA_ERR_INVALID_ARG
+    assert "multiple of h_kv" in L.sdpa_last_error()
+    assert fwd_ex(h_kv=0) == L.SDPA_ERR_INVALID_ARG
+    assert fwd_ex(mask=3) == L.SDPA_ERR_INVALID_ARG
+    assert fwd_ex(window=-2) == L.SDPA_ERR_INVALID_ARG
+    assert fwd_ex(d=96) == L.SDPA_ERR_UNSUPPORTED
+    assert fwd_ex(b=0) == L.SDPA_OK  # empty: nothing launched
+
+    def fwd8(d=128, out=0, dq=0x70000, dk=0x70010, dv=0x70020, so=None, scale=0.088):
+        return lib.sdpa_fwd_fp8(0x10000, 0x20000, 0x30000, 0x40000, None, dq, dk, dv, so, None,
+                                1, 2, 2, 128, 128, d, scale, 1, -1, out, None)
+
+    assert fwd8(d=64) == L.SDPA_ERR_UNSUPPORTED
+    assert fwd8(out=5) == L.SDPA_ERR_UNSUPPORTED
+    assert fwd8(dk=None) == L.SDPA_ERR_INVALID_ARG
+    assert fwd8(out=L.SDPA_FP8_E4M3) == L.SDPA_ERR_INVALID_ARG  # needs scale_o
+    assert "scale_o" in L.sdpa_last_error()
+    assert fwd8(scale=float("inf")) == L.SDPA_ERR_INVALID_ARG
+
+    assert lib.sdpa_bwd_ex_workspace_size(1, 4, 128, 128, 2) == ctypes.c_size_t(-1).value
+    assert lib.sdpa_selftest_wait_timeout(0, None) == L.SDPA_ERR_INVALID_ARG
+    assert lib.sdpa_selftest_wait_timeout(2000001, None) == L.SDPA_ERR_INVALID_ARG
+    assert "limit_us" in L.sdpa_last_error()
+    assert lib.sdpa_set_forward_variant(3) == L.SDPA_ERR_INVALID_ARG
+    assert lib.sdpa_set_forward_variant(0) == L.SDPA_OK
