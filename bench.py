@@ -58,10 +58,11 @@ REF_PREFIX = 2048         # tokens of one head per oracle sample
 # reports null.  Source: profiles/bwd_main_dram_c5_b1h32s16384d128.md.
 TRAFFIC = {("bwd_main", "sdpa_gb300 0.4 sm_103a"): 0.81430e9 + 0.49046e9,
            ("bwd_main", "sdpa_gb300 0.6 sm_103a"): 0.83157e9 + 0.50512e9,
-           # bwd.cu is unchanged from 0.6 to 0.9 (only the forwards changed)
+           # bwd.cu is unchanged from 0.6 to 0.10 (only the forwards changed)
            ("bwd_main", "sdpa_gb300 0.7 sm_103a"): 0.83157e9 + 0.50512e9,
            ("bwd_main", "sdpa_gb300 0.8 sm_103a"): 0.83157e9 + 0.50512e9,
-           ("bwd_main", "sdpa_gb300 0.9 sm_103a"): 0.83157e9 + 0.50512e9}
+           ("bwd_main", "sdpa_gb300 0.9 sm_103a"): 0.83157e9 + 0.50512e9,
+           ("bwd_main", "sdpa_gb300 0.10 sm_103a"): 0.83157e9 + 0.50512e9}
 
 
 def fwd_flops(w) -> float:

@@ -349,10 +349,10 @@ void sdpa_set_kernel_timer(void *start_event, void *stop_event);
  * Forward kernel choice for later calls on this host thread (a tuning and
  * testing hook; no counterpart on the pages).  0 (default): automatic -- the
  * two-tile kernel (256 query rows per work unit, two softmax warpgroups
- * ping-ponging on the tensor core) for d = 128 problems whose query and key
- * lengths reach 2048 (dense) or whose mean sequence lengths total_q / num_seqs
- * and total_kv / num_seqs reach 4096 (packed), the one-tile kernel (128 rows
- * per unit) otherwise; FP8 inputs with a left window, and 16-bit inputs with a
+ * ping-ponging on the tensor core) for problems whose query and key lengths
+ * reach 1024 (dense) or whose mean sequence lengths total_q / num_seqs and
+ * total_kv / num_seqs reach 2048 (packed), the one-tile kernel (128 rows per
+ * unit) otherwise; FP8 inputs with a left window, and 16-bit inputs with a
  * left window at d = 64, always take the one-tile kernel.  1: always one-tile.
  * 2: the two-tile kernel wherever it applies.  Both compute the same result to
  * rounding.
@@ -360,7 +360,7 @@ void sdpa_set_kernel_timer(void *start_event, void *stop_event);
  */
 int sdpa_set_forward_variant(int variant);
 
-/* Library version string, e.g. "sdpa_gb300 0.9 sm_103a"; the
+/* Library version string, e.g. "sdpa_gb300 0.10 sm_103a"; the
  * minor number changes whenever a kernel changes. */
 const char *sdpa_version(void);
 

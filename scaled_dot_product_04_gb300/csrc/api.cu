@@ -33,15 +33,16 @@ thread_local int t_fwd_variant = 0;  // 0 auto, 1 one-tile, 2 two-tile
 constexpr size_t kSliceMajorKVBytes = size_t(64) << 20;
 
 // Forward kernel choice.  The two-tile kernel (256 query rows per unit, two
-// softmax warpgroups) wins when every unit visits many key tiles; short
+// softmax warpgroups) wins once units visit a few key tiles: at d = 64 and 128
+// from 1024 rows on (dense) and from a mean of 2048 tokens per sequence
+// (packed, whose lists also hold short sequences that fill only tile A); short
 // problems do better with the one-tile kernel's 128-row units.  rows_*: the
-// dense lengths, or the packed totals over the sequence count (the mean
-// length, which must be longer: a packed list also holds short sequences).
+// dense lengths, or the packed totals over the sequence count.
 bool use_pair_kernel(bool packed, int d, int64_t rows_q, int64_t rows_kv) {
     if (t_fwd_variant == 1) return false;
     if (t_fwd_variant == 2) return true;
-    const int64_t min_rows = packed ? 4096 : 2048;
-    return d == 128 && rows_q >= min_rows && rows_kv >= min_rows;
+    const int64_t min_rows = packed ? 2048 : 1024;
+    return (d == 64 || d == 128) && rows_q >= min_rows && rows_kv >= min_rows;
 }
 
 int fail(int status, const char *fmt, ...) {
@@ -278,7 +279,7 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.9 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.10 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)

@@ -369,11 +369,11 @@ def test_slice_major_packed_one_tile(sdpa, d, n, lo, hi):
 
 
 def test_packed_long_sequences_two_tile(sdpa):
-    """A packed problem whose mean sequence length reaches 4096 runs the
+    """A packed problem whose mean sequence length reaches 2048 runs the
     two-tile kernel by default (longest sequence first); sampled rows against
     the oracle, and the same bits as the two-tile kernel forced."""
-    lens, h, d = [4200, 4500, 3000, 5000, 100], 4, 128
-    assert sum(lens) // len(lens) < 4096  # the short one keeps the mean below: one-tile
+    lens, h, d = [2100, 2500, 3000, 5000, 100, 90, 80], 4, 128
+    assert sum(lens) // len(lens) < 2048 <= sum(lens[:4]) // 4  # one-tile, then two-tile
     for ls in (lens, lens[:4]):
         q, k, v, _, cu, _ = sdpa_inputs.packed(ls, ls, h, d, seed=71 + len(ls))
         args = (q.cuda(), k.cuda(), v.cuda(), cu.cuda(), cu.cuda(), max(ls), max(ls))
