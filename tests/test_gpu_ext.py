@@ -58,6 +58,7 @@ DENSE_CASES = [
     (1, 2, 1, 520, 400, 128, "none", 70),              # left bound only
     (1, 8, 2, 2100, 2100, 128, "bottom_right", -1),    # long enough for the two-tile choice
     (1, 4, 2, 640, 900, 128, "bottom_right", 300),     # band of a bottom-right window, GQA
+    (1, 4, 2, 900, 350, 128, "bottom_right", 100),     # s_q > s_kv: keyless leading tiles
 ]
 
 
