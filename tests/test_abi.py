@@ -128,3 +128,31 @@ def test_extended_validation_before_any_cuda_call(lib):
     assert "limit_us" in L.sdpa_last_error()
     assert lib.sdpa_set_forward_variant(3) == L.SDPA_ERR_INVALID_ARG
     assert lib.sdpa_set_forward_variant(0) == L.SDPA_OK
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: pointing the binding at a library that does not exist raises
+    (in a fresh process, since this one may have loaded the real one)."""
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from scaled_dot_product_04_gb300 import _lib\n"
+            "try:\n"
+            "    _lib.load(%r)\n"
+            "except ImportError as e:\n"
+            "    print('raised:', e)\n"
+            "    sys.exit(0)\n"
+            "sys.exit(1)\n") % (ROOT, str(tmp_path / "absent.so"))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "not found" in r.stdout, r.stdout + r.stderr
+
+
+def test_product_package_never_uses_the_oracle():
+    """The package (binding, wrappers, build step) imports neither the oracle
+    nor the test input generators: every step of the path runs in the CUDA
+    library."""
+    pkg = os.path.join(ROOT, "scaled_dot_product_04_gb300")
+    for name in os.listdir(pkg):
+        if name.endswith(".py"):
+            text = open(os.path.join(pkg, name)).read()
+            assert not re.search(r"^\s*(import|from)\s+(oracle|sdpa_inputs)\b", text, flags=re.M), name
