@@ -42,6 +42,9 @@ namespace {
 
 constexpr int kPairThreads = 384;
 constexpr int kPairRows = 2 * kTileM;  // query rows per work unit
+// registers per thread the kernel is launched with (the most 384 threads may
+// have); the setmaxnreg split below hands out exactly kPairThreads x this
+constexpr int kPairLaunchRegs = 168;
 
 // kEb: bytes per input element (2 for bf16/fp16, 1 for E4M3).  kPk: packed
 // inputs, whose cu_seqlens cache also holds the sequence table of the unit
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // to the two softmax warpgroups: 128 x 104 + 256 x 200 = 384 x 168 (the
     // kWin walk's bookkeeping takes 48: 128 x 120 + 256 x 192).
     constexpr uint32_t kRegsWg0 = kWin ? 120 : 104, kRegsSoftmax = kWin ? 192 : 200;
-    static_assert(128 * kRegsWg0 + 256 * kRegsSoftmax == kPairThreads * 168,
+    static_assert(128 * kRegsWg0 + 256 * kRegsSoftmax == kPairThreads * kPairLaunchRegs,
                   "register split must hand out exactly the launch's registers");
     if (warp < 4) {
         setmaxnreg_dec<kRegsWg0>();
@@ -747,6 +750,14 @@ cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CU
                           const KernelTimer &timer) {
     using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2, kPacked>;
     auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut, kWin>;
+    // The softmax warpgroups' setmaxnreg.inc waits for the registers warpgroup
+    // 0 releases; a build launched with any other per-thread count than the
+    // split assumes would leave it waiting, so such a build is not launched.
+    static const int launch_regs = [&] {
+        cudaFuncAttributes fa{};
+        return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : -1;
+    }();
+    if (launch_regs != kPairLaunchRegs) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);
     if (e != cudaSuccess) return e;
