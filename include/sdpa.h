@@ -228,6 +228,13 @@ size_t sdpa_varlen_bwd_workspace_size(int total_q, int h, int d);
  * Packed (THD) backward.  Arguments as sdpa_varlen_fwd, plus o, dout
  * [total_q,h,d], lse [total_q,h] fp32 from that forward, outputs dq
  * [total_q,h,d], dk, dv [total_kv,h,d] and the workspace.
+ * It is the backward of the packed path of cudnn-frontend PR #554 ("THD /
+ * varlen" notes): the gradients keep the packed layouts of q, k and v, the
+ * token-major statistics of the forward are read as they are (no repadding
+ * into a dense layout), and nothing is read back to the host -- the PR's fix
+ * "drop the 2*B D2H syncs from the varlen backward" is why the totals and
+ * maximum lengths are host arguments here too.  Sequences are independent:
+ * dK, dV of sequence n take contributions of its own queries only.
  */
 int sdpa_varlen_bwd(const void *q, const void *k, const void *v, const void *o,
                     const void *dout, const float *lse, void *dq, void *dk,
@@ -295,8 +302,11 @@ int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v,
  * to 63,550 rows of b*h*s_q at d = 128) are rejected with
  * SDPA_ERR_WORKSPACE before anything is launched.
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *    that first call before any stream capture.  The kept address belongs
+ *    to the device's context, so after a cudaDeviceReset of a device (which
+ *    ends that context) do not call this entry point on it again in the
+ *    same process.
  *  - All calls share the one array, so calls whose work can overlap on the
  *    GPU (other streams, other host threads) race on it and give wrong
  *    gradients; serialise them.  Each call rewrites the part of the array it
@@ -309,8 +319,15 @@ int sdpa_bwd_noalloc(const void *q, const void *k, const void *v,
                      int s_kv, int d, float attn_scale, int causal, int dtype,
                      sdpa_stream_t stream);
 
-/* Message describing the last non-OK status returned on this host thread
- * ("" if none).  The pointer stays valid until the next call on the thread. */
+/*
+ * Message describing the last non-OK status returned on this host thread
+ * ("" if none).  The pointer stays valid until the next call on the thread.
+ * TransformerEngine PR #2964 moves its C API from a bare "no backend" code
+ * to a status plus the real error text (its probe functions return an empty
+ * string or the message, and the backend query returns the pair); every
+ * entry point here follows that convention: a non-zero sdpa_status, and this
+ * call for the text naming the argument or CUDA call that failed.
+ */
 const char *sdpa_last_error(void);
 
 /*
@@ -318,7 +335,12 @@ const char *sdpa_last_error(void);
  * kernels that give up on a bounded wait (about two seconds) record the
  * failure there instead of hanging.  Synchronises `stream` first.  Returns
  * SDPA_OK, SDPA_ERR_TIMEOUT (message says which kernel and which wait) or
- * SDPA_ERR_CUDA.
+ * SDPA_ERR_CUDA.  It reports device-side failures in the same status-plus-
+ * message form as sdpa_last_error (TransformerEngine PR #2964's C-API error
+ * message); it is the one call that synchronises, so the launching calls
+ * keep cudnn-frontend PR #554's "no host sync" rule and a caller checks
+ * when it chooses (the debug-build device check of the pages' descriptor
+ * contract).
  */
 int sdpa_check_device_error(sdpa_stream_t stream);
 

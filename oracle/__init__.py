@@ -51,12 +51,8 @@ def _load():
         if _lib is not None:
             return _lib
         lib = ctypes.CDLL(build())
-        lib.oracle_attn_fwd.argtypes = [_dp, _i64, _dp, _i64, _dp, _i64, _dp, _i64, _dp, _i64,
-                                        _int, _int, _int, _dbl, _int]
         lib.oracle_attn_fwd_rows.argtypes = [_dp, _i64, _dp, _i64, _dp, _i64, _dp, _dp,
                                              _int, _int, _int, _dbl, _int, _ip, _int]
-        lib.oracle_attn_bwd.argtypes = [_dp, _i64, _dp, _i64, _dp, _i64, _dp, _i64, _dp, _i64,
-                                        _dp, _i64, _dp, _i64, _int, _int, _int, _dbl, _int]
         lib.oracle_attn_bwd_rows.argtypes = [_dp, _i64, _dp, _i64, _dp, _i64, _dp, _i64,
                                              _dp, _dp, _dp, _int, _int, _int, _dbl, _int,
                                              _ip, _int, _ip, _int]

@@ -219,16 +219,6 @@ static void bwd_problem(const double *q, int64_t q_rs, const double *k, int64_t 
 /* Mask of the entry points that take a `causal` flag: top-left or none. */
 static int causal_mask(int causal) { return causal ? MASK_TOP_LEFT : MASK_NONE; }
 
-/* One problem, explicit row strides (elements). */
-void oracle_attn_fwd(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
-                     const double *v, int64_t v_rs, double *o, int64_t o_rs,
-                     double *lse, int64_t lse_rs, int n_q, int n_kv, int d,
-                     double scale, int causal)
-{
-    fwd_problem(q, q_rs, k, k_rs, v, v_rs, o, o_rs, lse, lse_rs, n_q, n_kv, d,
-                scale, causal_mask(causal), -1, NULL, 0);
-}
-
 /* Selected rows of one problem; outputs packed [n_rows, d] and [n_rows].
  * mask: 0 none, 1 causal top-left, 2 causal bottom-right; window_left < 0
  * means no left bound. */
@@ -248,16 +238,6 @@ void oracle_attn_fwd_rows(const double *q, int64_t q_rs, const double *k, int64_
 {
     oracle_attn_fwd_rows_ex(q, q_rs, k, k_rs, v, v_rs, o, lse, n_q, n_kv, d, scale,
                             causal_mask(causal), -1, rows, n_rows);
-}
-
-void oracle_attn_bwd(const double *q, int64_t q_rs, const double *k, int64_t k_rs,
-                     const double *v, int64_t v_rs, const double *dout, int64_t do_rs,
-                     double *dq, int64_t dq_rs, double *dk, int64_t dk_rs,
-                     double *dv, int64_t dv_rs, int n_q, int n_kv, int d,
-                     double scale, int causal)
-{
-    bwd_problem(q, q_rs, k, k_rs, v, v_rs, dout, do_rs, dq, dq_rs, dk, dk_rs, dv,
-                dv_rs, n_q, n_kv, d, scale, causal_mask(causal), -1, NULL, 0, NULL, 0);
 }
 
 /* Selected dQ rows and dK/dV rows of one problem; outputs packed. */

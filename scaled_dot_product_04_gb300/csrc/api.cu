@@ -265,6 +265,26 @@ int launch_status(cudaError_t e, const char *what) {
     return fail(SDPA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
 }
 
+// Runs a forward on the chosen kernel: launch(true) starts the two-tile kernel,
+// launch(false) the one-tile kernel, each with its own unit count and grid.
+// A two-tile build refused for its register split (fwd_pair_refused_regs) is
+// replaced by the one-tile kernel under the automatic choice; an explicit
+// two-tile request reports the mismatch instead.
+template <class Launch>
+int run_forward(bool pair, Launch &&launch, const char *what) {
+    if (!pair) return launch_status(launch(false), what);
+    const cudaError_t e = launch(true);
+    const int refused = fwd_pair_refused_regs();
+    if (e == cudaErrorInvalidConfiguration && refused != 0) {
+        if (t_fwd_variant == 0) return launch_status(launch(false), what);
+        return fail(SDPA_ERR_UNSUPPORTED,
+                    "%s: the two-tile forward kernel was built with %d registers per thread, but "
+                    "its register split hands out exactly %d, so it is not launched",
+                    what, refused, fwd_pair_split_regs());
+    }
+    return launch_status(e, what);
+}
+
 }  // namespace
 
 // Lets other translation units of the library set the message that
@@ -333,8 +353,7 @@ int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     if (bh == 0 || s_q == 0) return ok();
     // left windows take the two-tile kernel at d = 128 only (its walking instantiations)
     const bool pair = use_pair_kernel(false, d, s_q, s_kv) && (window_left < 0 || d == 128);
-    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
-    const int64_t q_tiles = (s_q + unit_rows - 1) / unit_rows;
+    const int64_t q_tiles = (s_q + kTileM - 1) / kTileM;  // 128-row units: the most units
     if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
     const size_t qbytes = (size_t)bh * s_q * d * 2, kvbytes = (size_t)bh_kv * s_kv * d * 2;
@@ -359,17 +378,20 @@ int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     p.group = h / h_kv;
     p.s_q = s_q;
     p.s_kv = s_kv;
-    p.q_tiles = (int)q_tiles;
-    p.n_units = (int)(q_tiles * bh);
     const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
-    const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer)
-                              : launch_fwd(tq, tk, tv, p, d, bf16, false, grid, slice_major, cs, t_timer),
-                         "sdpa_fwd");
+    auto launch = [&](bool two) {
+        const int rows = two ? fwd_pair_rows() : kTileM;
+        p.q_tiles = (s_q + rows - 1) / rows;
+        p.n_units = (int)(p.q_tiles * bh);
+        const int grid = std::min(p.n_units, dev->sm_count);
+        return two ? launch_fwd_pair(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer)
+                   : launch_fwd(tq, tk, tv, p, d, bf16, false, grid, slice_major, cs, t_timer);
+    };
+    return run_forward(pair, launch, "sdpa_fwd");
 }
 
 int sdpa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int b, int h,
@@ -415,8 +437,7 @@ int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o, flo
     const bool pair = use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
                                       (int64_t)total_kv / num_seqs) &&
                       (window_left < 0 || d == 128);
-    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
-    const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
+    const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;  // 128-row units: the most
     const int64_t slices = (int64_t)num_seqs * h;
     if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
@@ -445,17 +466,20 @@ int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o, flo
     p.h_kv = h_kv;
     p.group = h / h_kv;
     p.num_seqs = num_seqs;
-    p.q_tiles = (int)q_tiles;
-    p.n_units = (int)(q_tiles * slices);
     const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
     p.scale_log2 = attn_scale * kLog2e;
-    const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    return launch_status(pair ? launch_fwd_pair(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer)
-                              : launch_fwd(tq, tk, tv, p, d, bf16, true, grid, slice_major, cs, t_timer),
-                         "sdpa_varlen_fwd");
+    auto launch = [&](bool two) {
+        const int rows = two ? fwd_pair_rows() : kTileM;
+        p.q_tiles = (max_seqlen_q + rows - 1) / rows;
+        p.n_units = (int)(p.q_tiles * slices);
+        const int grid = std::min(p.n_units, dev->sm_count);
+        return two ? launch_fwd_pair(tq, tk, tv, p, d, bf16, true, grid, cs, t_timer)
+                   : launch_fwd(tq, tk, tv, p, d, bf16, true, grid, slice_major, cs, t_timer);
+    };
+    return run_forward(pair, launch, "sdpa_varlen_fwd");
 }
 
 int sdpa_varlen_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -498,8 +522,7 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     if (bh == 0 || s_q == 0) return ok();
     // FP8 with a left window runs the one-tile kernel
     const bool pair = window_left < 0 && use_pair_kernel(false, d, s_q, s_kv);
-    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
-    const int64_t q_tiles = (s_q + unit_rows - 1) / unit_rows;
+    const int64_t q_tiles = (s_q + kTileM - 1) / kTileM;  // 128-row units: the most units
     if (bh > INT32_MAX || q_tiles * bh > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
     const size_t ob = out_dtype == SDPA_FP8_E4M3 ? 1 : 2;
@@ -527,8 +550,6 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     p.group = h / h_kv;
     p.s_q = s_q;
     p.s_kv = s_kv;
-    p.q_tiles = (int)q_tiles;
-    p.n_units = (int)(q_tiles * bh);
     const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
@@ -538,13 +559,18 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     p.descale_v = descale_v;
     p.scale_o = scale_o;
     p.amax_o = amax_o;
-    const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
-    return launch_status(pair ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer)
-                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, slice_major, cs, t_timer),
-                         "sdpa_fwd_fp8");
+    auto launch = [&](bool two) {
+        const int rows = two ? fwd_pair_rows() : kTileM;
+        p.q_tiles = (s_q + rows - 1) / rows;
+        p.n_units = (int)(p.q_tiles * bh);
+        const int grid = std::min(p.n_units, dev->sm_count);
+        return two ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer)
+                   : launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, slice_major, cs, t_timer);
+    };
+    return run_forward(pair, launch, "sdpa_fwd_fp8");
 }
 
 int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -563,8 +589,7 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
     const bool pair = window_left < 0 && use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
                                                          (int64_t)total_kv / num_seqs);
-    const int unit_rows = pair ? fwd_pair_rows() : kTileM;
-    const int64_t q_tiles = (max_seqlen_q + unit_rows - 1) / unit_rows;
+    const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;  // 128-row units: the most
     const int64_t slices = (int64_t)num_seqs * h;
     if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)
         return fail(SDPA_ERR_INVALID_ARG, "problem too large for one launch");
@@ -596,8 +621,6 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
     p.h_kv = h_kv;
     p.group = h / h_kv;
     p.num_seqs = num_seqs;
-    p.q_tiles = (int)q_tiles;
-    p.n_units = (int)(q_tiles * slices);
     const bool slice_major = 2 * kvbytes > kSliceMajorKVBytes;
     p.mask = mask;
     p.window = window_left;
@@ -607,13 +630,18 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
     p.descale_v = descale_v;
     p.scale_o = scale_o;
     p.amax_o = amax_o;
-    const int grid = std::min(p.n_units, dev->sm_count);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (amax_o && cudaMemsetAsync(amax_o, 0, 4, cs) != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "clearing amax_o failed");
-    return launch_status(pair ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer)
-                              : launch_fwd_fp8(tq, tk, tv, p, out_dtype, true, grid, slice_major, cs, t_timer),
-                         "sdpa_varlen_fwd_fp8");
+    auto launch = [&](bool two) {
+        const int rows = two ? fwd_pair_rows() : kTileM;
+        p.q_tiles = (max_seqlen_q + rows - 1) / rows;
+        p.n_units = (int)(p.q_tiles * slices);
+        const int grid = std::min(p.n_units, dev->sm_count);
+        return two ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, true, grid, cs, t_timer)
+                   : launch_fwd_fp8(tq, tk, tv, p, out_dtype, true, grid, slice_major, cs, t_timer);
+    };
+    return run_forward(pair, launch, "sdpa_varlen_fwd_fp8");
 }
 
 static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }

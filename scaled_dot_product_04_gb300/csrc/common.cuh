@@ -114,6 +114,13 @@ struct KernelTimer {
 // Two-tile forward (fwd_pair.cu): 256 query rows per unit; q_tiles / n_units
 // then count 256-row blocks.
 int fwd_pair_rows();
+// The two-tile kernel's setmaxnreg split hands out exactly fwd_pair_split_regs()
+// registers per launched thread.  A build whose launch register count differs
+// is not launched: launch_fwd_pair* then return cudaErrorInvalidConfiguration
+// and fwd_pair_refused_regs() gives that build's count (0 after any launch
+// attempt that was not refused for this reason, on this host thread).
+int fwd_pair_split_regs();
+int fwd_pair_refused_regs();
 cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const FwdParams &p, int d, bool bf16, bool packed, int grid,
                             cudaStream_t stream, const KernelTimer &timer);

@@ -34,6 +34,8 @@
 // has read P_X before the later one writes S_X (the same ordering every
 // chained accumulation relies on).  When the softmax sees S_X(j+1) complete,
 // O_X therefore holds every earlier product and may be rescaled at once.
+#include <atomic>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -744,6 +746,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
 }
 
+// launch register count of the last build launch_pair_t refused on this thread
+thread_local int t_refused_regs = 0;
+
 template <int D, int kEl, bool kPacked, int kOut, bool kWin = false>
 cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const FwdParams &p, int grid, cudaStream_t stream,
@@ -753,11 +758,22 @@ cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CU
     // The softmax warpgroups' setmaxnreg.inc waits for the registers warpgroup
     // 0 releases; a build launched with any other per-thread count than the
     // split assumes would leave it waiting, so such a build is not launched.
-    static const int launch_regs = [&] {
+    // The count is read once per instantiation; a failed query is passed on
+    // (a missing kernel image stays "unsupported") and asked again next time.
+    static std::atomic<int> launch_regs{0};  // 0: not read yet
+    t_refused_regs = 0;
+    int regs = launch_regs.load(std::memory_order_relaxed);
+    if (regs == 0) {
         cudaFuncAttributes fa{};
-        return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : -1;
-    }();
-    if (launch_regs != kPairLaunchRegs) return cudaErrorInvalidConfiguration;
+        const cudaError_t q = cudaFuncGetAttributes(&fa, kern);
+        if (q != cudaSuccess) return q;
+        regs = fa.numRegs;
+        launch_regs.store(regs, std::memory_order_relaxed);
+    }
+    if (regs != kPairLaunchRegs) {
+        t_refused_regs = regs;
+        return cudaErrorInvalidConfiguration;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);
     if (e != cudaSuccess) return e;
@@ -771,6 +787,8 @@ cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CU
 }  // namespace
 
 int fwd_pair_rows() { return kPairRows; }
+int fwd_pair_split_regs() { return kPairLaunchRegs; }
+int fwd_pair_refused_regs() { return t_refused_regs; }
 
 cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const FwdParams &p, int d, bool bf16, bool packed, int grid,

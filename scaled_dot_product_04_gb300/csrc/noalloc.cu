@@ -12,7 +12,10 @@
 // the library holds it (kNoAllocScratchBytes) until the process exits.
 // Host code cannot use the symbol's name as a device address: the device
 // address is fetched once per device with cudaGetSymbolAddress, with that
-// device current, and passed to the kernels.
+// device current, and passed to the kernels.  The address belongs to the
+// device's context: a cudaDeviceReset destroys that context, and the kept
+// address would then name memory of a context that no longer exists, so a
+// process that resets a device must not call this entry point on it again.
 #include <cstdio>
 #include <mutex>
 
@@ -41,7 +44,7 @@ extern "C" int sdpa_bwd_noalloc(const void *q, const void *k, const void *v, con
                                 const void *dout, const float *lse, void *dq, void *dk, void *dv,
                                 int b, int h, int s_q, int s_kv, int d, float attn_scale,
                                 int causal, int dtype, sdpa_stream_t stream) {
-    char msg[256];
+    char msg[512];
     const size_t need = sdpa_bwd_workspace_size(b, h, s_q, d);
     if (need == (size_t)-1)  // invalid sizes: let sdpa_bwd report them
         return sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, b, h, s_q, s_kv, d, attn_scale,
@@ -49,16 +52,24 @@ extern "C" int sdpa_bwd_noalloc(const void *q, const void *k, const void *v, con
     if (need > kNoAllocScratchBytes) {
         snprintf(msg, sizeof(msg),
                  "sdpa_bwd_noalloc: this problem needs %zu bytes of scratch but the built-in "
-                 "array holds %zu (about b*h*s_q*(d+1)*4 must fit); use sdpa_bwd with a workspace",
+                 "array holds %zu (b*h*s_q*d*4 for the dQ accumulator plus b*h*s_q*16 for the "
+                 "row terms, each rounded up to 256 bytes, must fit); use sdpa_bwd with a "
+                 "workspace",
                  need, kNoAllocScratchBytes);
         return sdpa::report_error(SDPA_ERR_WORKSPACE, msg);
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    if (e != cudaSuccess) {
         snprintf(msg, sizeof(msg), "sdpa_bwd_noalloc: cudaGetDevice failed (%s)",
                  cudaGetErrorString(e));
         return sdpa::report_error(SDPA_ERR_CUDA, msg);
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        snprintf(msg, sizeof(msg),
+                 "sdpa_bwd_noalloc: device index %d is outside the %d devices this library "
+                 "keeps a scratch address for", dev, kMaxDevices);
+        return sdpa::report_error(SDPA_ERR_UNSUPPORTED, msg);
     }
     void *scratch = nullptr;
     {

@@ -1,19 +1,22 @@
-"""Full-size parity of the two other timed configurations, on sampled rows.
+"""Full-size parity of the other timed configurations of the long workload.
 
 The long causal workload (b1 h32 s16384 d128, Q and K doubled) run exactly as
 the benchmark's variants launch it:
-- the backward with its deterministic dQ pass: sampled dQ/dK/dV rows against
-  the fp64 oracle (tolerance 2e-2 of max|ref| per tensor), and a bit-identical
-  rerun;
-- the FP8 (E4M3) forward with per-tensor descales and bf16 output: sampled O
-  rows within the derived bound 2^-4 max|V| + 2^-8 max|O_ref| of the oracle on
-  the decoded inputs, LSE within 1e-3.
+- the backward with its deterministic dQ pass: whole heads 0, 3, 4 and 31 of
+  dQ/dK/dV against the fp64 oracle (tolerance 2e-2 of max|ref| per tensor),
+  and a bit-identical rerun;
+- the FP8 (E4M3) forward with per-tensor descales and bf16 output: whole heads
+  0, 16 and 31 of O within the derived bound 2^-4 max|V| + 2^-8 max|O_ref| of
+  the oracle on the decoded inputs, LSE within 1e-3;
+- the extended-call rows: whole heads under the left window and the
+  bottom-right mask, sampled rows of one key/value head group for GQA.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
+import oracle_refs
 import sdpa_inputs
 from helpers import GRAD_TOL, check_lse, check_rel, np64
 
@@ -36,9 +39,9 @@ def _rows(n, seed):
     return np.array(sorted(r for r in base if 0 <= r < n), np.int32)
 
 
-def test_full_size_deterministic_bwd_sampled_and_bitwise(sdpa):
+def test_full_size_deterministic_bwd_whole_heads_and_bitwise(sdpa):
     w = sdpa_inputs.WORKLOADS[NAME]
-    t = sdpa_inputs.make(w)
+    t = oracle_refs.inputs(NAME)
     q, k, v, do = (t[x].cuda() for x in ("q", "k", "v", "do"))
     o, lse = sdpa.attention(q, k, v, scale=w.scale, causal=True)
     ws = torch.empty(sdpa.sdpa_bwd_ex_workspace_size(w.b, w.h, w.s, w.d, 1), dtype=torch.uint8,
@@ -52,18 +55,15 @@ def test_full_size_deterministic_bwd_sampled_and_bitwise(sdpa):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{name} differs on rerun"
     dq, dk, dv = (x.cpu() for x in g1)
     del g1, g2
-    for hh in (0, w.h - 1):
-        qr, kr = _rows(w.s, hh), _rows(w.s, hh + 1)
-        r_dq, r_dk, r_dv = oracle.attn_bwd_rows(t["q"][0, hh], t["k"][0, hh], t["v"][0, hh],
-                                                t["do"][0, hh], qr, kr, w.scale, True)
-        check_rel(dq[0, hh][qr], r_dq, GRAD_TOL, f"dq[{hh}]")
-        check_rel(dk[0, hh][kr], r_dk, GRAD_TOL, f"dk[{hh}]")
-        check_rel(dv[0, hh][kr], r_dv, GRAD_TOL, f"dv[{hh}]")
+    for hh in (0, 3, 4, w.h - 1):
+        r = oracle_refs.dense_slice(NAME, 0, hh, True)
+        for g, rr, nm in zip((dq, dk, dv), r[2:], ("dq", "dk", "dv")):
+            check_rel(g[0, hh], rr, GRAD_TOL, f"{nm}[{hh}]")
 
 
-def test_full_size_fp8_fwd_sampled(sdpa):
+def test_full_size_fp8_fwd_whole_heads(sdpa):
     w = sdpa_inputs.WORKLOADS[NAME]
-    t = sdpa_inputs.make(w)
+    t = oracle_refs.inputs(NAME)
     enc = [sdpa_inputs.fp8_quantize(t[x].float()) for x in ("q", "k", "v")]
     (qc, dsq), (kc, dsk), (vc, dsv) = enc
     ds = [torch.tensor([x], dtype=torch.float32, device="cuda") for x in (dsq, dsk, dsv)]
@@ -73,15 +73,14 @@ def test_full_size_fp8_fwd_sampled(sdpa):
     o, lse = o.cpu(), lse.cpu()
     assert torch.isfinite(o.float()).all()
     for hh in (0, w.h // 2, w.h - 1):
-        rows = _rows(w.s, 50 + hh)
-        qd = oracle.e4m3_to_f64(qc[0, hh], dsq)
-        kd = oracle.e4m3_to_f64(kc[0, hh], dsk)
-        vd = oracle.e4m3_to_f64(vc[0, hh], dsv)
-        ro, rlse = oracle.attn_fwd_rows_ex(qd, kd, vd, rows, w.scale, "top_left", -1)
-        err = float(np.abs(np64(o[0, hh][rows]) - ro).max())
+        qd = oracle.e4m3_to_f64(qc[0:1, hh:hh + 1], dsq)
+        kd = oracle.e4m3_to_f64(kc[0:1, hh:hh + 1], dsk)
+        vd = oracle.e4m3_to_f64(vc[0:1, hh:hh + 1], dsv)
+        ro, rlse = oracle.sdpa_fwd(qd, kd, vd, w.scale, True)
+        err = float(np.abs(np64(o[0, hh]) - ro[0, 0]).max())
         bound = 2.0 ** -4 * float(np.abs(vd).max()) + 2.0 ** -8 * float(np.abs(ro).max()) + 1e-6
         assert err <= bound, f"head {hh}: max|dO| {err:.3e} > bound {bound:.3e}"
-        check_lse(lse[0, hh][rows], rlse, f"lse[{hh}]")
+        check_lse(lse[0, hh], rlse[0, 0], f"lse[{hh}]")
 
 
 # The extended-call rows as bench.py runs them on the long workload: 8

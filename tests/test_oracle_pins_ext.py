@@ -239,6 +239,55 @@ def test_extended_varlen_equals_dense_per_sequence():
             np.testing.assert_allclose(dv[ks], rdv[0].transpose(1, 0, 2), rtol=0, atol=1e-14)
 
 
+ROW_CASES = [
+    # s_q, s_kv, mask, window, h, h_kv
+    (9, 13, "bottom_right", 2, 4, 2),    # s_q < s_kv, window, GQA groups of 2
+    (13, 9, "bottom_right", -1, 2, 1),   # s_q > s_kv: leading dead rows, MQA
+    (11, 11, "top_left", 3, 6, 3),
+    (10, 7, "none", 1, 2, 2),
+]
+
+
+@pytest.mark.parametrize("case", ROW_CASES)
+def test_row_sampled_extended_entry_points_match_full(case):
+    """The row-selecting calls that check full-size GPU results (one query
+    head and its key/value head at a time, rows listed in any order) equal
+    the matching rows of the full extended calls, and those rows equal
+    torch's float64 reference; dK/dV of a key/value head are the sums of its
+    group's per-query-head row results."""
+    s_q, s_kv, mask, window, h, h_kv = case
+    d, scale, g = 4, 0.45, h // h_kv
+    seed = 800 + ROW_CASES.index(case)
+    q, k, v = _rand((1, h, s_q, d), seed), _rand((1, h_kv, s_kv, d), seed + 1), \
+        _rand((1, h_kv, s_kv, d), seed + 2)
+    do = _rand((1, h, s_q, d), seed + 3)
+    o, lse = oracle.sdpa_fwd_ex(q, k, v, scale, mask, window)
+    dq, dk, dv = oracle.sdpa_bwd_ex(q, k, v, do, scale, mask, window)
+    ro, rlse, rdq, rdk, rdv, live = _torch_ref(q, k, v, do, scale, mask, window)
+    rng = np.random.default_rng(seed)
+    q_rows = rng.permutation(s_q)[: max(2, s_q - 3)].astype(np.int32)
+    kv_rows = rng.permutation(s_kv)[: max(2, s_kv - 2)].astype(np.int32)
+    for hk in range(h_kv):
+        sum_dk = sum_dv = 0
+        for hq in range(hk * g, (hk + 1) * g):
+            args = (q[0, hq], k[0, hk], v[0, hk])
+            fo, flse = oracle.attn_fwd_rows_ex(*args, q_rows, scale, mask, window)
+            np.testing.assert_array_equal(fo, o[0, hq][q_rows])
+            np.testing.assert_array_equal(flse, lse[0, hq][q_rows])
+            np.testing.assert_allclose(fo, ro[0, hq][q_rows].numpy(), rtol=0, atol=1e-12)
+            bq, bk, bv = oracle.attn_bwd_rows_ex(*args, do[0, hq], q_rows, kv_rows, scale, mask,
+                                                 window)
+            np.testing.assert_array_equal(bq, dq[0, hq][q_rows])
+            np.testing.assert_allclose(bq, rdq[0, hq][q_rows].numpy(), rtol=0, atol=1e-11)
+            sum_dk, sum_dv = sum_dk + bk, sum_dv + bv
+        np.testing.assert_allclose(sum_dk, dk[0, hk][kv_rows], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(sum_dv, dv[0, hk][kv_rows], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(sum_dk, rdk[0, hk][kv_rows].numpy(), rtol=0, atol=1e-11)
+        np.testing.assert_allclose(sum_dv, rdv[0, hk][kv_rows].numpy(), rtol=0, atol=1e-11)
+    if mask == "bottom_right" and s_q > s_kv:  # the listed rows include dead ones
+        assert (~live.numpy())[q_rows].any()
+
+
 # ------------------------------------------------------------------ FP8 E4M3
 def test_e4m3_decoder_matches_torch_on_every_code():
     codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
