@@ -257,6 +257,11 @@ int check_ptrs(const Span *in, int n_in, const Span *out, int n_out) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Backward CTA order (bwd.cu): key/value slices per group, and the working
+// set (dQ accumulator, Q, dO, K, V) below which one group holds every slice.
+constexpr int kBwdSliceGroup = 4;
+constexpr size_t kBwdOneGroupBytes = size_t(64) << 20;
+
 int launch_status(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return ok();
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
@@ -299,7 +304,7 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.10 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.11 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)
@@ -760,6 +765,13 @@ int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o, cons
     p.window = window_left;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
+    // CTA order of the main kernel: groups of four key/value slices keep the
+    // resident CTAs' dQ accumulator, Q and dO in L2; a problem whose whole
+    // working set fits in half of L2 runs as one group (heaviest units first).
+    const size_t working = (size_t)bh * s_q * d * 4 + 2 * qbytes + 2 * kvbytes;
+    p.slice_group = working <= kBwdOneGroupBytes ? (int)bh_kv : kBwdSliceGroup;
+    p.seq_table = 0;
+    p.grid = (int)(kv_tiles * bh_kv);
     return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
 }
 
@@ -857,6 +869,16 @@ int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *
     p.window = window_left;
     p.scale = attn_scale;
     p.scale_log2 = attn_scale * kLog2e;
+    // CTA grid of the main kernel: the sequences' own key tiles from a per-CTA
+    // sequence table (sum over n of ceil(Lkv_n / 128) <= total_kv / 128 +
+    // num_seqs, and <= num_seqs times the longest), or the envelope of the
+    // longest sequence for lists too long to tabulate.
+    p.slice_group = kBwdSliceGroup;
+    p.seq_table = num_seqs <= kBwdSeqTableMax ? 1 : 0;
+    const int64_t tiles = p.seq_table ? std::min<int64_t>((int64_t)num_seqs * kv_tiles,
+                                                          total_kv / kTileN + num_seqs)
+                                      : (int64_t)num_seqs * kv_tiles;
+    p.grid = (int)(tiles * h_kv);
     return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
 }
 

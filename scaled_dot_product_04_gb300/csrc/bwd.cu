@@ -200,8 +200,6 @@ struct BwdLayout {
 // warps: 0 TMA, 1 MMA, 2-5 compute (queries 0-63 of a tile), 6-9 compute
 // (queries 64-127), 10-13 dQ epilogue
 constexpr int kBwdThreads = 448;
-// slices whose key tiles are interleaved in the CTA order
-constexpr int kSliceGroup = 4;
 
 template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -217,36 +215,157 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // A CTA owns one key tile of one key/value slice ((batch, kv head) or
     // (sequence, kv head)) and walks every query tile that can see it, for
     // each of the group's h / h_kv query heads in turn, so dK and dV sum over
-    // the group in TMEM.  Order: slices in groups of kSliceGroup, key tile
+    // the group in TMEM.  Order: slices in groups of p.slice_group, key tile
     // major within a group (under a causal mask the first key tiles see the
-    // most query tiles, so the heaviest units of a group start first).  The
-    // CTAs resident at any time then share a few slices, whose fp32 dQ
-    // accumulator, Q and dO stay in L2 instead of every head's at once; and
-    // the heaviest unit of the last group starts early enough not to run
-    // alone at the end, as the last slice's first key tile would in plain
-    // slice-major order.
-    const int per_group = kSliceGroup * p.kv_tiles;
-    const int group_i = blockIdx.x / per_group;
-    const int in_group = blockIdx.x - group_i * per_group;
-    const int group_n = min(kSliceGroup, p.kv_slices - group_i * kSliceGroup);
-    const int slice = group_i * kSliceGroup + in_group % group_n;  // key/value slice
-    const int kt = in_group / group_n;
-    const int hk = slice % p.h_kv;              // key/value head
+    // most query tiles, so the heaviest units of a group start first).  For
+    // large problems the groups hold four slices: the CTAs resident at
+    // any time then share a few slices, whose fp32 dQ accumulator, Q and dO
+    // stay in L2 instead of every head's at once, and the heaviest unit of
+    // the last group starts early enough not to run alone at the end, as the
+    // last slice's first key tile would in plain slice-major order.  When the
+    // whole problem fits in L2 anyway, one group holds every slice, which
+    // starts the heaviest units of all slices first.
+    //
+    // Packed inputs with a sequence table (p.seq_table) use a compact grid:
+    // the units are the sequences' own key tiles, sequences longest first
+    // (most query tiles) and, within a sequence, its key/value heads in groups
+    // of p.slice_group with the key tiles major within a group, so no CTA
+    // lands past its sequence's last key tile, the resident CTAs share a few
+    // heads' Q, dO and dQ accumulator in L2, and the last units to start are
+    // the shortest sequence's.
+    int slice, kt;
     int Lq, Lkv, tok_q0 = 0, tok_kv0 = 0;
+    if constexpr (kPacked) {
+        if (p.seq_table) {
+            // The table: sequences ordered by query tiles, most first (ties in
+            // sequence order); first unit of each = exclusive prefix sum of
+            // key tiles x key/value heads in that order.  Lists of up to 32
+            // sequences are tabulated by warp 0 in registers (lane = sequence);
+            // longer ones in the dS tile's shared memory (unused until the
+            // compute warps' first dS), sorted only up to 256 sequences.
+            static_assert(4 * (4 * kBwdSeqTableMax + 7) <= 2 * L::kChunkBytes,
+                          "the sequence table must fit in the dS tile");
+            const int ns = p.num_seqs;
+            const int u = blockIdx.x;
+            int *pick = reinterpret_cast<int *>(smem + L::kDS);  // [n, first unit, total units]
+            if (ns <= 32) {
+                if (threadIdx.x < 32) {
+                    const int ln = threadIdx.x;
+                    int tq = -1, tk = 0;
+                    if (ln < ns) {
+                        tq = (p.cu_q[ln + 1] - p.cu_q[ln] + kTileM - 1) / kTileM;
+                        tk = (p.cu_kv[ln + 1] - p.cu_kv[ln] + kTileN - 1) / kTileN;
+                    }
+                    const int units = tk * p.h_kv;
+                    int first = 0, total = 0;
+                    for (int m = 0; m < ns; ++m) {
+                        const int tm = __shfl_sync(0xffffffffu, tq, m);
+                        const int um = __shfl_sync(0xffffffffu, units, m);
+                        // m comes before this lane's sequence in the table
+                        if (tm > tq || (tm == tq && m < ln)) first += um;
+                        total += um;
+                    }
+                    const bool mine = ln < ns && u >= first && u < first + units;
+                    const unsigned who = __ballot_sync(0xffffffffu, mine);
+                    if (mine) {
+                        pick[0] = ln;
+                        pick[1] = first;
+                    }
+                    if (ln == 0) pick[2] = total;
+                    if (who == 0 && ln == 0) pick[0] = -1;
+                }
+            } else {
+                int *cq = pick + 4;
+                int *ckv = cq + (ns + 1);
+                int *order = ckv + (ns + 1);
+                int *first = order + ns;  // ns + 1 entries
+                for (int i = threadIdx.x; i <= ns; i += blockDim.x) {
+                    cq[i] = p.cu_q[i];
+                    ckv[i] = p.cu_kv[i];
+                }
+                __syncthreads();
+                auto q_tiles_of = [&](int n) { return (cq[n + 1] - cq[n] + kTileM - 1) / kTileM; };
+                for (int n = threadIdx.x; n < ns; n += blockDim.x) {
+                    int rank = n;  // long lists keep their own order
+                    if (ns <= 256) {
+                        const int tn = q_tiles_of(n);
+                        rank = 0;
+                        for (int m = 0; m < ns; ++m) {
+                            const int tm = q_tiles_of(m);
+                            rank += (tm > tn || (tm == tn && m < n)) ? 1 : 0;
+                        }
+                    }
+                    order[rank] = n;
+                }
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    int run = 0;
+                    for (int i = 0; i < ns; ++i) {
+                        first[i] = run;
+                        const int n = order[i];
+                        run += (ckv[n + 1] - ckv[n] + kTileN - 1) / kTileN * p.h_kv;
+                    }
+                    first[ns] = run;
+                    pick[2] = run;
+                    pick[0] = -1;
+                    if (u < run) {
+                        int lo = 0, hi = ns;  // first[lo] <= u < first[hi]
+                        while (hi - lo > 1) {
+                            const int mid = (lo + hi) >> 1;
+                            if (first[mid] <= u) lo = mid;
+                            else hi = mid;
+                        }
+                        pick[0] = order[lo];
+                        pick[1] = first[lo];
+                    }
+                }
+            }
+            __syncthreads();
+            const int n = pick[0], first_u = pick[1];
+            __syncthreads();  // every thread has read the pick before the region is reused
+            if (n < 0) return;  // the host sizes the grid by an upper bound
+            tok_q0 = p.cu_q[n];
+            tok_kv0 = p.cu_kv[n];
+            Lq = p.cu_q[n + 1] - tok_q0;
+            Lkv = p.cu_kv[n + 1] - tok_kv0;
+            // within the sequence: its key/value heads in groups of
+            // p.slice_group, key tile major within a group (as the dense order)
+            const int local = u - first_u;
+            const int n_kt = (Lkv + kTileN - 1) / kTileN;
+            const int per_group = p.slice_group * n_kt;
+            const int group_i = local / per_group;
+            const int in_group = local - group_i * per_group;
+            const int group_n = min(p.slice_group, p.h_kv - group_i * p.slice_group);
+            kt = in_group / group_n;
+            slice = n * p.h_kv + group_i * p.slice_group + in_group % group_n;
+        }
+    }
+    if (!kPacked || !p.seq_table) {
+        const int per_group = p.slice_group * p.kv_tiles;
+        const int group_i = blockIdx.x / per_group;
+        const int in_group = blockIdx.x - group_i * per_group;
+        const int group_n = min(p.slice_group, p.kv_slices - group_i * p.slice_group);
+        slice = group_i * p.slice_group + in_group % group_n;  // key/value slice
+        kt = in_group / group_n;
+        if constexpr (kPacked) {
+            const int n = slice / p.h_kv;
+            tok_q0 = p.cu_q[n];
+            tok_kv0 = p.cu_kv[n];
+            Lq = p.cu_q[n + 1] - tok_q0;
+            Lkv = p.cu_kv[n + 1] - tok_kv0;
+        } else {
+            Lq = p.s_q;
+            Lkv = p.s_kv;
+        }
+    }
+    const int hk = slice % p.h_kv;              // key/value head
     int q_slice0;                               // dense: query slice of the group's first head
     RowMap km;
     if constexpr (!kPacked) {
-        Lq = p.s_q;
-        Lkv = p.s_kv;
         q_slice0 = (slice / p.h_kv) * p.h + hk * p.group;
         km = {(int64_t)slice * p.s_kv * D, D, 0};
     } else {
-        const int n = slice / p.h_kv;
         q_slice0 = 0;
-        tok_q0 = p.cu_q[n];
-        tok_kv0 = p.cu_kv[n];
-        Lq = p.cu_q[n + 1] - tok_q0;
-        Lkv = p.cu_kv[n + 1] - tok_kv0;
         km = {((int64_t)tok_kv0 * p.h_kv + hk) * D, (int64_t)p.h_kv * D, 0};
     }
     const int k0 = kt * kTileN;
@@ -718,10 +837,12 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     auto kern = bwd_main_kernel<D, kBf16, kPacked>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    const int grid = p.kv_tiles * p.kv_slices;
+    const int grid = p.grid;  // 0 when no sequence has a key: dK, dV are empty then
     if (timer.start) cudaEventRecord(timer.start, stream);
-    kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, trx, p);
-    e = cudaGetLastError();
+    if (grid > 0) {
+        kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, trx, p);
+        e = cudaGetLastError();
+    }
     if (p.deterministic) {
         // the timed span covers the main kernel and the dQ pass
         if (e == cudaSuccess) e = launch_bwd_dq(tq, tk, tv, tdo, p, p.q_tiles, D, kBf16, kPacked, stream);

@@ -97,7 +97,14 @@ struct BwdParams {
     int deterministic;           // 1: the main kernel skips dQ (bwd_dq.cu computes it)
     int q_tiles;                 // query tiles per slice: dense ceil(s_q/128), packed
                                  // ceil(max_seqlen_q/128) (the dQ pass's grid)
+    int slice_group;             // key/value slices interleaved in the main kernel's CTA order
+    int seq_table;               // packed: 1 = compact grid over a per-CTA table of the
+                                 // sequences (longest first), 0 = envelope grid
+    int grid;                    // main kernel CTAs
 };
+// Largest sequence count of the packed backward's per-CTA sequence table (it
+// is built in the dS tile's shared memory before that is used).
+constexpr int kBwdSeqTableMax = 1024;
 
 // Failure-detection self-test (selftest.cu): one CTA waits, with the bounded
 // wait of every kernel and the given limit, on a barrier phase that nothing
