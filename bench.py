@@ -62,7 +62,9 @@ TRAFFIC = {("bwd_main", "sdpa_gb300 0.4 sm_103a"): 0.81430e9 + 0.49046e9,
            ("bwd_main", "sdpa_gb300 0.7 sm_103a"): 0.83157e9 + 0.50512e9,
            ("bwd_main", "sdpa_gb300 0.8 sm_103a"): 0.83157e9 + 0.50512e9,
            ("bwd_main", "sdpa_gb300 0.9 sm_103a"): 0.83157e9 + 0.50512e9,
-           ("bwd_main", "sdpa_gb300 0.10 sm_103a"): 0.83157e9 + 0.50512e9}
+           ("bwd_main", "sdpa_gb300 0.10 sm_103a"): 0.83157e9 + 0.50512e9,
+           # 0.11 changed the CTA order of small and packed problems only
+           ("bwd_main", "sdpa_gb300 0.11 sm_103a"): 0.832530e9 + 0.505720e9}
 
 
 def fwd_flops(w) -> float:
