@@ -68,6 +68,9 @@ struct RowMap {
 template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const BwdParams p, int64_t rows, int64_t acc_elems) {
+    // the main kernel may set up (barriers, TMEM, its K and V loads) meanwhile;
+    // it waits for this grid before it reads a row term or adds into dQ
+    griddep_launch_dependents();
     constexpr int kLanesPerRow = D / 8;
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
     const int64_t warp_global = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------ dq convert
 template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BwdParams p, int64_t rows) {
+    griddep_wait();  // the main kernel's dQ accumulator is complete
     // thread handles 8 consecutive elements of one row of dQ (I/O order)
     constexpr int kPerRow = D / 8;
     const int64_t total = rows * kPerRow;
@@ -467,6 +471,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(sbase + L::kV + c * L::kChunkBytes, &tm_v, bar(L::bKVFull), c * 64, ky, kz);
             }
         }
+        // The row terms come from the preprocess grid; once it is done, the
+        // kernel behind this one (dQ convert, or the deterministic dQ pass,
+        // which needs only the row terms) may start filling freed SMs.
+        griddep_wait();
+        if (lane == 0) griddep_launch_dependents();
         int issued = 0, issued_do = 0;
         for (int i = 0; i < n_it; ++i) {
             const int st = i & 1, use = i >> 1;
@@ -747,6 +756,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t stage = sbase + L::kDQStage + quad * (L::kDQSlots * L::kDQBoxBytes);
         uint8_t *stage_ptr = smem + L::kDQStage + quad * (L::kDQSlots * L::kDQBoxBytes) + lane * 64;
         int boxes = 0, slot = 0;  // boxes sent by this warp; slot of the next one
+        griddep_wait();  // the preprocess grid has zeroed the accumulator
         // one 32 x 16 box: registers r[0..16) -> staging slot -> reduce-add
         // into accumulator rows [arow, arow + 32), columns [col, col + 16)
         auto send = [&](const uint32_t *r, int col, int arow) {
@@ -839,10 +849,9 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     if (e != cudaSuccess) return e;
     const int grid = p.grid;  // 0 when no sequence has a key: dK, dV are empty then
     if (timer.start) cudaEventRecord(timer.start, stream);
-    if (grid > 0) {
-        kern<<<grid, kBwdThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, trx, p);
-        e = cudaGetLastError();
-    }
+    if (grid > 0)
+        e = launch_overlapped(kern, dim3(grid), dim3(kBwdThreads), L::kBytes, stream, tq, tk, tv, tdo,
+                              tdq, trx, p);
     if (p.deterministic) {
         // the timed span covers the main kernel and the dQ pass
         if (e == cudaSuccess) e = launch_bwd_dq(tq, tk, tv, tdo, p, p.q_tiles, D, kBf16, kPacked, stream);
@@ -851,8 +860,8 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     }
     if (timer.stop) cudaEventRecord(timer.stop, stream);
     if (e != cudaSuccess) return e;
-    bwd_dq_convert_kernel<D, kBf16, kPacked><<<small_grid, 256, 0, stream>>>(p, rows);
-    return cudaGetLastError();
+    return launch_overlapped(bwd_dq_convert_kernel<D, kBf16, kPacked>, dim3(small_grid), dim3(256), 0,
+                             stream, p, rows);
 }
 
 }  // namespace

@@ -377,8 +377,10 @@ cudaError_t launch_dq_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
     if (e != cudaSuccess) return e;
     const int grid = q_tiles * p.bh;
-    kern<<<grid, kDqThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, tdo, p, q_tiles);
-    return cudaGetLastError();
+    // starts as the main kernel's last CTAs start (they signal once the row
+    // terms it reads are complete); it shares no data with the main kernel
+    return launch_overlapped(kern, dim3(grid), dim3(kDqThreads), L::kSmemAlloc, stream, tq, tk, tv, tdo,
+                             p, q_tiles);
 }
 
 }  // namespace

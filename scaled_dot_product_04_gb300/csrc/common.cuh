@@ -118,6 +118,25 @@ struct KernelTimer {
     cudaEvent_t start = nullptr, stop = nullptr;
 };
 
+// Launch with programmatic stream serialization (see griddep_wait in
+// ptx.cuh): the kernel may start while the previous kernel on `stream`
+// finishes, and waits for it only where it reads that kernel's results.
+template <class... KArgs, class... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Two-tile forward (fwd_pair.cu): 256 query rows per unit; q_tiles / n_units
 // then count 256-row blocks.
 int fwd_pair_rows();

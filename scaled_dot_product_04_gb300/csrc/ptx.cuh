@@ -53,6 +53,15 @@ SDPA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may start while the kernel ahead of it in the
+// stream is still running: griddep_wait() blocks until that kernel has
+// completed and its memory writes are visible, and griddep_launch_dependents()
+// lets the kernel behind this one start once every CTA of this grid has issued
+// it or exited.  Without the attribute both are no-ops.
+SDPA_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SDPA_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Per-warpgroup register budgets (all four warps of a warpgroup execute it).
 template <uint32_t N>
 SDPA_DEV void setmaxnreg_dec() {
