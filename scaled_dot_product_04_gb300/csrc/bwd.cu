@@ -327,7 +327,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncthreads();
             const int n = pick[0], first_u = pick[1];
             __syncthreads();  // every thread has read the pick before the region is reused
-            if (n < 0) return;  // the host sizes the grid by an upper bound
+            if (n < 0) {  // the host sizes the grid by an upper bound
+                griddep_wait();  // see the early exits below
+                return;
+            }
             tok_q0 = p.cu_q[n];
             tok_kv0 = p.cu_kv[n];
             Lq = p.cu_q[n + 1] - tok_q0;
@@ -373,7 +376,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         km = {((int64_t)tok_kv0 * p.h_kv + hk) * D, (int64_t)p.h_kv * D, 0};
     }
     const int k0 = kt * kTileN;
-    if (k0 >= Lkv) return;  // packed: this sequence has fewer key tiles
+    // Every early exit waits for the preprocess grid first: the kernel behind
+    // this one (the deterministic dQ pass, which reads the row terms without a
+    // wait of its own) may start once every CTA has signalled or exited, so no
+    // CTA may exit before the row terms are complete.
+    if (k0 >= Lkv) {  // packed: this sequence has fewer key tiles
+        griddep_wait();
+        return;
+    }
     // Query rows that see at least one key of [k0, k_last]: a causal mask
     // needs i + delta >= k0, a window i + delta - window <= k_last.
     const int delta = mask_delta(p.mask, Lq, Lkv);
@@ -405,6 +415,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int i = 0; i < D / 8; ++i) a[i] = b[i] = make_uint4(0, 0, 0, 0);
             }
         }
+        griddep_wait();
         return;
     }
 
@@ -412,6 +423,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if ((sbase & 1023u) != 0) {
         // The swizzled operand tiles need a 1024-byte aligned base.
         if (threadIdx.x == 0) atomicCAS(p.err, 0u, (kTagBwdMain << 16) | 0xfffu);
+        griddep_wait();
         return;
     }
     auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * i; };
@@ -854,7 +866,10 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
                               tdq, trx, p);
     if (p.deterministic) {
         // the timed span covers the main kernel and the dQ pass
-        if (e == cudaSuccess) e = launch_bwd_dq(tq, tk, tv, tdo, p, p.q_tiles, D, kBf16, kPacked, stream);
+        // it overlaps the main kernel's last wave; with no main kernel it
+        // follows the preprocess kernel in plain stream order
+        if (e == cudaSuccess)
+            e = launch_bwd_dq(tq, tk, tv, tdo, p, p.q_tiles, D, kBf16, kPacked, grid > 0, stream);
         if (timer.stop) cudaEventRecord(timer.stop, stream);
         return e;
     }

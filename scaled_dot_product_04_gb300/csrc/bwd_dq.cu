@@ -371,26 +371,31 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
 template <int D, bool kBf16, bool kPacked>
 cudaError_t launch_dq_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const CUtensorMap &tdo, const BwdParams &p, int q_tiles, cudaStream_t stream) {
+                        const CUtensorMap &tdo, const BwdParams &p, int q_tiles, bool overlap,
+                        cudaStream_t stream) {
     using L = DqLayout<D>;
     auto kern = bwd_dq_kernel<D, kBf16, kPacked>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
     if (e != cudaSuccess) return e;
     const int grid = q_tiles * p.bh;
-    // starts as the main kernel's last CTAs start (they signal once the row
-    // terms it reads are complete); it shares no data with the main kernel
-    return launch_overlapped(kern, dim3(grid), dim3(kDqThreads), L::kSmemAlloc, stream, tq, tk, tv, tdo,
-                             p, q_tiles);
+    // overlap: start as the main kernel's last CTAs start (they signal once
+    // the row terms this pass reads are complete); it shares no data with
+    // the main kernel
+    if (overlap)
+        return launch_overlapped(kern, dim3(grid), dim3(kDqThreads), L::kSmemAlloc, stream, tq, tk, tv,
+                                 tdo, p, q_tiles);
+    kern<<<grid, kDqThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, tdo, p, q_tiles);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tdo, const BwdParams &p, int q_tiles, int d, bool bf16,
-                          bool packed, cudaStream_t stream) {
+                          bool packed, bool overlap, cudaStream_t stream) {
 #define SDPA_DQ_CASE(D_, BF_, PK_)                                             \
     if (d == D_ && bf16 == BF_ && packed == PK_)                               \
-        return launch_dq_t<D_, BF_, PK_>(tq, tk, tv, tdo, p, q_tiles, stream);
+        return launch_dq_t<D_, BF_, PK_>(tq, tk, tv, tdo, p, q_tiles, overlap, stream);
     SDPA_DQ_CASE(64, true, false)
     SDPA_DQ_CASE(64, true, true)
     SDPA_DQ_CASE(64, false, false)

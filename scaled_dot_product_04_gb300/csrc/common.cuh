@@ -164,9 +164,12 @@ cudaError_t launch_fwd_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const C
                            cudaStream_t stream, const KernelTimer &timer);
 // Deterministic dQ pass (bwd_dq.cu): one CTA per (query slice, query tile);
 // q_tiles = query tiles per slice.  Writes p.dq from the row terms in p.rowx.
+// overlap: launched to overlap the main kernel just ahead of it on `stream`
+// (which must wait for the preprocess kernel before signalling), else in plain
+// stream order.
 cudaError_t launch_bwd_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tdo, const BwdParams &p, int q_tiles, int d, bool bf16,
-                          bool packed, cudaStream_t stream);
+                          bool packed, bool overlap, cudaStream_t stream);
 // tdq: 2-D fp32 map over the dQ accumulator [rows][d], box 16 x 32, 64-byte swizzle.
 // trx: map over the row terms (dense [b*h][s_q][4], packed [T][h][4] fp32), 128-row boxes.
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

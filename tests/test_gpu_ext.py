@@ -239,6 +239,39 @@ def test_deterministic_packed_bwd(sdpa, case):
     _grads_ok(runs[0], oracle.sdpa_varlen_bwd_ex(q, k, v, do, cu_q, cu_kv, scale, mask, window))
 
 
+def test_deterministic_packed_bwd_without_keys_or_with_unseen_key_tiles(sdpa):
+    """The deterministic dQ pass starts while the main kernel runs and reads
+    the preprocess kernel's row terms without waiting itself: here every main
+    CTA either has no key tile (no sequence has keys: the pass then follows
+    the preprocess kernel in plain order) or sees no query for some of its key
+    tiles (a bottom-right band of 6 keys leaves the first key tiles unseen)."""
+    h, d = 2, 64
+    lq, lk = [40, 7, 130], [0, 0, 0]
+    q, k, v, do, cu_q, cu_kv = sdpa_inputs.packed(lq, lk, h, d, seed=8100)
+    qc, doc, cq, ck = q.cuda(), do.cuda(), cu_q.cuda(), cu_kv.cuda()
+    kc = torch.empty((8, h, d), dtype=q.dtype, device="cuda")  # capacity only, total_kv = 0
+    o, lse = sdpa.attention_varlen(qc, kc, kc, cq, ck, max(lq), 0, scale=0.125, causal=True,
+                                   total_kv=0)
+    dq, dk, dv = sdpa.attention_varlen_bwd(qc, kc, kc, o, doc, lse, cq, ck, max(lq), 0,
+                                           scale=0.125, causal=True, deterministic=True,
+                                           total_kv=0)
+    torch.cuda.synchronize()
+    assert torch.isneginf(lse).all() and float(o.abs().max()) == 0.0
+    assert float(dq.abs().max()) == 0.0
+    lq, lk = [50, 200, 64], [400, 390, 500]
+    q, k, v, do, cu_q, cu_kv = sdpa_inputs.packed(lq, lk, h, d, seed=8101)
+    qc, kc, vc, doc, cq, ck = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu_q.cuda(), cu_kv.cuda()
+    o, lse = sdpa.attention_varlen(qc, kc, vc, cq, ck, max(lq), max(lk), scale=0.125,
+                                   mask="bottom_right", window_left=5)
+    runs = [sdpa.attention_varlen_bwd(qc, kc, vc, o, doc, lse, cq, ck, max(lq), max(lk),
+                                      scale=0.125, mask="bottom_right", window_left=5,
+                                      deterministic=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(runs[0][i], runs[1][i])
+    _grads_ok(runs[0], oracle.sdpa_varlen_bwd_ex(q, k, v, do, cu_q, cu_kv, 0.125, "bottom_right", 5))
+
+
 def test_deterministic_workspace_is_the_row_terms(sdpa):
     assert sdpa.sdpa_bwd_ex_workspace_size(2, 3, 100, 128, 1) == 2 * 3 * 100 * 16 + 256 - (2 * 3 * 100 * 16) % 256
     assert sdpa.sdpa_bwd_ex_workspace_size(2, 3, 100, 128, 0) == sdpa.sdpa_bwd_workspace_size(2, 3, 100, 128)
