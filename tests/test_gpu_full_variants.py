@@ -85,16 +85,17 @@ def test_full_size_fp8_fwd_whole_heads(sdpa):
 
 # The extended-call rows as bench.py runs them on the long workload: 8
 # key/value heads; causal with window_left = 2048; 4096 queries against the
-# 16384 keys under the bottom-right mask.  Sampled rows of O, LSE, dQ, dK, dV
-# against the oracle's extended definitions (GQA: a key/value head's dK and dV
-# sum over its group's query heads).
+# 16384 keys under the bottom-right mask.  O, LSE, dQ, dK, dV against the
+# oracle's extended definitions: a whole head for the window and the
+# bottom-right mask; sampled rows of one key/value head's group for GQA (a
+# key/value head's dK and dV sum over its group's query heads).
 EXT = {"gqa": (8, 16384, "top_left", -1),
        "window": (32, 16384, "top_left", 2048),
        "bottom_right": (32, 4096, "bottom_right", -1)}
 
 
 @pytest.mark.parametrize("name", list(EXT))
-def test_full_size_extended_rows_sampled(sdpa, name):
+def test_full_size_extended_rows(sdpa, name):
     from helpers import O_TOL
     w = sdpa_inputs.WORKLOADS[NAME]
     h_kv, s_q, mask, window = EXT[name]
@@ -110,6 +111,17 @@ def test_full_size_extended_rows_sampled(sdpa, name):
     group = w.h // h_kv
     hk = min(1, h_kv - 1)
     heads = [hk * group + g for g in range(group)]
+    if group == 1:
+        # one query head per key/value head: the whole head, every row
+        hh = heads[0]
+        sl = [x[0:1, hh:hh + 1] for x in (q, k, v, do)]
+        ro, rl = oracle.sdpa_fwd_ex(sl[0], sl[1], sl[2], w.scale, mask, window)
+        check_rel(o[0, hh], ro[0, 0], O_TOL[torch.bfloat16], f"o[{hh}]")
+        check_lse(lse[0, hh], rl[0, 0], f"lse[{hh}]")
+        r = oracle.sdpa_bwd_ex(*sl, w.scale, mask, window)
+        for g, rr, nm in zip((dq, dk, dv), r, ("dq", "dk", "dv")):
+            check_rel(g[0, hh], rr[0, 0], GRAD_TOL, f"{nm}[{hh}]")
+        return
     qr, kr = _rows(s_q, 7), _rows(w.s, 8)
     r_dk = r_dv = 0
     for hh in heads:
