@@ -382,6 +382,32 @@ void sdpa_set_kernel_timer(void *start_event, void *stop_event);
  */
 int sdpa_set_forward_variant(int variant);
 
+/*
+ * Backward main-kernel choice for later calls on this host thread (a tuning
+ * and testing hook; no counterpart on the pages).  0 (default): automatic --
+ * the persistent kernel (one CTA per SM, each taking (key/value slice, key
+ * tile) units from a counter) where units are short: dense problems whose
+ * units average at most 8 (query head, query tile) pairs, and packed lists of
+ * up to 128 sequences whose estimated mean (from total_kv / num_seqs, the
+ * mask and the window) is at most 3; one CTA per unit otherwise.  1: always
+ * one CTA per unit.  2: the persistent kernel wherever it applies (not for
+ * packed lists of more than 128 sequences).  Both give the same dK and dV bit
+ * for bit, and dQ to rounding (its fp32 additions may come in another order).
+ * Returns SDPA_ERR_INVALID_ARG for other values.
+ */
+int sdpa_set_backward_variant(int variant);
+
+/* Main kernel that this host thread's last backward call launched (or would
+ * have launched, had it had a unit of work): 1 one CTA per unit, 2 persistent;
+ * 0 before the first call that reached the choice. */
+int sdpa_last_backward_variant(void);
+
+/* Testing hook: at most max_ctas CTAs for the persistent backward kernel on
+ * this host thread (0, the default: one per SM), so that small problems
+ * exercise CTAs that take many units each.  The result is the same.
+ * Returns SDPA_ERR_INVALID_ARG for a negative count. */
+int sdpa_set_backward_grid_limit(int max_ctas);
+
 /* Library version string, e.g. "sdpa_gb300 0.10 sm_103a"; the
  * minor number changes whenever a kernel changes. */
 const char *sdpa_version(void);

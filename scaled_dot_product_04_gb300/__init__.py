@@ -18,6 +18,8 @@ from ._lib import (SDPA_BF16, SDPA_FP16, SDPA_FP8_E4M3, sdpa_fwd_fp8, sdpa_varle
                    sdpa_bwd_ex_workspace_size, sdpa_bwd_noalloc, sdpa_bwd_workspace_size,
                    sdpa_check_device_error, sdpa_fwd, sdpa_fwd_ex, sdpa_last_error,
                    sdpa_selftest_wait_timeout,
+                   sdpa_last_backward_variant, sdpa_set_backward_grid_limit,
+                   sdpa_set_backward_variant,
                    sdpa_set_forward_variant, sdpa_set_kernel_timer, sdpa_varlen_bwd,
                    sdpa_varlen_bwd_ex, sdpa_varlen_bwd_ex_workspace_size,
                    sdpa_varlen_bwd_workspace_size, sdpa_varlen_fwd, sdpa_varlen_fwd_ex, sdpa_version)
@@ -28,7 +30,8 @@ __all__ = ["attention", "attention_varlen", "attention_bwd", "attention_varlen_b
            "sdpa_bwd_workspace_size", "sdpa_varlen_bwd_workspace_size",
            "sdpa_bwd_ex_workspace_size", "sdpa_varlen_bwd_ex_workspace_size", "sdpa_last_error",
            "sdpa_check_device_error", "sdpa_selftest_wait_timeout", "sdpa_set_forward_variant",
-           "sdpa_set_kernel_timer",
+           "sdpa_set_backward_variant", "sdpa_last_backward_variant",
+           "sdpa_set_backward_grid_limit", "sdpa_set_kernel_timer",
            "sdpa_version", "SdpaError", "load", "SDPA_MASK_NONE", "SDPA_MASK_CAUSAL",
            "SDPA_MASK_CAUSAL_BOTTOM_RIGHT", "SDPA_FP8_E4M3", "sdpa_fwd_fp8", "sdpa_varlen_fwd_fp8",
            "attention_fp8"]

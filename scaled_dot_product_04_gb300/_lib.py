@@ -37,9 +37,9 @@ EXPORTS = ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_fwd_ex", "sdpa_varlen_fwd_ex", "
            "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_varlen_bwd_workspace_size",
            "sdpa_varlen_bwd", "sdpa_bwd_ex_workspace_size", "sdpa_varlen_bwd_ex_workspace_size",
            "sdpa_bwd_ex", "sdpa_varlen_bwd_ex", "sdpa_bwd_noalloc", "sdpa_last_error",
-           "sdpa_check_device_error", "sdpa_selftest_wait_timeout", "sdpa_set_forward_variant",
-           "sdpa_set_kernel_timer",
-           "sdpa_version")
+           "sdpa_check_device_error", "sdpa_selftest_wait_timeout", "sdpa_set_kernel_timer",
+           "sdpa_set_forward_variant", "sdpa_set_backward_variant", "sdpa_last_backward_variant",
+           "sdpa_set_backward_grid_limit", "sdpa_version")
 
 
 class SdpaError(RuntimeError):
@@ -107,6 +107,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.sdpa_version.restype = ctypes.c_char_p
         lib.sdpa_set_forward_variant.argtypes = [_I]
         lib.sdpa_set_forward_variant.restype = _I
+        lib.sdpa_set_backward_variant.argtypes = [_I]
+        lib.sdpa_set_backward_variant.restype = _I
+        lib.sdpa_last_backward_variant.argtypes = []
+        lib.sdpa_last_backward_variant.restype = _I
+        lib.sdpa_set_backward_grid_limit.argtypes = [_I]
+        lib.sdpa_set_backward_grid_limit.restype = _I
         lib.sdpa_set_kernel_timer.argtypes = [_P, _P]
         lib.sdpa_set_kernel_timer.restype = None
         for name in ("sdpa_fwd", "sdpa_varlen_fwd", "sdpa_bwd", "sdpa_varlen_bwd",
@@ -289,6 +295,21 @@ def sdpa_set_kernel_timer(start_event=None, stop_event=None) -> None:
 def sdpa_set_forward_variant(variant: int) -> None:
     """0: automatic forward kernel choice, 1: one-tile kernel, 2: two-tile kernel."""
     _check(load().sdpa_set_forward_variant(int(variant)))
+
+
+def sdpa_set_backward_variant(variant: int) -> None:
+    """0: automatic backward main-kernel choice, 1: one CTA per key tile, 2: persistent."""
+    _check(load().sdpa_set_backward_variant(int(variant)))
+
+
+def sdpa_last_backward_variant() -> int:
+    """Main kernel of this thread's last backward call: 1 one CTA per key tile, 2 persistent."""
+    return int(load().sdpa_last_backward_variant())
+
+
+def sdpa_set_backward_grid_limit(max_ctas: int) -> None:
+    """Most CTAs of the persistent backward kernel on this thread (0: one per SM)."""
+    _check(load().sdpa_set_backward_grid_limit(int(max_ctas)))
 
 
 def sdpa_version() -> str:

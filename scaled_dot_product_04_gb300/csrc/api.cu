@@ -3,6 +3,7 @@
 // synchronises the host (except sdpa_check_device_error, which exists to do
 // exactly that).  Declarations and the contract live in include/sdpa.h.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -22,10 +23,17 @@ namespace {
 // device: (kernel tag << 16) | wait site.  Read and cleared by
 // sdpa_check_device_error.
 __device__ uint32_t g_error_word;
+// Unit counters of the persistent backward kernel, one per call in flight: a
+// call takes the next slot, its preprocess kernel zeroes it and its main
+// kernel's CTAs take units from it.
+constexpr int kUnitCounterSlots = 1024;
+__device__ uint32_t g_unit_counters[kUnitCounterSlots];
+std::atomic<uint32_t> g_unit_counter_next{0};
 
 thread_local std::string t_last_error;
 thread_local KernelTimer t_timer;
 thread_local int t_fwd_variant = 0;  // 0 auto, 1 one-tile, 2 two-tile
+thread_local int t_bwd_variant = 0;  // 0 auto, 1 one CTA per key tile, 2 persistent
 
 // K + V bytes above which the one-tile forward orders its units slice group by
 // slice group: with the latest-tile-first order over all slices, the units in
@@ -66,6 +74,7 @@ struct DeviceState {
     bool ready = false;
     int sm_count = 0;
     uint32_t *err = nullptr;
+    uint32_t *unit_counters = nullptr;  // kUnitCounterSlots
 };
 std::mutex g_dev_mutex;
 DeviceState g_dev[kMaxDevices];
@@ -92,6 +101,10 @@ int device_state(DeviceState **out) {
         if (e != cudaSuccess)
             return fail(SDPA_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
         s.err = static_cast<uint32_t *>(addr);
+        e = cudaGetSymbolAddress(&addr, g_unit_counters);
+        if (e != cudaSuccess)
+            return fail(SDPA_ERR_CUDA, "cudaGetSymbolAddress(unit counters): %s", cudaGetErrorString(e));
+        s.unit_counters = static_cast<uint32_t *>(addr);
         s.ready = true;
     }
     *out = &s;
@@ -261,6 +274,46 @@ constexpr float kLog2e = 1.4426950408889634f;
 // set (dQ accumulator, Q, dO, K, V) below which one group holds every slice.
 constexpr int kBwdSliceGroup = 4;
 constexpr size_t kBwdOneGroupBytes = size_t(64) << 20;
+// Mean (query head, query tile) pairs per unit up to which the backward takes
+// the persistent kernel, whose tiles run a few percent slower than the
+// one-CTA-per-unit kernel's but whose units cost less to start and end: in
+// measured sweeps it was ahead for dense problems up to a mean of 8 (by 3-13
+// %), even at 8.5-16 and behind beyond, and for packed lists up to a mean of
+// about 2 (by 35-105 %: short sequences), behind from 4 (by 5-7 %).
+constexpr double kPersistMaxMeanTilesDense = 8.0;
+constexpr double kPersistMaxMeanTilesPacked = 3.0;
+thread_local int t_bwd_used = 0;  // main kernel of this thread's last backward
+thread_local int t_bwd_grid_limit = 0;  // most CTAs of the persistent kernel, 0 = one per SM
+
+// Query tiles that see key tile kt of a sequence (the backward's unit length
+// per query head, as the main kernels count it).
+int64_t unit_query_tiles(int mask, int window, int Lq, int Lkv, int kt) {
+    const int delta = mask == SDPA_MASK_CAUSAL_BOTTOM_RIGHT ? Lkv - Lq : 0;
+    const int k0 = kt * kTileN;
+    const int k_last = std::min(k0 + kTileN, Lkv) - 1;
+    const int row_lo = mask != SDPA_MASK_NONE ? std::max(0, k0 - delta) : 0;
+    const int row_hi = window >= 0 ? std::min(Lq, k_last - delta + window + 1) : Lq;
+    if (row_hi <= row_lo) return 0;
+    return (row_hi + kTileM - 1) / kTileM - row_lo / kTileM;
+}
+
+// Main-kernel form of a backward call (sets p.persist, p.grid, p.unit_ctr).
+// units: length of the unit list (an upper bound for packed inputs);
+// short_units: the units are short enough for the persistent kernel;
+// fits: the persistent kernel can take this problem.
+void choose_bwd_kernel(BwdParams &p, const DeviceState &dev, int64_t units, bool short_units, bool fits) {
+    const bool persist = fits && units > 0 && (t_bwd_variant == 2 || (t_bwd_variant == 0 && short_units));
+    p.persist = persist ? 1 : 0;
+    if (persist) {
+        const int ctas = t_bwd_grid_limit > 0 ? std::min(t_bwd_grid_limit, dev.sm_count) : dev.sm_count;
+        p.grid = (int)std::min<int64_t>(units, ctas);
+        p.unit_ctr = dev.unit_counters + (g_unit_counter_next.fetch_add(1) % kUnitCounterSlots);
+    } else {
+        p.grid = (int)units;
+        p.unit_ctr = nullptr;
+    }
+    t_bwd_used = persist ? 2 : 1;
+}
 
 int launch_status(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return ok();
@@ -304,12 +357,28 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.13 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.14 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)
         return fail(SDPA_ERR_INVALID_ARG, "forward variant %d (0 auto, 1 one-tile, 2 two-tile)", variant);
     t_fwd_variant = variant;
+    return ok();
+}
+
+int sdpa_set_backward_variant(int variant) {
+    if (variant < 0 || variant > 2)
+        return fail(SDPA_ERR_INVALID_ARG, "backward variant %d (0 auto, 1 one CTA per key tile, 2 persistent)",
+                    variant);
+    t_bwd_variant = variant;
+    return ok();
+}
+
+int sdpa_last_backward_variant(void) { return t_bwd_used; }
+
+int sdpa_set_backward_grid_limit(int max_ctas) {
+    if (max_ctas < 0) return fail(SDPA_ERR_INVALID_ARG, "backward grid limit %d (0 = one CTA per SM)", max_ctas);
+    t_bwd_grid_limit = max_ctas;
     return ok();
 }
 
@@ -771,7 +840,10 @@ int sdpa_bwd_ex(const void *q, const void *k, const void *v, const void *o, cons
     const size_t working = (size_t)bh * s_q * d * 4 + 2 * qbytes + 2 * kvbytes;
     p.slice_group = working <= kBwdOneGroupBytes ? (int)bh_kv : kBwdSliceGroup;
     p.seq_table = 0;
-    p.grid = (int)(kv_tiles * bh_kv);
+    int64_t tiles = 0;
+    for (int kt = 0; kt < kv_tiles; ++kt) tiles += unit_query_tiles(mask, window_left, s_q, s_kv, kt);
+    const double mean_tiles = kv_tiles > 0 ? (double)tiles * p.group / kv_tiles : 0.0;
+    choose_bwd_kernel(p, *dev, kv_tiles * bh_kv, mean_tiles <= kPersistMaxMeanTilesDense, true);
     return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, false, cs, t_timer), "sdpa_bwd");
 }
 
@@ -878,7 +950,18 @@ int sdpa_varlen_bwd_ex(const void *q, const void *k, const void *v, const void *
     const int64_t tiles = p.seq_table ? std::min<int64_t>((int64_t)num_seqs * kv_tiles,
                                                           total_kv / kTileN + num_seqs)
                                       : (int64_t)num_seqs * kv_tiles;
-    p.grid = (int)(tiles * h_kv);
+    // The persistent kernel (lists of up to kPersistSeqMax sequences) for
+    // short sequences.  The lengths stay on the device, so the mean unit
+    // length is estimated from the mean sequence length: a sequence of L
+    // keys has ceil(L / 128) key tiles, about L / 128 + 1/2, and under a
+    // causal mask its key tiles see (tiles + 1) / 2 query tiles on average;
+    // a window bounds that by its own width.
+    const double seq_tiles = (double)total_kv / num_seqs / kTileN + 0.5;
+    double mean_tiles = mask != SDPA_MASK_NONE ? (seq_tiles + 1.0) / 2.0 : seq_tiles;
+    if (window_left >= 0) mean_tiles = std::min(mean_tiles, (double)window_left / kTileM + 2.0);
+    mean_tiles *= p.group;
+    choose_bwd_kernel(p, *dev, tiles * h_kv, mean_tiles <= kPersistMaxMeanTilesPacked,
+                      num_seqs <= kPersistSeqMax);
     return launch_status(launch_bwd(tq, tk, tv, tdo, tdq, trx, p, d, bf16, true, cs, t_timer), "sdpa_varlen_bwd");
 }
 

@@ -36,6 +36,7 @@
 // latencies one warp alone leaves exposed).  The MMA warp issues dQ before dK:
 // dQ shares its TMEM columns with dP at d = 128, and the dQ epilogue's read-out
 // then overlaps dK, so dP of the next tile follows without a gap.
+#include "bwd_layout.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -46,21 +47,7 @@ namespace {
 // then exact in fp32 and is the low part of the pair).
 SDPA_DEV float tf32_hi(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
 
-SDPA_DEV bool warp_wait_b(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
-    bool ok = mbar_wait_lean(bar, parity, w, site);
-    return __all_sync(0xffffffffu, ok);
-}
 
-// -------------------------------------------------------------------- layouts
-// Row r of a problem slice in the I/O tensors and in the fp32 buffers:
-//   dense  : I/O element offset (slice*S + r)*d, row-term index slice*S + r
-//   packed : I/O element offset ((tok0 + r)*h + head)*d, row terms (tok0 + r)*h + head
-// The dQ accumulator is head-major in both cases: [slices or heads][rows][d],
-// so a query tile of one head is contiguous.
-struct RowMap {
-    int64_t io0, io_rs;      // I/O tensors (elements)
-    int64_t acc0;            // dQ accumulator row 0 (elements, row stride d)
-};
 
 // ------------------------------------------------------------------ preprocess
 // One warp handles 32/(d/8) rows at a time; each lane reads 8 elements of O
@@ -112,6 +99,7 @@ __global__ void __launch_bounds__(256)
             p.rowx[r] = t;
         }
     }
+    if (p.unit_ctr && blockIdx.x == 0 && threadIdx.x == 0) *p.unit_ctr = 0u;
     // zero the fp32 dQ accumulator
     float4 *acc4 = reinterpret_cast<float4 *>(p.dq_acc);
     const int64_t n4 = acc_elems / 4;
@@ -152,58 +140,6 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BwdParams p, 
 }
 
 // ------------------------------------------------------------------ main
-template <int D>
-struct BwdLayout {
-    static constexpr int kChunks = D / 64;
-    static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 128 bytes
-    static constexpr int kTileBytes = kChunks * kChunkBytes;
-    static constexpr int kK = 0;
-    static constexpr int kV = kK + kTileBytes;
-    // dO is read by dP^T_i and dV_i only, and dO_{i+1} is not needed before
-    // dP^T_{i+1}, so one buffer suffices at d = 128 and frees room for the
-    // dQ staging boxes.
-    static constexpr int kDOStages = (D == 128) ? 1 : 2;
-    static constexpr int kQ = kV + kTileBytes;               // 2 stages
-    static constexpr int kDO = kQ + 2 * kTileBytes;          // kDOStages stages
-    static constexpr int kDS = kDO + kDOStages * kTileBytes; // 128 keys x 128 queries bf16
-    static constexpr int kDQBoxBytes = 32 * 16 * 4;           // 32 rows x 16 fp32
-    static constexpr int kDQSlots = 3;                        // staging boxes per warp
-    static constexpr int kDQStage = kDS + 2 * kChunkBytes;   // 4 warps x kDQSlots boxes
-    static constexpr int kRowXBytes = 128 * 16;               // 128 query rows x 4 fp32
-    static constexpr int kRowX = kDQStage + 4 * kDQSlots * kDQBoxBytes;  // 2 stages, with Q
-    static constexpr int kAexS = kRowX + 2 * kRowXBytes;      // 128 rows (0.5, 0.5, 0, 0)
-    static constexpr int kAexD = kAexS + kRowXBytes;          // 128 rows (0, 0, 0.5, 0.5)
-    static constexpr int kBar = kAexD + kRowXBytes;
-    // barriers
-    static constexpr int bKVFull = 0;
-    static constexpr int bQFull = 1;       // 2: Q and its row terms
-    static constexpr int bDOFull = 3;      // 2
-    static constexpr int bQEmpty = 7;      // 2: Q (and row terms) stage, freed after dK
-    static constexpr int bDOEmpty = 18;    // kDOStages: dO stage, freed after dV
-    static constexpr int bSFull = 9;
-    static constexpr int bDPFull = 10;
-    static constexpr int bPReady = 11;
-    static constexpr int bDSReady = 12;
-    static constexpr int bDVDone = 13;
-    static constexpr int bDQFull = 14;
-    static constexpr int bDQFree = 15;
-    static constexpr int bDSFree = 16;
-    static constexpr int bMmaIdle = 17;
-    static constexpr int kNumBars = 20;
-    static constexpr int kMisc = kBar + kNumBars * 8;
-    static constexpr int kBytes = kMisc + 16;
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColDV = 0;
-    static constexpr uint32_t kColDK = D;
-    static constexpr uint32_t kColS = 2 * D;
-    static constexpr uint32_t kColDP = 2 * D + 128;
-    static constexpr bool kDQAliasDP = (D == 128);  // no spare columns at d = 128
-    static constexpr uint32_t kColDQ = kDQAliasDP ? kColDP : 2 * D + 256;
-};
-
-// warps: 0 TMA, 1 MMA, 2-5 compute (queries 0-63 of a tile), 6-9 compute
-// (queries 64-127), 10-13 dQ epilogue
-constexpr int kBwdThreads = 448;
 
 template <int D, bool kBf16, bool kPacked>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -727,30 +663,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(L::bDSReady));
         }
-        // dK, dV epilogue: group 0 writes dV, group 1 dK
+        // dK, dV epilogue: group 0 writes dV, group 1 dK, each warp its 32
+        // key rows, staged in its rows of the dS tile (every product is done)
         if (ok) ok = warp_wait_b(bar(L::bMmaIdle), 0, wc, 16);
         if (ok) {
             tc_fence_after();
             const uint32_t col = grp == 0 ? L::kColDV : L::kColDK;
-            uint16_t *dst_row = static_cast<uint16_t *>(grp == 0 ? p.dv : p.dk) + km.io0 +
-                                (int64_t)key * km.io_rs;
+            const int key0 = k0 + quad * 32;  // the warp's first key
+            uint16_t *row0 = static_cast<uint16_t *>(grp == 0 ? p.dv : p.dk) + km.io0 + (int64_t)key0 * km.io_rs;
             const float f = grp == 0 ? 1.f : p.scale;  // dK = scale * sum dS'^T Q
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(t_lane + col + c * 32, r);
-                tmem_ld_wait_regs<32>(r);
-                if (key_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c * 32);
-                    auto g = [&](int e) { return __uint_as_float(r[e]) * f; };
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pack2<kBf16>(g(8 * v), g(8 * v + 1)),
-                                            pack2<kBf16>(g(8 * v + 2), g(8 * v + 3)),
-                                            pack2<kBf16>(g(8 * v + 4), g(8 * v + 5)),
-                                            pack2<kBf16>(g(8 * v + 6), g(8 * v + 7)));
-                }
-            }
+            store_tile_rows<D, kBf16>(t_lane + col, ds_row - lane * 128, lane, row0, km.io_rs,
+                                      min(32, Lkv - key0), f, [] {});
         }
     } else {
         // ============================================================ dQ epilogue
@@ -857,11 +780,15 @@ cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = bwd_main_kernel<D, kBf16, kPacked>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    if (e != cudaSuccess) return e;
+    if (!p.persist) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        if (e != cudaSuccess) return e;
+    }
     const int grid = p.grid;  // 0 when no sequence has a key: dK, dV are empty then
     if (timer.start) cudaEventRecord(timer.start, stream);
-    if (grid > 0)
+    if (grid > 0 && p.persist)
+        e = launch_bwd_persist(tq, tk, tv, tdo, tdq, trx, p, D, kBf16, kPacked, stream);
+    else if (grid > 0)
         e = launch_overlapped(kern, dim3(grid), dim3(kBwdThreads), L::kBytes, stream, tq, tk, tv, tdo,
                               tdq, trx, p);
     if (p.deterministic) {

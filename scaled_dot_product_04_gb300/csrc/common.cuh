@@ -101,10 +101,16 @@ struct BwdParams {
     int seq_table;               // packed: 1 = compact grid over a per-CTA table of the
                                  // sequences (longest first), 0 = envelope grid
     int grid;                    // main kernel CTAs
+    int persist;                 // 1: persistent main kernel (bwd_persist.cu), units taken
+                                 // from *unit_ctr, which the preprocess kernel zeroes
+    uint32_t *unit_ctr;
 };
 // Largest sequence count of the packed backward's per-CTA sequence table (it
 // is built in the dS tile's shared memory before that is used).
 constexpr int kBwdSeqTableMax = 1024;
+// Largest sequence count of the persistent backward's packed unit table (in
+// shared memory beside the kernel's operand tiles).
+constexpr int kPersistSeqMax = 128;
 
 // Failure-detection self-test (selftest.cu): one CTA waits, with the bounded
 // wait of every kernel and the given limit, on a barrier phase that nothing
@@ -172,6 +178,11 @@ cudaError_t launch_bwd_dq(const CUtensorMap &tq, const CUtensorMap &tk, const CU
                           bool packed, bool overlap, cudaStream_t stream);
 // tdq: 2-D fp32 map over the dQ accumulator [rows][d], box 16 x 32, 64-byte swizzle.
 // trx: map over the row terms (dense [b*h][s_q][4], packed [T][h][4] fp32), 128-row boxes.
+// Persistent main kernel alone (p.grid CTAs, p.unit_ctr zeroed by the kernel
+// ahead of it on `stream`, which must signal its dependents).
+cudaError_t launch_bwd_persist(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &trx,
+                               const BwdParams &p, int d, bool bf16, bool packed, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const CUtensorMap &tdq, const CUtensorMap &trx,
                        const BwdParams &p, int d, bool bf16, bool packed, cudaStream_t stream,

@@ -153,6 +153,15 @@ SDPA_DEV void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int 
         : "memory");
 }
 
+// Fetch a tile into L2 only (no shared memory, no barrier), so that a later
+// load of the same box hits L2.
+SDPA_DEV void tma_prefetch_l2_3d(const CUtensorMap *m, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Element-wise add of a shared-memory box into global memory through a 2-D
 // tensor map (out-of-bounds parts of the box are dropped), tracked as a bulk
 // async-group of the issuing thread.

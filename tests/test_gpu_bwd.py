@@ -15,7 +15,8 @@ import oracle
 import sdpa_inputs
 from helpers import GRAD_TOL, check_rel, np64
 
-pytestmark = pytest.mark.gpu
+# every test here runs on each backward main kernel (tests/conftest.py)
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("bwd_variant")]
 
 
 @pytest.fixture(scope="module")

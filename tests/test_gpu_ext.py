@@ -75,6 +75,7 @@ def test_ext_dense_fwd(sdpa, variant, case):
     check_lse(lse, rlse)
 
 
+@pytest.mark.usefixtures("bwd_variant")
 @pytest.mark.parametrize("case", DENSE_CASES, ids=lambda c: f"b{c[0]}h{c[1]}kv{c[2]}s{c[3]}x{c[4]}d{c[5]}_{c[6]}_w{c[7]}")
 def test_ext_dense_bwd(sdpa, case):
     b, h, h_kv, s_q, s_kv, d, mask, window = case
@@ -129,6 +130,7 @@ def test_ext_packed_fwd(sdpa, variant, case):
             check_rel(o[s], ro[s], O_TOL[torch.bfloat16], f"o seq {n}")
 
 
+@pytest.mark.usefixtures("bwd_variant")
 @pytest.mark.parametrize("case", PACKED_CASES, ids=lambda c: f"n{len(c[0])}h{c[2]}kv{c[3]}d{c[4]}_{c[5]}_w{c[6]}")
 def test_ext_packed_bwd(sdpa, case):
     lq, lk, h, h_kv, d, mask, window = case
@@ -138,6 +140,7 @@ def test_ext_packed_bwd(sdpa, case):
     _grads_ok(got, ref)
 
 
+@pytest.mark.usefixtures("bwd_variant")
 def test_ext_fp16_gqa_window(sdpa, variant):
     b, h, h_kv, s, d = 1, 4, 2, 500, 128
     q, k, v, do = sdpa_inputs.dense(b, h, s, s, d, seed=77, dtype=torch.float16, h_kv=h_kv)
@@ -202,6 +205,7 @@ DET_DENSE = [
 ]
 
 
+@pytest.mark.usefixtures("bwd_variant")
 @pytest.mark.parametrize("case", DET_DENSE, ids=lambda c: f"b{c[0]}h{c[1]}kv{c[2]}s{c[3]}x{c[4]}d{c[5]}_{c[6]}_w{c[7]}")
 def test_deterministic_dense_bwd_parity_and_bits(sdpa, case):
     b, h, h_kv, s_q, s_kv, d, mask, window = case
@@ -222,6 +226,7 @@ def test_deterministic_dense_bwd_parity_and_bits(sdpa, case):
     check_rel(runs[0][0], plain[0].double().cpu().numpy(), 1e-2, "dq vs default")
 
 
+@pytest.mark.usefixtures("bwd_variant")
 @pytest.mark.parametrize("case", PACKED_CASES[:4], ids=lambda c: f"n{len(c[0])}h{c[2]}kv{c[3]}d{c[4]}_{c[5]}_w{c[6]}")
 def test_deterministic_packed_bwd(sdpa, case):
     lq, lk, h, h_kv, d, mask, window = case
@@ -239,6 +244,7 @@ def test_deterministic_packed_bwd(sdpa, case):
     _grads_ok(runs[0], oracle.sdpa_varlen_bwd_ex(q, k, v, do, cu_q, cu_kv, scale, mask, window))
 
 
+@pytest.mark.usefixtures("bwd_variant")
 def test_deterministic_packed_bwd_without_keys_or_with_unseen_key_tiles(sdpa):
     """The deterministic dQ pass starts while the main kernel runs and reads
     the preprocess kernel's row terms without waiting itself: here every main

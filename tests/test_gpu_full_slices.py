@@ -100,6 +100,7 @@ def test_full_size_dense_fwd_whole_slices(sdpa, name, variant):
         check_lse(lse[bb, hh], r_lse, f"lse[{bb},{hh}]")
 
 
+@pytest.mark.usefixtures("bwd_kernel")
 @pytest.mark.parametrize("name", [C3, C5])
 def test_full_size_dense_bwd_whole_slices(sdpa, name):
     o, lse, dq, dk, dv = _dense_run(sdpa, name, 0, backward=True)
@@ -130,6 +131,7 @@ def test_full_size_packed_fwd_every_sequence(sdpa, variant):
         check_lse(lse[:, hh], r_lse, f"lse head {hh}")
 
 
+@pytest.mark.usefixtures("bwd_kernel")
 def test_full_size_packed_bwd_every_sequence(sdpa):
     o, lse, dq, dk, dv = _packed_run(sdpa, 0, backward=True)
     _finite(o, lse, dq, dk, dv)

@@ -39,6 +39,7 @@ def _rows(n, seed):
     return np.array(sorted(r for r in base if 0 <= r < n), np.int32)
 
 
+@pytest.mark.usefixtures("bwd_kernel")
 def test_full_size_deterministic_bwd_whole_heads_and_bitwise(sdpa):
     w = sdpa_inputs.WORKLOADS[NAME]
     t = oracle_refs.inputs(NAME)
