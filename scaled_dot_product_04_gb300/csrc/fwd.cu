@@ -546,22 +546,16 @@ __global__ void __launch_bounds__(192, 1)
                     for (int i = 0; i < 8; ++i)
                         pk[i] = pack_e4m3x4(__uint_as_float(o[4 * i]) * so, __uint_as_float(o[4 * i + 1]) * so,
                                             __uint_as_float(o[4 * i + 2]) * so, __uint_as_float(o[4 * i + 3]) * so);
-                    if (pend.row_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(pend.orow + c * 32 * kOb);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    }
+                    if (pend.row_ok) st_global_32b(pend.orow + c * 32 * kOb, pk);
                 } else {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         pk[i] = pack2<kOut == kElBf16>(__uint_as_float(o[2 * i]) * inv_l,
                                                        __uint_as_float(o[2 * i + 1]) * inv_l);
-                    if (pend.row_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(pend.orow + c * 32 * kOb);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    if (pend.row_ok) {  // whole 32-byte sectors
+                        st_global_32b(pend.orow + c * 32 * kOb, pk);
+                        st_global_32b(pend.orow + c * 32 * kOb + 32, pk + 8);
                     }
                 }
             }

@@ -162,6 +162,25 @@ SDPA_DEV void tma_prefetch_l2_3d(const CUtensorMap *m, int c0, int c1, int c2) {
                  : "memory");
 }
 
+// One 32-byte global store (a whole sector); the address must be 32-byte
+// aligned.
+SDPA_DEV void st_global_v8(void *p, const uint32_t *v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+// 32 bytes at p (16-byte aligned): one sector store when p is 32-byte
+// aligned, two 16-byte stores otherwise.
+SDPA_DEV void st_global_32b(uint8_t *p, const uint32_t *v) {
+    if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+        st_global_v8(p, v);
+    } else {
+        uint4 *d = reinterpret_cast<uint4 *>(p);
+        d[0] = make_uint4(v[0], v[1], v[2], v[3]);
+        d[1] = make_uint4(v[4], v[5], v[6], v[7]);
+    }
+}
+
 // Element-wise add of a shared-memory box into global memory through a 2-D
 // tensor map (out-of-bounds parts of the box are dropped), tracked as a bulk
 // async-group of the issuing thread.
