@@ -315,6 +315,17 @@ void choose_bwd_kernel(BwdParams &p, const DeviceState &dev, int64_t units, bool
     t_bwd_used = persist ? 2 : 1;
 }
 
+// Dense two-tile lists of equal units (no mask, no window) whose count leaves
+// a partial last wave on the grid: those last units are cut into two 128-row
+// units each (their count is added to FwdParams::n_units) when their halves
+// fill at most one wave, so the launch ends about half a unit earlier.  Under a causal mask or a window
+// the list runs heaviest first and its last units are already short.
+int pair_tail_split(int units, int grid, int mask, int window) {
+    if (mask != SDPA_MASK_NONE || window >= 0 || units <= grid) return 0;
+    const int rest = units % grid;
+    return (rest > 0 && 2 * rest <= grid) ? rest : 0;
+}
+
 int launch_status(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return ok();
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
@@ -357,7 +368,7 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.15 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.16 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)
@@ -460,8 +471,9 @@ int sdpa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     auto launch = [&](bool two) {
         const int rows = two ? fwd_pair_rows() : kTileM;
         p.q_tiles = (s_q + rows - 1) / rows;
-        p.n_units = (int)(p.q_tiles * bh);
-        const int grid = std::min(p.n_units, dev->sm_count);
+        const int units = (int)(p.q_tiles * bh);
+        const int grid = std::min(units, dev->sm_count);
+        p.n_units = units + (two ? pair_tail_split(units, grid, mask, window_left) : 0);
         return two ? launch_fwd_pair(tq, tk, tv, p, d, bf16, false, grid, cs, t_timer)
                    : launch_fwd(tq, tk, tv, p, d, bf16, false, grid, slice_major, cs, t_timer);
     };
@@ -639,8 +651,9 @@ int sdpa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
     auto launch = [&](bool two) {
         const int rows = two ? fwd_pair_rows() : kTileM;
         p.q_tiles = (s_q + rows - 1) / rows;
-        p.n_units = (int)(p.q_tiles * bh);
-        const int grid = std::min(p.n_units, dev->sm_count);
+        const int units = (int)(p.q_tiles * bh);
+        const int grid = std::min(units, dev->sm_count);
+        p.n_units = units + (two ? pair_tail_split(units, grid, mask, window_left) : 0);
         return two ? launch_fwd_pair_fp8(tq, tk, tv, p, out_dtype, false, grid, cs, t_timer)
                    : launch_fwd_fp8(tq, tk, tv, p, out_dtype, false, grid, slice_major, cs, t_timer);
     };

@@ -48,7 +48,8 @@ struct FwdParams {
     int num_seqs;                // packed
     int q_tiles;                 // row blocks per slice (128 rows, or 256 for the
                                  // two-tile kernel): dense from s_q, packed from max_seqlen_q
-    int n_units;                 // q_tiles * bh (units a persistent CTA may visit)
+    int n_units;                 // units a persistent CTA may visit: q_tiles * bh (dense two-tile
+                                 // lists with a cut tail: plus the number of cut 256-row units)
     int mask;                    // MaskKind
     int window;                  // window_left, -1 for none
     float scale_log2;            // attn_scale * log2(e)

@@ -111,6 +111,7 @@ struct PairUnit {
     int kt0;       // kWin: first key tile of the walk (else 0)
     int first[2];  // kWin: first walk step of tile A / B (else 0)
     bool live;    // tile A holds at least one query row
+    bool single;  // a 128-row unit: tile B takes no part
     int64_t o_row0, o_rs, lse_row0, lse_rs;
 };
 
@@ -119,7 +120,15 @@ struct PairUnit {
 // longest first: sequence order[i] owns units [first_unit[i], first_unit[i+1]),
 // its 256-row blocks latest first with the heads innermost, so the CTAs in
 // flight share one or two sequences' K and V in L2.
-template <int D, bool kPacked, bool kWin>
+//
+// Dense lists of equal units whose count leaves a partial last wave end with
+// n_split = p.n_units - p.q_tiles * p.bh of their 256-row blocks cut in two:
+// the host sizes the list so that the blocks before them fill whole waves of
+// the grid and the 2 n_split 128-row units of the cut blocks take at most one
+// more wave, each about half a block's time, where the uncut blocks would
+// have taken a whole one.  Only the kSplit instantiations decode such a list,
+// so the others compile as they did without it.
+template <int D, bool kPacked, bool kWin, bool kSplit = false>
 SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const int *cu_kv,
                               const int *order, const int *first_unit) {
     PairUnit U;
@@ -140,8 +149,18 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
             U.slice = u % p.bh;
         }
     } else {
+        int half = -1;  // a cut block: which 128-row half
+        if constexpr (kSplit) {
+            const int split_from = 2 * p.q_tiles * p.bh - p.n_units;  // blocks - cut blocks
+            if (u >= split_from) {
+                half = (u - split_from) & 1;
+                u = split_from + ((u - split_from) >> 1);
+            }
+        }
         qp = p.q_tiles - 1 - u / p.bh;  // latest (heaviest) rows first
         U.slice = u % p.bh;
+        U.single = half >= 0;
+        U.row0 = qp * kPairRows + (half > 0 ? kTileM : 0);
     }
     if constexpr (!kPacked) {
         U.head = 0;
@@ -168,7 +187,10 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
         U.lse_row0 = (int64_t)U.tok_q0 * p.h + U.head;
         U.lse_rs = p.h;
     }
-    U.row0 = qp * kPairRows;
+    if constexpr (kPacked) {
+        U.single = false;
+        U.row0 = qp * kPairRows;
+    }
     U.live = U.row0 < U.Lq;
     U.delta = mask_delta(p.mask, U.Lq, U.Lkv);
     U.kt0 = 0;
@@ -178,7 +200,7 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
         for (int x = 0; x < 2; ++x) {
             const int r0 = U.row0 + x * kTileM;
             int n = 0;
-            if (r0 < U.Lq) {
+            if (r0 < U.Lq && !(kSplit && x == 1 && U.single)) {
                 const int hi = key_range(p.mask, p.window, min(r0 + kTileM, U.Lq) - 1, U.delta, U.Lkv).hi;
                 n = hi > 0 ? (hi + kTileN - 1) / kTileN : 0;
             }
@@ -193,7 +215,7 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
         for (int x = 0; x < 2; ++x) {
             const int r0 = U.row0 + x * kTileM;
             f[x] = e[x] = 0;
-            if (r0 < U.Lq) {
+            if (r0 < U.Lq && !(kSplit && x == 1 && U.single)) {
                 const int lo = max(0, key_range(p.mask, p.window, r0, U.delta, U.Lkv).lo);
                 const int hi = key_range(p.mask, p.window, min(r0 + kTileM, U.Lq) - 1, U.delta, U.Lkv).hi;
                 if (hi > lo) {
@@ -215,7 +237,7 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
 
 // kEl / kOut: input and output element kinds as in fwd.cu (E4M3 inputs with
 // device descales, P as E4M3 quads, kind::f8f6f4 products; amax of O).
-template <int D, int kEl, bool kPacked, int kOut, bool kWin>
+template <int D, int kEl, bool kPacked, int kOut, bool kWin, bool kSplit = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -360,7 +382,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int u = unit_of(k, first, step);
                     if (u >= n_units) break;
-                    const PairUnit U = decode_pair<D, kPacked, kWin>(p, u, cu_q, cu_kv, order, first_s);
+                    const PairUnit U = decode_pair<D, kPacked, kWin, kSplit>(p, u, cu_q, cu_kv, order, first_s);
                     const int nmax = max(U.n_kv[0], U.n_kv[1]);
                     if (nmax == 0) continue;
                     // the previous unit's last V goes out before waiting for Q's slot
@@ -458,7 +480,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 for (int k = 0; ok; ++k) {
                     const int u = unit_of(k, first, step);
                     if (u >= n_units) break;
-                    const PairUnit U = decode_pair<D, kPacked, kWin>(p, u, cu_q, cu_kv, order, first_s);
+                    const PairUnit U = decode_pair<D, kPacked, kWin, kSplit>(p, u, cu_q, cu_kv, order, first_s);
                     const int nmax = max(U.n_kv[0], U.n_kv[1]);
                     if (nmax == 0) continue;
                     ok = mbar_wait(bar(L::bQFull), units & 1, wc, 4) &&
@@ -559,9 +581,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int k = 0; ok; ++k) {
             const int u = unit_of(k, first, step);
             if (u >= n_units) break;
-            const PairUnit U = decode_pair<D, kPacked, kWin>(p, u, cu_q, cu_kv, order, first_s);
+            const PairUnit U = decode_pair<D, kPacked, kWin, kSplit>(p, u, cu_q, cu_kv, order, first_s);
             const int row0 = U.row0 + x * kTileM;
-            if (!U.live || row0 >= U.Lq) continue;  // no row of this tile
+            if (!U.live || row0 >= U.Lq || (kSplit && x == 1 && U.single)) continue;  // no row of this tile
             const int q_idx = row0 + r;
             const bool row_ok = q_idx < U.Lq;
             uint8_t *orow = static_cast<uint8_t *>(p.o) + (U.o_row0 + (int64_t)q_idx * U.o_rs) * kOb;
@@ -743,12 +765,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 // launch register count of the last build launch_pair_t refused on this thread
 thread_local int t_refused_regs = 0;
 
-template <int D, int kEl, bool kPacked, int kOut, bool kWin = false>
+template <int D, int kEl, bool kPacked, int kOut, bool kWin = false, bool kSplit = false>
 cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const FwdParams &p, int grid, cudaStream_t stream,
                           const KernelTimer &timer) {
     using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2, kPacked>;
-    auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut, kWin>;
+    auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut, kWin, kSplit>;
     // The softmax warpgroups' setmaxnreg.inc waits for the registers warpgroup
     // 0 releases; a build launched with any other per-thread count than the
     // split assumes would leave it waiting, so such a build is not launched.
@@ -797,6 +819,16 @@ cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const 
         return packed ? launch_pair_t<128, kElFp16, true, kElFp16, true>(tq, tk, tv, p, grid, stream, timer)
                       : launch_pair_t<128, kElFp16, false, kElFp16, true>(tq, tk, tv, p, grid, stream, timer);
     }
+    // dense lists with a cut tail (more units than blocks)
+    if (!packed && p.n_units > p.q_tiles * p.bh) {
+        if (d == 64)
+            return bf16 ? launch_pair_t<64, kElBf16, false, kElBf16, false, true>(tq, tk, tv, p, grid, stream, timer)
+                        : launch_pair_t<64, kElFp16, false, kElFp16, false, true>(tq, tk, tv, p, grid, stream, timer);
+        if (d == 128)
+            return bf16 ? launch_pair_t<128, kElBf16, false, kElBf16, false, true>(tq, tk, tv, p, grid, stream, timer)
+                        : launch_pair_t<128, kElFp16, false, kElFp16, false, true>(tq, tk, tv, p, grid, stream, timer);
+        return cudaErrorInvalidValue;
+    }
 #define SDPA_PAIR_CASE(D_, EL_, PK_)                                           \
     if (d == D_ && (bf16 ? kElBf16 : kElFp16) == EL_ && packed == PK_)         \
         return launch_pair_t<D_, EL_, PK_, EL_>(tq, tk, tv, p, grid, stream, timer);
@@ -816,6 +848,12 @@ cudaError_t launch_fwd_pair_fp8(const CUtensorMap &tq, const CUtensorMap &tk, co
                                 const FwdParams &p, int out, bool packed, int grid,
                                 cudaStream_t stream, const KernelTimer &timer) {
     if (p.window >= 0) return cudaErrorInvalidValue;  // the host keeps windows on the one-tile kernel
+    if (!packed && p.n_units > p.q_tiles * p.bh) {  // dense lists with a cut tail
+        if (out == kElBf16) return launch_pair_t<128, kElE4m3, false, kElBf16, false, true>(tq, tk, tv, p, grid, stream, timer);
+        if (out == kElFp16) return launch_pair_t<128, kElE4m3, false, kElFp16, false, true>(tq, tk, tv, p, grid, stream, timer);
+        if (out == kElE4m3) return launch_pair_t<128, kElE4m3, false, kElE4m3, false, true>(tq, tk, tv, p, grid, stream, timer);
+        return cudaErrorInvalidValue;
+    }
 #define SDPA_PAIR_FP8_CASE(OUT_, PK_)                                          \
     if (out == OUT_ && packed == PK_)                                          \
         return launch_pair_t<128, kElE4m3, PK_, OUT_>(tq, tk, tv, p, grid, stream, timer);
