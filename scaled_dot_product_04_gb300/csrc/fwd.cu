@@ -43,6 +43,8 @@
 // never the caller's capacity tail (cudnn-frontend PR #554, "clamp the f16
 // THD K/V descriptors to the packed total"); keys of the next sequence that
 // share a tile are masked to -inf before the exponent.
+#include <atomic>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -208,10 +210,37 @@ SDPA_DEV Unit decode_unit(const FwdParams &p, int u, const int *cu_q, const int 
 // (times scale_o for an E4M3 output) into the output factor; amax_o, if
 // given, receives max |O| of the real-valued output.  P enters P V as E4M3,
 // four per TMEM column; every product is a kind::f8f6f4 MMA of K = 32.
-template <int D, int kEl, bool kPacked, int kOut>
+// Units taken dynamically (kDyn): packed lists ordered sequence by sequence
+// (see packed_slot) are sawtooth-shaped -- each sequence's units go from
+// heaviest to lightest -- so a fixed deal of the list leaves some CTAs with
+// more work than others (a dispatch simulation of the 16-sequence workload:
+// makespan 370 tile steps against 352 dealt on demand).  The kDyn
+// instantiations take units from a counter instead, in the same list order
+// (which keeps each sequence's K and V in L2): the producer thread takes the
+// next unit when it has issued the current one's loads and hands it to the
+// MMA thread and the softmax warps through a ring of kUnitRing slots placed
+// after the layout.  `sched`: bit 0 selects the slice-major order; kDyn
+// launches carry their counter's slot (in g_fwd_unit_counters) + 1 above it.
+// The other instantiations read `sched` as the plain slice-major flag and
+// compile as before.
+constexpr int kUnitRing = 4;
+constexpr int kFwdCounterSlots = 1024;
+__device__ uint32_t g_fwd_unit_counters[kFwdCounterSlots];
+template <int D, int kEb>
+struct FwdDynLayout {
+    using L = FwdLayout<D, kEb>;
+    static constexpr int kRing = L::kBytes;                  // kUnitRing ints
+    static constexpr int kRingBar = kRing + 4 * kUnitRing;  // full, empty: kUnitRing each
+    static constexpr int kBytes = kRingBar + 2 * kUnitRing * 8;
+    static constexpr int kSmemAlloc = kBytes + 1024;
+};
+static_assert(FwdDynLayout<128, 2>::kSmemAlloc <= 232448, "dynamic one-tile forward exceeds shared memory");
+
+template <int D, int kEl, bool kPacked, int kOut, bool kDyn = false>
 __global__ void __launch_bounds__(192, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int slice_major) {
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p, const int sched) {
+    const int slice_major = kDyn ? (sched & 1) : sched;
     constexpr bool kFp8 = kEl == kElE4m3;
     constexpr bool kBf16 = kEl == kElBf16;
     constexpr int kEb = kFp8 ? 1 : 2;
@@ -225,6 +254,11 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
+    // kDyn: the unit ring, its barriers and this launch's counter
+    using DL = FwdDynLayout<D, kEb>;
+    auto dbar = [&](int i) -> uint32_t { return sbase + DL::kRingBar + 8u * i; };
+    volatile int *ring = reinterpret_cast<volatile int *>(smem + DL::kRing);
+    uint32_t *unit_ctr = kDyn ? g_fwd_unit_counters + ((sched >> 1) - 1) : nullptr;
 
     // cu_seqlens of packed inputs, cached when they fit, and then the
     // sequence-major unit list (see packed_slot)
@@ -317,6 +351,12 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(L::bOFree + b), kTileM);
         }
         mbar_init(bar(L::bMmaIdle), 1);
+        if constexpr (kDyn) {
+            for (int b = 0; b < kUnitRing; ++b) {
+                mbar_init(dbar(b), 1);              // full: the producer
+                mbar_init(dbar(kUnitRing + b), 5);  // empty: the MMA thread and 4 softmax warps
+            }
+        }
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -354,8 +394,21 @@ __global__ void __launch_bounds__(192, 1)
                 return true;
             };
             for (int k = 0; ok; ++k) {
-                const int u = unit_of(k, first, step);
-                if (u >= n_units) break;
+                int u;
+                if constexpr (kDyn) {
+                    // take the next unit (the first by the CTA's index) and hand it on
+                    const int slot = k % kUnitRing;
+                    if (k >= kUnitRing && !mbar_wait(dbar(kUnitRing + slot), ((k / kUnitRing) - 1) & 1, wc, 20))
+                        break;
+                    u = k == 0 ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(unit_ctr, 1u);
+                    if (u >= n_units) u = -1;
+                    ring[slot] = u;
+                    mbar_arrive(dbar(slot));
+                    if (u < 0) break;
+                } else {
+                    u = unit_of(k, first, step);
+                    if (u >= n_units) break;
+                }
                 const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
                 if (U.n_kv == 0) continue;
                 // the previous unit's last V goes out before waiting for Q's slot
@@ -461,8 +514,17 @@ __global__ void __launch_bounds__(192, 1)
             int t = 0;  // tiles processed by this CTA
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int u = unit_of(k, first, step);
-                if (u >= n_units) break;
+                int u;
+                if constexpr (kDyn) {
+                    const int slot = k % kUnitRing;
+                    if (!(ok = mbar_wait(dbar(slot), (k / kUnitRing) & 1, wc, 21))) break;
+                    u = ring[slot];
+                    mbar_arrive(dbar(kUnitRing + slot));
+                    if (u < 0) break;
+                } else {
+                    u = unit_of(k, first, step);
+                    if (u >= n_units) break;
+                }
                 const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
                 if (U.n_kv == 0) continue;
                 ok = mbar_wait(bar(L::bQFull + (units & 1)), (units >> 1) & 1, wc, 4) && issue_s_tile(t);
@@ -567,8 +629,18 @@ __global__ void __launch_bounds__(192, 1)
         int t = 0, units = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const int u = unit_of(k, first, step);
-            if (u >= n_units) break;
+            int u;
+            if constexpr (kDyn) {
+                const int slot = k % kUnitRing;
+                if (!(ok = warp_wait(dbar(slot), (k / kUnitRing) & 1, wc, 22))) break;
+                u = ring[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dbar(kUnitRing + slot));
+                if (u < 0) break;
+            } else {
+                u = unit_of(k, first, step);
+                if (u >= n_units) break;
+            }
             const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
             if (!U.live) continue;
             const int q_idx = U.row0 + r;
@@ -714,11 +786,35 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+std::atomic<uint32_t> g_fwd_counter_next{0};
+
 template <int D, int kEl, bool kPacked, int kOut>
 cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const FwdParams &p, int grid, bool slice_major, cudaStream_t stream,
                          const KernelTimer &timer) {
-    using L = FwdLayout<D, kEl == kElE4m3 ? 1 : 2>;
+    constexpr int kEb = kEl == kElE4m3 ? 1 : 2;
+    using L = FwdLayout<D, kEb>;
+    // packed lists in the sequence-major order (the kernel's sequence table)
+    // take their units dynamically
+    if constexpr (kPacked) {
+      if (slice_major && p.num_seqs + 1 <= L::kCuCap) {
+        using DL = FwdDynLayout<D, kEb>;
+        auto kern = fwd_kernel<D, kEl, kPacked, kOut, true>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DL::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        const int slot = (int)(g_fwd_counter_next.fetch_add(1) % kFwdCounterSlots);
+        void *ctr = nullptr;
+        e = cudaGetSymbolAddress(&ctr, g_fwd_unit_counters);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(static_cast<uint32_t *>(ctr) + slot, 0, sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return e;
+        if (timer.start) cudaEventRecord(timer.start, stream);
+        kern<<<grid, 192, DL::kSmemAlloc, stream>>>(tq, tk, tv, p, 1 | ((slot + 1) << 1));
+        e = cudaGetLastError();
+        if (timer.stop) cudaEventRecord(timer.stop, stream);
+        return e;
+      }
+    }
     auto kern = fwd_kernel<D, kEl, kPacked, kOut>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemAlloc);
