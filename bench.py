@@ -493,9 +493,9 @@ def run_ours(args):
                     free[st].record(d2h)
 
         # the first step's input copy and the last step's result copy cannot
-        # overlap any compute; 40 steps (more when more are timed, up to 60)
+        # overlap any compute; 100 steps (more when more are timed, up to 150)
         # spread that fill and drain thinly, as a caller's long loop would
-        n_e2e = max(40, min(args.steps, 60))
+        n_e2e = max(100, min(args.steps, 150))
         pipeline(2)
         torch.cuda.synchronize(dev)
         ev_a, ev_z = new_ev(), new_ev()
