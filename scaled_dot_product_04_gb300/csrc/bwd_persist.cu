@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             if (u < 0) break;
             const PUnit U = unit(u);
-            if (U.n_q == 0) continue;  // the compute warps write zeros
+            if (U.n_q == 0) continue;  // the dQ warps write zeros
             if (kv == 0) {
                 load_k(U);  // inputs only: no wait for the preprocess grid
                 load_v(U);
