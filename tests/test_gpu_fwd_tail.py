@@ -73,12 +73,15 @@ def test_split_tail_fp16_gqa(sdpa):
     check_lse(lse, rlse)
 
 
+def _sc(x):
+    return torch.tensor([x], dtype=torch.float32, device="cuda")
+
+
 def test_split_tail_fp8(sdpa):
     s, d = 1000, 128
     h = _heads(s)
     qc, kc, vc, dq, dk, dv = sdpa_inputs.fp8_dense(1, h, s, s, d, seed=9100)
-    sc = lambda x: torch.tensor([x], dtype=torch.float32, device="cuda")  # noqa: E731
-    o, lse, _ = sdpa.attention_fp8(qc.cuda(), kc.cuda(), vc.cuda(), sc(dq), sc(dk), sc(dv),
+    o, lse, _ = sdpa.attention_fp8(qc.cuda(), kc.cuda(), vc.cuda(), _sc(dq), _sc(dk), _sc(dv),
                                    scale=1.0 / math.sqrt(d), mask="none")
     torch.cuda.synchronize()
     ro, rlse = oracle.sdpa_fwd_fp8(qc, kc, vc, dq, dk, dv, 1.0 / math.sqrt(d), "none", -1)
@@ -87,3 +90,29 @@ def test_split_tail_fp8(sdpa):
     bound = 2.0 ** -4 * vmax + 2.0 ** -8 * float(np.abs(ro).max()) + 1e-6
     assert err <= bound, f"max|dO| {err:.3e} > bound {bound:.3e}"
     check_lse(lse, rlse)
+
+
+def test_split_tail_fp8_fp16_and_e4m3_outputs(sdpa):
+    """The other output kinds of the cut-tail FP8 instantiations: fp16 against
+    the oracle, E4M3 (O x scale_o) against the bf16 output of the same call."""
+    s, d = 770, 128
+    h = _heads(s)
+    qc, kc, vc, dq, dk, dv = sdpa_inputs.fp8_dense(1, h, s, s, d, seed=9101)
+    args = (qc.cuda(), kc.cuda(), vc.cuda(), _sc(dq), _sc(dk), _sc(dv))
+    scale = 1.0 / math.sqrt(d)
+    o16, _, amax16 = sdpa.attention_fp8(*args, scale=scale, mask="none")
+    oh, lseh, _ = sdpa.attention_fp8(*args, scale=scale, mask="none", out_dtype=torch.float16)
+    scale_o = 448.0 / float(amax16)
+    o8, lse8, amax8 = sdpa.attention_fp8(*args, scale=scale, mask="none",
+                                         out_dtype=torch.float8_e4m3fn, scale_o=_sc(scale_o))
+    torch.cuda.synchronize()
+    ro, rlse = oracle.sdpa_fwd_fp8(qc, kc, vc, dq, dk, dv, scale, "none", -1)
+    vmax = float(np.abs(oracle.e4m3_to_f64(vc, dv)).max())
+    bound = 2.0 ** -4 * vmax + 2.0 ** -11 * float(np.abs(ro).max()) + 1e-6
+    assert float(np.abs(np64(oh) - ro).max()) <= bound
+    check_lse(lseh, rlse)
+    assert float(amax8) == float(amax16)
+    dec = oracle.e4m3_to_f64(o8, 1.0 / scale_o)
+    ref = np64(o16)
+    assert np.all(np.abs(dec - ref) <= 2.0 ** -4 * np.abs(ref) * 1.01 + 2.0 ** -8 * np.abs(ref) + 2.0 ** -9 / scale_o)
+    check_lse(lse8, rlse)
