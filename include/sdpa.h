@@ -371,11 +371,13 @@ void sdpa_set_kernel_timer(void *start_event, void *stop_event);
  * Forward kernel choice for later calls on this host thread (a tuning and
  * testing hook; no counterpart on the pages).  0 (default): automatic -- the
  * two-tile kernel (256 query rows per work unit, two softmax warpgroups
- * ping-ponging on the tensor core) for problems whose query and key lengths
- * reach 1024 (dense) or whose mean sequence lengths total_q / num_seqs and
- * total_kv / num_seqs reach 2048 (packed), the one-tile kernel (128 rows per
- * unit) otherwise; FP8 inputs with a left window, and 16-bit inputs with a
- * left window at d = 64, always take the one-tile kernel.  1: always one-tile.
+ * ping-ponging on the tensor core) for dense problems whose query and key
+ * lengths reach 1024, for packed lists without a left window of up to 95
+ * sequences (d = 128, 16-bit inputs) or 1023 (d = 64 or FP8 inputs), and for
+ * longer packed lists whose mean sequence lengths total_q / num_seqs and
+ * total_kv / num_seqs reach 2048; the one-tile kernel (128 rows per unit)
+ * otherwise.  FP8 inputs with a left window, and 16-bit inputs with a left
+ * window at d = 64, always take the one-tile kernel.  1: always one-tile.
  * 2: the two-tile kernel wherever it applies.  Both compute the same result to
  * rounding.
  * Returns SDPA_ERR_INVALID_ARG for other values.

@@ -43,12 +43,17 @@ constexpr size_t kSliceMajorKVBytes = size_t(64) << 20;
 // Forward kernel choice.  The two-tile kernel (256 query rows per unit, two
 // softmax warpgroups) wins once units visit a few key tiles: at d = 64 and 128
 // from 1024 rows on (dense) and from a mean of 2048 tokens per sequence
-// (packed, whose lists also hold short sequences that fill only tile A); short
-// problems do better with the one-tile kernel's 128-row units.  rows_*: the
-// dense lengths, or the packed totals over the sequence count.
-bool use_pair_kernel(bool packed, int d, int64_t rows_q, int64_t rows_kv) {
+// (packed lists whose sequences do not fit its table, which also hold short
+// sequences that fill only tile A); short problems do better with the one-tile
+// kernel's 128-row units.  Packed lists that fit the two-tile kernel's
+// sequence table (pair_table) take its units on demand, and measured so it
+// won from a mean of 200 tokens on (d = 128: 3-16 %, d = 64: 1-12 %), so they
+// take it at any length.  rows_*: the dense lengths, or the packed totals over
+// the sequence count.
+bool use_pair_kernel(bool packed, int d, int64_t rows_q, int64_t rows_kv, bool pair_table = false) {
     if (t_fwd_variant == 1) return false;
     if (t_fwd_variant == 2) return true;
+    if (packed && pair_table) return d == 64 || d == 128;
     const int64_t min_rows = packed ? 2048 : 1024;
     return (d == 64 || d == 128) && rows_q >= min_rows && rows_kv >= min_rows;
 }
@@ -368,7 +373,7 @@ extern "C" {
 
 const char *sdpa_last_error(void) { return t_last_error.c_str(); }
 
-const char *sdpa_version(void) { return "sdpa_gb300 0.17 sm_103a"; }
+const char *sdpa_version(void) { return "sdpa_gb300 0.18 sm_103a"; }
 
 int sdpa_set_forward_variant(int variant) {
     if (variant < 0 || variant > 2)
@@ -520,8 +525,8 @@ int sdpa_varlen_fwd_ex(const void *q, const void *k, const void *v, void *o, flo
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const bool pair = use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
-                                      (int64_t)total_kv / num_seqs) &&
+    const bool pair = use_pair_kernel(true, d, (int64_t)total_q / num_seqs, (int64_t)total_kv / num_seqs,
+                                      window_left < 0 && num_seqs + 1 <= fwd_pair_table_cap(d, false)) &&
                       (window_left < 0 || d == 128);
     const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;  // 128-row units: the most
     const int64_t slices = (int64_t)num_seqs * h;
@@ -674,8 +679,9 @@ int sdpa_varlen_fwd_fp8(const void *q, const void *k, const void *v, void *o, fl
                                  max_seqlen_q, max_seqlen_kv, h)))
         return st;
     if (h == 0 || total_q == 0 || num_seqs == 0) return ok();
-    const bool pair = window_left < 0 && use_pair_kernel(true, d, (int64_t)total_q / num_seqs,
-                                                         (int64_t)total_kv / num_seqs);
+    const bool pair = window_left < 0 &&
+                      use_pair_kernel(true, d, (int64_t)total_q / num_seqs, (int64_t)total_kv / num_seqs,
+                                      num_seqs + 1 <= fwd_pair_table_cap(d, true));
     const int64_t q_tiles = (max_seqlen_q + kTileM - 1) / kTileM;  // 128-row units: the most
     const int64_t slices = (int64_t)num_seqs * h;
     if (slices > INT32_MAX || q_tiles * slices > INT32_MAX)

@@ -44,7 +44,8 @@ struct FwdParams {
     int h;                       // query heads
     int h_kv;                    // key/value heads (h is a multiple)
     int group;                   // h / h_kv: query head hq reads key/value head hq / group
-    int s_q, s_kv;               // dense lengths
+    int s_q, s_kv;               // dense lengths (packed two-tile launches that take their
+                                 // units dynamically carry their counter slot + 1 in s_q)
     int num_seqs;                // packed
     int q_tiles;                 // row blocks per slice (128 rows, or 256 for the
                                  // two-tile kernel): dense from s_q, packed from max_seqlen_q
@@ -147,6 +148,9 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // Two-tile forward (fwd_pair.cu): 256 query rows per unit; q_tiles / n_units
 // then count 256-row blocks.
 int fwd_pair_rows();
+// Entries of the two-tile kernel's packed sequence table (num_seqs + 1 must
+// fit for its sequence-by-sequence, dynamically taken unit list).
+int fwd_pair_table_cap(int d, bool fp8);
 // The two-tile kernel's setmaxnreg split hands out exactly fwd_pair_split_regs()
 // registers per launched thread.  A build whose launch register count differs
 // is not launched: launch_fwd_pair* then return cudaErrorInvalidConfiguration

@@ -92,6 +92,29 @@ struct PairLayout {
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only if the max grows by 2^8
 
+// Units taken dynamically (kDyn, packed lists with a sequence table): the
+// list runs sequence by sequence, longest first, and within a sequence from
+// its heaviest 256-row block to its lightest, a sawtooth that a fixed deal
+// spreads unevenly over the CTAs.  The kDyn instantiations take units from a
+// counter instead, in the same order: the producer thread takes the next unit
+// once it has issued the current one's loads and hands it to the MMA thread
+// and the softmax warps through a ring of kUnitRing slots placed after the
+// layout.  The counter is a slot of g_pair_unit_counters, zeroed by the host
+// before the launch; packed launches carry that slot + 1 in FwdParams::s_q,
+// which no packed kernel reads otherwise.
+constexpr int kUnitRing = 4;
+constexpr int kPairCounterSlots = 1024;
+__device__ uint32_t g_pair_unit_counters[kPairCounterSlots];
+template <int D, int kEb>
+struct PairDynLayout {
+    using L = PairLayout<D, kEb, true>;
+    static constexpr int kRing = L::kBytes;                  // kUnitRing ints
+    static constexpr int kRingBar = kRing + 4 * kUnitRing;  // full, empty: kUnitRing each
+    static constexpr int kBytes = kRingBar + 2 * kUnitRing * 8;
+    static constexpr int kSmemAlloc = kBytes + 1024;
+};
+static_assert(PairDynLayout<128, 2>::kSmemAlloc <= 232448, "dynamic two-tile forward exceeds shared memory");
+
 SDPA_DEV bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx &w, uint32_t site) {
     bool ok = mbar_wait(bar, parity, w, site);
     return __all_sync(0xffffffffu, ok);
@@ -237,7 +260,7 @@ SDPA_DEV PairUnit decode_pair(const FwdParams &p, int u, const int *cu_q, const 
 
 // kEl / kOut: input and output element kinds as in fwd.cu (E4M3 inputs with
 // device descales, P as E4M3 quads, kind::f8f6f4 products; amax of O).
-template <int D, int kEl, bool kPacked, int kOut, bool kWin, bool kSplit = false>
+template <int D, int kEl, bool kPacked, int kOut, bool kWin, bool kSplit = false, bool kDyn = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -336,6 +359,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             mbar_init(bar(L::bOFree + x), kTileM);
         }
         mbar_init(bar(L::bMmaIdle), 1);
+        if constexpr (kDyn) {
+            const uint32_t rb = sbase + PairDynLayout<D, kEb>::kRingBar;  // the unit ring's barriers
+            for (int b = 0; b < kUnitRing; ++b) {
+                mbar_init(rb + 8u * b, 1);                // full: the producer
+                mbar_init(rb + 8u * (kUnitRing + b), 9);  // empty: the MMA thread and 8 softmax warps
+            }
+        }
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -380,8 +410,25 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     return true;
                 };
                 for (int k = 0; ok; ++k) {
-                    const int u = unit_of(k, first, step);
-                    if (u >= n_units) break;
+                    int u;
+                    if constexpr (kDyn) {
+                        // take the next unit (the first by the CTA's index) and hand it on
+                        using DL = PairDynLayout<D, kEb>;
+                        const uint32_t rb = sbase + DL::kRingBar;
+                        const int slot = k % kUnitRing;
+                        if (k >= kUnitRing &&
+                            !mbar_wait(rb + 8u * (kUnitRing + slot), ((k / kUnitRing) - 1) & 1, wc, 20))
+                            break;
+                        u = k == 0 ? (int)blockIdx.x
+                                   : (int)gridDim.x + (int)atomicAdd(g_pair_unit_counters + (p.s_q - 1), 1u);
+                        if (u >= n_units) u = -1;
+                        reinterpret_cast<volatile int *>(smem + DL::kRing)[slot] = u;
+                        mbar_arrive(rb + 8u * slot);
+                        if (u < 0) break;
+                    } else {
+                        u = unit_of(k, first, step);
+                        if (u >= n_units) break;
+                    }
                     const PairUnit U = decode_pair<D, kPacked, kWin, kSplit>(p, u, cu_q, cu_kv, order, first_s);
                     const int nmax = max(U.n_kv[0], U.n_kv[1]);
                     if (nmax == 0) continue;
@@ -478,8 +525,19 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 int t = 0, units = 0, cnt[2] = {0, 0}, uo[2] = {0, 0};
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
-                    const int u = unit_of(k, first, step);
-                    if (u >= n_units) break;
+                    int u;
+                    if constexpr (kDyn) {
+                        using DL = PairDynLayout<D, kEb>;
+                        const uint32_t rb = sbase + DL::kRingBar;
+                        const int slot = k % kUnitRing;
+                        if (!(ok = mbar_wait(rb + 8u * slot, (k / kUnitRing) & 1, wc, 21))) break;
+                        u = reinterpret_cast<volatile int *>(smem + DL::kRing)[slot];
+                        mbar_arrive(rb + 8u * (kUnitRing + slot));
+                        if (u < 0) break;
+                    } else {
+                        u = unit_of(k, first, step);
+                        if (u >= n_units) break;
+                    }
                     const PairUnit U = decode_pair<D, kPacked, kWin, kSplit>(p, u, cu_q, cu_kv, order, first_s);
                     const int nmax = max(U.n_kv[0], U.n_kv[1]);
                     if (nmax == 0) continue;
@@ -579,8 +637,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         int cnt = 0, uo = 0;  // tiles and units of this tile's chain
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const int u = unit_of(k, first, step);
-            if (u >= n_units) break;
+            int u;
+            if constexpr (kDyn) {
+                using DL = PairDynLayout<D, kEb>;
+                const uint32_t rb = sbase + DL::kRingBar;
+                const int slot = k % kUnitRing;
+                if (!(ok = warp_wait(rb + 8u * slot, (k / kUnitRing) & 1, wc, 22))) break;
+                u = reinterpret_cast<volatile int *>(smem + DL::kRing)[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rb + 8u * (kUnitRing + slot));
+                if (u < 0) break;
+            } else {
+                u = unit_of(k, first, step);
+                if (u >= n_units) break;
+            }
             const PairUnit U = decode_pair<D, kPacked, kWin, kSplit>(p, u, cu_q, cu_kv, order, first_s);
             const int row0 = U.row0 + x * kTileM;
             if (!U.live || row0 >= U.Lq || (kSplit && x == 1 && U.single)) continue;  // no row of this tile
@@ -765,12 +835,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 // launch register count of the last build launch_pair_t refused on this thread
 thread_local int t_refused_regs = 0;
 
-template <int D, int kEl, bool kPacked, int kOut, bool kWin = false, bool kSplit = false>
+std::atomic<uint32_t> g_pair_counter_next{0};
+
+template <int D, int kEl, bool kPacked, int kOut, bool kWin = false, bool kSplit = false, bool kDyn = false>
 cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const FwdParams &p, int grid, cudaStream_t stream,
                           const KernelTimer &timer) {
     using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2, kPacked>;
-    auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut, kWin, kSplit>;
+    auto kern = fwd_pair_kernel<D, kEl, kPacked, kOut, kWin, kSplit, kDyn>;
     // The softmax warpgroups' setmaxnreg.inc waits for the registers warpgroup
     // 0 releases; a build launched with any other per-thread count than the
     // split assumes would leave it waiting, so such a build is not launched.
@@ -790,19 +862,54 @@ cudaError_t launch_pair_t(const CUtensorMap &tq, const CUtensorMap &tk, const CU
         t_refused_regs = regs;
         return cudaErrorInvalidConfiguration;
     }
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    if (timer.start) cudaEventRecord(timer.start, stream);
-    kern<<<grid, kPairThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, p);
-    e = cudaGetLastError();
-    if (timer.stop) cudaEventRecord(timer.stop, stream);
-    return e;
+    if constexpr (kDyn) {
+        // a zeroed counter slot for this launch, carried in s_q (see PairDynLayout)
+        using DL = PairDynLayout<D, kEl == kElE4m3 ? 1 : 2>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DL::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        const int slot = (int)(g_pair_counter_next.fetch_add(1) % kPairCounterSlots);
+        void *ctr = nullptr;
+        e = cudaGetSymbolAddress(&ctr, g_pair_unit_counters);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(static_cast<uint32_t *>(ctr) + slot, 0, sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return e;
+        FwdParams pd = p;
+        pd.s_q = slot + 1;
+        if (timer.start) cudaEventRecord(timer.start, stream);
+        kern<<<grid, kPairThreads, DL::kSmemAlloc, stream>>>(tq, tk, tv, pd);
+        e = cudaGetLastError();
+        if (timer.stop) cudaEventRecord(timer.stop, stream);
+        return e;
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             L::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        if (timer.start) cudaEventRecord(timer.start, stream);
+        kern<<<grid, kPairThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, p);
+        e = cudaGetLastError();
+        if (timer.stop) cudaEventRecord(timer.stop, stream);
+        return e;
+    }
+}
+
+// Packed lists: those that fit the kernel's sequence table take their units
+// dynamically (PairDynLayout), longer ones keep the fixed deal.
+template <int D, int kEl, int kOut>
+cudaError_t launch_pair_packed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const FwdParams &p, int grid, cudaStream_t stream, const KernelTimer &timer) {
+    using L = PairLayout<D, kEl == kElE4m3 ? 1 : 2, true>;
+    if (p.num_seqs + 1 <= L::kCuCap)
+        return launch_pair_t<D, kEl, true, kOut, false, false, true>(tq, tk, tv, p, grid, stream, timer);
+    return launch_pair_t<D, kEl, true, kOut>(tq, tk, tv, p, grid, stream, timer);
 }
 
 }  // namespace
 
 int fwd_pair_rows() { return kPairRows; }
+int fwd_pair_table_cap(int d, bool fp8) {
+    if (fp8) return PairLayout<128, 1, true>::kCuCap;
+    return d == 64 ? PairLayout<64, 2, true>::kCuCap : PairLayout<128, 2, true>::kCuCap;
+}
 int fwd_pair_split_regs() { return kPairLaunchRegs; }
 int fwd_pair_refused_regs() { return t_refused_regs; }
 
@@ -829,17 +936,14 @@ cudaError_t launch_fwd_pair(const CUtensorMap &tq, const CUtensorMap &tk, const 
                         : launch_pair_t<128, kElFp16, false, kElFp16, false, true>(tq, tk, tv, p, grid, stream, timer);
         return cudaErrorInvalidValue;
     }
-#define SDPA_PAIR_CASE(D_, EL_, PK_)                                           \
-    if (d == D_ && (bf16 ? kElBf16 : kElFp16) == EL_ && packed == PK_)         \
-        return launch_pair_t<D_, EL_, PK_, EL_>(tq, tk, tv, p, grid, stream, timer);
-    SDPA_PAIR_CASE(64, kElBf16, false)
-    SDPA_PAIR_CASE(64, kElBf16, true)
-    SDPA_PAIR_CASE(64, kElFp16, false)
-    SDPA_PAIR_CASE(64, kElFp16, true)
-    SDPA_PAIR_CASE(128, kElBf16, false)
-    SDPA_PAIR_CASE(128, kElBf16, true)
-    SDPA_PAIR_CASE(128, kElFp16, false)
-    SDPA_PAIR_CASE(128, kElFp16, true)
+#define SDPA_PAIR_CASE(D_, EL_)                                                \
+    if (d == D_ && (bf16 ? kElBf16 : kElFp16) == EL_)                          \
+        return packed ? launch_pair_packed<D_, EL_, EL_>(tq, tk, tv, p, grid, stream, timer) \
+                      : launch_pair_t<D_, EL_, false, EL_>(tq, tk, tv, p, grid, stream, timer);
+    SDPA_PAIR_CASE(64, kElBf16)
+    SDPA_PAIR_CASE(64, kElFp16)
+    SDPA_PAIR_CASE(128, kElBf16)
+    SDPA_PAIR_CASE(128, kElFp16)
 #undef SDPA_PAIR_CASE
     return cudaErrorInvalidValue;
 }
@@ -854,15 +958,13 @@ cudaError_t launch_fwd_pair_fp8(const CUtensorMap &tq, const CUtensorMap &tk, co
         if (out == kElE4m3) return launch_pair_t<128, kElE4m3, false, kElE4m3, false, true>(tq, tk, tv, p, grid, stream, timer);
         return cudaErrorInvalidValue;
     }
-#define SDPA_PAIR_FP8_CASE(OUT_, PK_)                                          \
-    if (out == OUT_ && packed == PK_)                                          \
-        return launch_pair_t<128, kElE4m3, PK_, OUT_>(tq, tk, tv, p, grid, stream, timer);
-    SDPA_PAIR_FP8_CASE(kElBf16, false)
-    SDPA_PAIR_FP8_CASE(kElBf16, true)
-    SDPA_PAIR_FP8_CASE(kElFp16, false)
-    SDPA_PAIR_FP8_CASE(kElFp16, true)
-    SDPA_PAIR_FP8_CASE(kElE4m3, false)
-    SDPA_PAIR_FP8_CASE(kElE4m3, true)
+#define SDPA_PAIR_FP8_CASE(OUT_)                                               \
+    if (out == OUT_)                                                           \
+        return packed ? launch_pair_packed<128, kElE4m3, OUT_>(tq, tk, tv, p, grid, stream, timer) \
+                      : launch_pair_t<128, kElE4m3, false, OUT_>(tq, tk, tv, p, grid, stream, timer);
+    SDPA_PAIR_FP8_CASE(kElBf16)
+    SDPA_PAIR_FP8_CASE(kElFp16)
+    SDPA_PAIR_FP8_CASE(kElE4m3)
 #undef SDPA_PAIR_FP8_CASE
     return cudaErrorInvalidValue;
 }

@@ -322,27 +322,30 @@ def test_slice_major_packed_one_tile(sdpa, d, n, lo, hi):
         check_lse(lse[a:e, hh][rows], rl, f"lse seq {i}")
 
 
-def test_packed_long_sequences_two_tile(sdpa):
-    """A packed problem whose mean sequence length reaches 2048 runs the
-    two-tile kernel by default (longest sequence first); sampled rows against
-    the oracle, and the same bits as the two-tile kernel forced."""
-    lens, h, d = [2100, 2500, 3000, 5000, 100, 90, 80], 4, 128
-    assert sum(lens) // len(lens) < 2048 <= sum(lens[:4]) // 4  # one-tile, then two-tile
-    for ls in (lens, lens[:4]):
+def test_packed_kernel_choice(sdpa):
+    """Packed lists that fit the two-tile kernel's sequence table (95 sequences
+    at d = 128) run it by default, whatever their lengths; a longer list of
+    short sequences runs the one-tile kernel.  Sampled rows against the
+    oracle, and the same bits as the kernel forced."""
+    h, d = 4, 128
+    cases = [([2100, 2500, 3000, 5000, 100, 90, 80], 2),   # mean below 2048: two-tile (table)
+             ([300, 17, 256, 129], 2),
+             ([40] * 100, 1)]                               # 100 sequences: past the table
+    for ls, expect in cases:
         q, k, v, _, cu, _ = sdpa_inputs.packed(ls, ls, h, d, seed=71 + len(ls))
         args = (q.cuda(), k.cuda(), v.cuda(), cu.cuda(), cu.cuda(), max(ls), max(ls))
+        sdpa.sdpa_set_forward_variant(0)  # the automatic choice (the module's fixture forces one)
         o, lse = sdpa.attention_varlen(*args, scale=0.088, causal=True)
-        sdpa.sdpa_set_forward_variant(2)
+        sdpa.sdpa_set_forward_variant(expect)
         try:
             o2, lse2 = sdpa.attention_varlen(*args, scale=0.088, causal=True)
         finally:
             sdpa.sdpa_set_forward_variant(0)
         torch.cuda.synchronize()
-        if len(ls) == 4:
-            assert torch.equal(o, o2) and torch.equal(lse, lse2)
+        assert torch.equal(o, o2) and torch.equal(lse, lse2), f"{len(ls)} sequences"
         o, lse = o.cpu(), lse.cpu()
         cl = cu.tolist()
-        for i, L in enumerate(ls):
+        for i, L in enumerate(ls[:8]):
             hh = i % h
             a, e = cl[i], cl[i + 1]
             rows = _sampled_rows(L, i + 3)

@@ -1,8 +1,9 @@
-"""The one-tile forward taking its units dynamically: packed lists whose K and
-V outgrow 64 MiB run sequence by sequence (longest first, from each CTA's
-table of the sequences), and those launches take their units from a counter
-instead of a fixed deal of the list.  Every sequence of every case is checked
-against the fp64 oracle.
+"""The forwards taking their units dynamically: packed lists run sequence by
+sequence (longest first, from each CTA's table of the sequences) -- on the
+one-tile kernel when their K and V outgrow 64 MiB, on the two-tile kernel
+always -- and those launches take their units from a counter instead of a
+fixed deal of the list.  Every case runs on both kernels; every sequence is
+checked against the fp64 oracle.
 
 Tolerances: O within 1e-2 of max|O_ref| per sequence (16-bit), LSE within
 1e-3; FP8 within the derived bound of tests/test_gpu_fp8.py (2^-4 max|V| +
@@ -23,11 +24,11 @@ pytestmark = pytest.mark.gpu
 SLICE_MAJOR_KV_BYTES = 64 << 20  # above this K + V, packed lists go sequence by sequence
 
 
-@pytest.fixture(scope="module")
-def sdpa():
+@pytest.fixture(scope="module", params=[1, 2], ids=["one_tile", "two_tile"])
+def sdpa(request):
     import scaled_dot_product_04_gb300 as m
     m.load()
-    m.sdpa_set_forward_variant(1)  # the one-tile kernel
+    m.sdpa_set_forward_variant(request.param)
     yield m
     m.sdpa_set_forward_variant(0)
 
