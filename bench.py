@@ -424,10 +424,15 @@ def run_ours(args):
 
     # ------------------------------------------------------------ end to end
     # Each step copies its inputs from pinned host memory, runs the path and
-    # copies its results back.  Two device buffer sets and two copy streams
+    # copies its results back.  Three device buffer sets and two copy streams
     # (host->device and device->host, one copy engine each) let step i's
-    # copies overlap the compute of steps i-1 and i+1; every step's own
-    # copies stay inside the timed region.
+    # copies overlap the compute of its neighbours; every step's own copies
+    # stay inside the timed region.  A set is refilled only once its previous
+    # results have reached the host, so with two sets a set's result copy,
+    # its next input copy and its compute would run back to back: (D2H + H2D
+    # + compute) / 2 a step, which a host link sharing its bandwidth between
+    # the two directions makes longer than the compute.  Three sets spread
+    # that chain over three steps.
     e2e = None
     if not args.no_e2e:
         names_in = ["q", "k", "v"] + ([] if fp8 else ["do"])
@@ -440,14 +445,15 @@ def run_ours(args):
                 outs += [torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)]
             return ins, outs
 
-        sets = [dev_set(), dev_set()]
+        n_sets = 3
+        sets = [dev_set() for _ in range(n_sets)]
         host_out = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in sets[0][1]]
-                    for _ in range(2)]
-        ws2 = [ws, torch.empty_like(ws)]
+                    for _ in range(n_sets)]
+        ws_sets = [ws] + [torch.empty_like(ws) for _ in range(n_sets - 1)]
         h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
         def run_step(i):
-            ins, outs = sets[i & 1]
+            ins, outs = sets[i % n_sets]
             qq, kk, vv = ins[0], ins[1], ins[2]
             oo, ll = outs[0], outs[1]
             if fp8:
@@ -456,7 +462,7 @@ def run_ours(args):
                 return
             ddo = ins[3]
             gq, gk, gv = outs[2], outs[3], outs[4]
-            wsi = ws2[i & 1]
+            wsi = ws_sets[i % n_sets]
             if ext:
                 sdpa.sdpa_fwd_ex(qq, kk, vv, oo, ll, b, h, hk, s_q, s, d, scale, mask, window, 0,
                                  stream)
@@ -472,9 +478,9 @@ def run_ours(args):
                               wsi, wsi.numel(), stream)
 
         def pipeline(n):
-            free = [None, None]  # device->host copy of the set's last results done
+            free = [None] * n_sets  # device->host copy of the set's last results done
             for i in range(n):
-                st = i & 1
+                st = i % n_sets
                 ins, outs = sets[st]
                 with torch.cuda.stream(h2d):
                     if free[st] is not None:
@@ -498,7 +504,7 @@ def run_ours(args):
         # overlap any compute; 100 steps (more when more are timed, up to 150)
         # spread that fill and drain thinly, as a caller's long loop would
         n_e2e = max(100, min(args.steps, 150))
-        pipeline(2)
+        pipeline(n_sets)
         torch.cuda.synchronize(dev)
         ev_a, ev_z = new_ev(), new_ev()
         ev_a.record(h2d)             # before the first step's first copy
@@ -511,9 +517,10 @@ def run_ours(args):
         e2e = {"value": world * f_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                "ms_per_step": e_ms, "steps": n_e2e,
-               "copies": "pinned host buffers; two copy streams overlap each step's copies "
-                         "with the neighbouring steps' compute; CUDA events before the first "
-                         "copy and after the last (the pipeline's fill and drain included)"}
+               "copies": "pinned host buffers; three device buffer sets and two copy streams "
+                         "overlap each step's copies with the neighbouring steps' compute; "
+                         "CUDA events before the first copy and after the last (the "
+                         "pipeline's fill and drain included)"}
 
     # ------------------------------------------------------------ roofline
     # Per-kernel figures use the median over the timed steps (an L2 flush

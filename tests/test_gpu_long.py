@@ -1,0 +1,112 @@
+"""Parity on sequences four times longer than the long-context workload's.
+
+One key/value slice of 65,536 tokens at d = 128, bf16 N(0, 1) inputs from
+sdpa_inputs.dense, scale 1/sqrt(d):
+- causal (top-left), one head: the forward's units walk up to 512 key tiles and
+  the backward's units up to 512 query tiles, four times the 16,384-token
+  workload's;
+- a bottom-right band (window_left 5000) with s_q = 61,000 (a ragged last
+  query tile) against s_kv = 65,536, two query heads on one key/value head.
+
+Rows are sampled and the oracle computes them one by one (attn_fwd_rows /
+attn_bwd_rows and their masked forms).  Key rows need every query row's
+statistics, about 1.1 TFLOP of fp64 work for the causal head, so the
+references are computed once per process.  Both backward main kernels run
+each case.
+
+Tolerances are those of helpers.py, relative to a tensor's largest reference
+value.  On a sample that maximum can only be underestimated, and under a
+causal mask the largest dQ, O, dK and dV values sit in the first rows, which
+see few keys.  So the sample holds the first two query and key tiles whole,
+besides the tile boundaries, the middle, the last rows and seeded random rows.
+Those first rows are also where the backward's inherent error is largest: D =
+rowsum(dO * O) is formed from the 16-bit O the backward is given, and a row
+that sees two keys has a dQ that is a difference of nearly equal terms (row 1
+of the causal case: about 3 % of that row, which an emulation of the same
+rounding on the CPU reproduces).
+"""
+import functools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sdpa_inputs
+from helpers import GRAD_TOL, O_TOL, check_lse, check_rel
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+SCALE = 1.0 / math.sqrt(D)
+CAUSAL = dict(h=1, h_kv=1, s_q=65536, s_kv=65536, mask="top_left", window=-1, seed=65536)
+BAND = dict(h=2, h_kv=1, s_q=61000, s_kv=65536, mask="bottom_right", window=5000, seed=61000)
+CASES = {"causal_s65536": CAUSAL, "band_gqa_s61000_s65536": BAND}
+
+
+@pytest.fixture(scope="module")
+def sdpa():
+    import scaled_dot_product_04_gb300 as m
+    m.load()
+    return m
+
+
+def _rows(n, seed):
+    g = np.random.default_rng(seed)
+    base = set(range(min(n, 256)))
+    base |= {n // 2 - 1, n // 2, n - 129, n - 128, n - 2, n - 1}
+    base |= set(g.integers(0, n, 8).tolist())
+    return np.array(sorted(r for r in base if 0 <= r < n), np.int32)
+
+
+@functools.lru_cache(maxsize=None)
+def _inputs(name):
+    c = CASES[name]
+    return sdpa_inputs.dense(1, c["h"], c["s_q"], c["s_kv"], D, seed=c["seed"], h_kv=c["h_kv"])
+
+
+@functools.lru_cache(maxsize=None)
+def _reference(name):
+    """Sampled rows of every query head: (q_rows, kv_rows, o, lse, dq) per
+    head, and dK/dV rows per key/value head (summed over its query heads)."""
+    c = CASES[name]
+    q, k, v, do = _inputs(name)
+    group = c["h"] // c["h_kv"]
+    q_rows, kv_rows = _rows(c["s_q"], c["seed"] + 1), _rows(c["s_kv"], c["seed"] + 2)
+    o, lse, dq = [], [], []
+    dk = [np.zeros((len(kv_rows), D)) for _ in range(c["h_kv"])]
+    dv = [np.zeros((len(kv_rows), D)) for _ in range(c["h_kv"])]
+    for hq in range(c["h"]):
+        hk = hq // group
+        args = (q[0, hq], k[0, hk], v[0, hk])
+        ro, rl = oracle.attn_fwd_rows_ex(*args, q_rows, SCALE, c["mask"], c["window"])
+        rdq, rdk, rdv = oracle.attn_bwd_rows_ex(*args, do[0, hq], q_rows, kv_rows, SCALE, c["mask"],
+                                                c["window"])
+        o.append(ro)
+        lse.append(rl)
+        dq.append(rdq)
+        dk[hk] += rdk
+        dv[hk] += rdv
+    return q_rows, kv_rows, o, lse, dq, dk, dv
+
+
+@pytest.mark.usefixtures("bwd_kernel")
+@pytest.mark.parametrize("name", list(CASES))
+def test_long_sequence_sampled_rows(sdpa, name):
+    c = CASES[name]
+    q, k, v, do = (x.cuda() for x in _inputs(name))
+    o, lse = sdpa.attention(q, k, v, scale=SCALE, mask=c["mask"], window_left=c["window"])
+    dq, dk, dv = sdpa.attention_bwd(q, k, v, o, do, lse, scale=SCALE, mask=c["mask"],
+                                    window_left=c["window"])
+    torch.cuda.synchronize()
+    q_rows, kv_rows, ro, rl, rdq, rdk, rdv = _reference(name)
+    qi, ki = torch.from_numpy(q_rows).long(), torch.from_numpy(kv_rows).long()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    for hq in range(c["h"]):
+        check_rel(o[0, hq, qi], ro[hq], O_TOL[torch.bfloat16], f"o[{hq}]")
+        check_lse(lse[0, hq, qi], rl[hq], f"lse[{hq}]")
+        check_rel(dq[0, hq, qi], rdq[hq], GRAD_TOL, f"dq[{hq}]")
+    for hk in range(c["h_kv"]):
+        check_rel(dk[0, hk, ki], rdk[hk], GRAD_TOL, f"dk[{hk}]")
+        check_rel(dv[0, hk, ki], rdv[hk], GRAD_TOL, f"dv[{hk}]")
