@@ -1,12 +1,14 @@
 """Parity on sequences four times longer than the long-context workload's.
 
-One key/value slice of 65,536 tokens at d = 128, bf16 N(0, 1) inputs from
-sdpa_inputs.dense, scale 1/sqrt(d):
-- causal (top-left), one head: the forward's units walk up to 512 key tiles and
-  the backward's units up to 512 query tiles, four times the 16,384-token
-  workload's;
+Key/value slices of 65,536 tokens, bf16 N(0, 1) inputs from sdpa_inputs.dense,
+scale 1/sqrt(d):
+- causal (top-left), one head, at d = 128 and d = 64: the forward's units walk up
+  to 512 key tiles and the backward's units up to 512 query tiles, four times the
+  16,384-token workload's (d = 64 runs the other TMEM layout: dQ has columns of
+  its own and dO two stages);
 - a bottom-right band (window_left 5000) with s_q = 61,000 (a ragged last
-  query tile) against s_kv = 65,536, two query heads on one key/value head.
+  query tile) against s_kv = 65,536, two query heads on one key/value head,
+  d = 128.
 
 Rows are sampled and the oracle computes them one by one (attn_fwd_rows /
 attn_bwd_rows and their masked forms).  Key rows need every query row's
@@ -38,11 +40,18 @@ from helpers import GRAD_TOL, O_TOL, check_lse, check_rel
 
 pytestmark = pytest.mark.gpu
 
-D = 128
-SCALE = 1.0 / math.sqrt(D)
-CAUSAL = dict(h=1, h_kv=1, s_q=65536, s_kv=65536, mask="top_left", window=-1, seed=65536)
-BAND = dict(h=2, h_kv=1, s_q=61000, s_kv=65536, mask="bottom_right", window=5000, seed=61000)
-CASES = {"causal_s65536": CAUSAL, "band_gqa_s61000_s65536": BAND}
+CASES = {
+    "causal_s65536": dict(d=128, h=1, h_kv=1, s_q=65536, s_kv=65536, mask="top_left", window=-1,
+                          seed=65536),
+    "causal_s65536_d64": dict(d=64, h=1, h_kv=1, s_q=65536, s_kv=65536, mask="top_left",
+                              window=-1, seed=65537),
+    "band_gqa_s61000_s65536": dict(d=128, h=2, h_kv=1, s_q=61000, s_kv=65536, mask="bottom_right",
+                                   window=5000, seed=61000),
+}
+
+
+def _scale(c):
+    return 1.0 / math.sqrt(c["d"])
 
 
 @pytest.fixture(scope="module")
@@ -63,7 +72,8 @@ def _rows(n, seed):
 @functools.lru_cache(maxsize=None)
 def _inputs(name):
     c = CASES[name]
-    return sdpa_inputs.dense(1, c["h"], c["s_q"], c["s_kv"], D, seed=c["seed"], h_kv=c["h_kv"])
+    return sdpa_inputs.dense(1, c["h"], c["s_q"], c["s_kv"], c["d"], seed=c["seed"],
+                             h_kv=c["h_kv"])
 
 
 @functools.lru_cache(maxsize=None)
@@ -75,14 +85,14 @@ def _reference(name):
     group = c["h"] // c["h_kv"]
     q_rows, kv_rows = _rows(c["s_q"], c["seed"] + 1), _rows(c["s_kv"], c["seed"] + 2)
     o, lse, dq = [], [], []
-    dk = [np.zeros((len(kv_rows), D)) for _ in range(c["h_kv"])]
-    dv = [np.zeros((len(kv_rows), D)) for _ in range(c["h_kv"])]
+    dk = [np.zeros((len(kv_rows), c["d"])) for _ in range(c["h_kv"])]
+    dv = [np.zeros((len(kv_rows), c["d"])) for _ in range(c["h_kv"])]
     for hq in range(c["h"]):
         hk = hq // group
         args = (q[0, hq], k[0, hk], v[0, hk])
-        ro, rl = oracle.attn_fwd_rows_ex(*args, q_rows, SCALE, c["mask"], c["window"])
-        rdq, rdk, rdv = oracle.attn_bwd_rows_ex(*args, do[0, hq], q_rows, kv_rows, SCALE, c["mask"],
-                                                c["window"])
+        ro, rl = oracle.attn_fwd_rows_ex(*args, q_rows, _scale(c), c["mask"], c["window"])
+        rdq, rdk, rdv = oracle.attn_bwd_rows_ex(*args, do[0, hq], q_rows, kv_rows, _scale(c),
+                                                c["mask"], c["window"])
         o.append(ro)
         lse.append(rl)
         dq.append(rdq)
@@ -96,8 +106,8 @@ def _reference(name):
 def test_long_sequence_sampled_rows(sdpa, name):
     c = CASES[name]
     q, k, v, do = (x.cuda() for x in _inputs(name))
-    o, lse = sdpa.attention(q, k, v, scale=SCALE, mask=c["mask"], window_left=c["window"])
-    dq, dk, dv = sdpa.attention_bwd(q, k, v, o, do, lse, scale=SCALE, mask=c["mask"],
+    o, lse = sdpa.attention(q, k, v, scale=_scale(c), mask=c["mask"], window_left=c["window"])
+    dq, dk, dv = sdpa.attention_bwd(q, k, v, o, do, lse, scale=_scale(c), mask=c["mask"],
                                     window_left=c["window"])
     torch.cuda.synchronize()
     q_rows, kv_rows, ro, rl, rdq, rdk, rdv = _reference(name)
