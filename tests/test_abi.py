@@ -130,6 +130,28 @@ def test_extended_validation_before_any_cuda_call(lib):
     assert lib.sdpa_set_forward_variant(0) == L.SDPA_OK
 
 
+def test_problem_too_large_for_one_launch(lib):
+    """Sizes whose row, tile or slice counts pass 2^31 - 1 (the TMA coordinates and
+    the grid are 32-bit) are refused on the host, before any CUDA call."""
+    from scaled_dot_product_04_gb300 import _lib as L
+    big = 65536  # b * h = 2^32 slices
+    assert _fwd(lib, b=big, h=big) == L.SDPA_ERR_INVALID_ARG
+    assert "too large" in L.sdpa_last_error()
+    assert lib.sdpa_fwd_ex(0x10000, 0x20000, 0x30000, 0x40000, None, big, big, big, 128, 128, 64,
+                           0.125, 1, -1, 0, None) == L.SDPA_ERR_INVALID_ARG
+    # backward: b * h * s_q = 2^32 accumulator rows
+    rc = lib.sdpa_bwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000, 0x80000,
+                      0x90000, 1, 32, 1 << 27, 128, 64, 0.125, 1, 0, 0xa0000, 1 << 20, None)
+    assert rc == L.SDPA_ERR_INVALID_ARG
+    assert "too large" in L.sdpa_last_error()
+    # packed backward: total_q * h = 2^32 accumulator rows
+    rc = lib.sdpa_varlen_bwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000,
+                             0x80000, 0x90000, 0xb0000, 0xc0000, 1, 1 << 27, 1 << 27, 1 << 27,
+                             1 << 27, 32, 64, 0.125, 1, 0, 0xa0000, 1 << 20, None)
+    assert rc == L.SDPA_ERR_INVALID_ARG
+    assert "too large" in L.sdpa_last_error()
+
+
 def test_missing_library_fails_loudly(tmp_path):
     """No fallback: pointing the binding at a library that does not exist raises
     (in a fresh process, since this one may have loaded the real one)."""
