@@ -14,8 +14,9 @@
 // that the unwindowed loop compiles exactly as it would without them.
 //
 // Roles inside a CTA (12 warps):
-//   warp 0       TMA producer: Q_A, Q_B of each unit, then K_j and V_j into
-//                two rings (V one tile behind K);
+//   warp 0       TMA producer: Q_A, Q_B and the first K tile of each unit,
+//                then per key tile j the pair V_j, K_{j+1} on one barrier
+//                (K and V keep rings of their own);
 //   warp 1       MMA issuer (one thread).  Per key tile j it issues
 //                O_A += P_A(j) V_j, S_A(j+1) = Q_A K_{j+1}^T,
 //                O_B += P_B(j) V_j, S_B(j+1) = Q_B K_{j+1}^T.
@@ -393,20 +394,27 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_k);
                 tma_prefetch_desc(&tm_v);
-                // V_x goes out one tile after K_x, so a wait for a free V stage
-                // never holds back the K load the next S products need first.
+                // Per unit: Q_A, Q_B, the unit's first K tile (on its K stage's
+                // full barrier), then per key step j the pair V_j, K_{j+1}: both
+                // land on V_j's full barrier, so the MMA thread waits once per
+                // step.  A K tile that rides on a V barrier still completes a
+                // phase of its own stage's full barrier (a plain arrive), so the
+                // K barriers keep one phase per K tile; the MMA thread waits on
+                // them only for a unit's first K, whose stage cannot be refilled
+                // before that wait (the refill waits for the tile's release).
                 int k_it = 0, v_it = 0, units = 0;
-                int pv_y = 0, pv_z = 0;
-                bool v_pending = false, ok = true;
-                auto issue_v = [&](int y, int z) -> bool {
-                    const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
-                    if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) return false;
-                    mbar_arrive_expect_tx(bar(L::bVFull + vs), L::kTileBytes);
+                bool ok = true;
+                // K_{j+1} of a pair: into its stage once released, landing on
+                // `full` (V_j's barrier); its own full barrier gets a plain arrive
+                auto k_stage = [&](uint32_t full, int ky, int kz) -> bool {
+                    const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
+                    if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) return false;
+                    mbar_arrive(bar(L::bKFull + ks));
     #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
-                                    bar(L::bVFull + vs), c * (128 / kEb), y, z);
-                    ++v_it;
+                        tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k, full,
+                                    c * (128 / kEb), ky, kz);
+                    ++k_it;
                     return true;
                 };
                 for (int k = 0; ok; ++k) {
@@ -432,9 +440,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     const PairUnit U = decode_pair<D, kPacked, kWin, kSplit>(p, u, cu_q, cu_kv, order, first_s);
                     const int nmax = max(U.n_kv[0], U.n_kv[1]);
                     if (nmax == 0) continue;
-                    // the previous unit's last V goes out before waiting for Q's slot
-                    if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
-                    v_pending = false;
                     if (units > 0 && !mbar_wait(bar(L::bQEmpty), (units - 1) & 1, wc, 1)) break;
                     mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTileBytes);
     #pragma unroll
@@ -447,29 +452,53 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                         bar(L::bQFull), c * (128 / kEb), qy, qz);
                     }
                     ++units;
-                    for (int j = 0; j < nmax; ++j) {
+                    // key tile j of the unit's walk: (y, z) coordinates of K_j and V_j
+                    auto kv_yz = [&](int j, int &y, int &z) {
                         const int kj = kWin ? U.kt0 + j : j;  // absolute key tile
-                        const int ky = kPacked ? U.kv_head : kj * kTileN;
-                        const int kz = kPacked ? U.tok_kv0 + kj * kTileN : U.kv_slice;
+                        y = kPacked ? U.kv_head : kj * kTileN;
+                        z = kPacked ? U.tok_kv0 + kj * kTileN : U.kv_slice;
+                    };
+                    {
+                        int ky, kz;
+                        kv_yz(0, ky, kz);
+                        const uint32_t full = bar(L::bKFull + k_it % L::kKStages);
                         const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
                         if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(bar(L::bKFull + ks), L::kTileBytes);
+                        mbar_arrive_expect_tx(full, L::kTileBytes);
     #pragma unroll
                         for (int c = 0; c < L::kChunks; ++c)
-                            tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
-                                        bar(L::bKFull + ks), c * (128 / kEb), ky, kz);
+                            tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k, full,
+                                        c * (128 / kEb), ky, kz);
                         ++k_it;
-                        if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
-                        pv_y = ky;
-                        pv_z = kz;
-                        v_pending = true;
+                    }
+                    for (int j = 0; j < nmax; ++j) {
+                        const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
+                        if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) {
+                            ok = false;
+                            break;
+                        }
+                        const bool pair_k = j + 1 < nmax;
+                        const uint32_t vfull = bar(L::bVFull + vs);
+                        int vy, vz;
+                        kv_yz(j, vy, vz);
+                        mbar_arrive_expect_tx(vfull, pair_k ? 2 * L::kTileBytes : L::kTileBytes);
+    #pragma unroll
+                        for (int c = 0; c < L::kChunks; ++c)
+                            tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v, vfull,
+                                        c * (128 / kEb), vy, vz);
+                        ++v_it;
+                        if (pair_k) {
+                            int ky, kz;
+                            kv_yz(j + 1, ky, kz);
+                            if (!(ok = k_stage(vfull, ky, kz))) break;
+                        }
                     }
                 }
-                if (ok && v_pending) issue_v(pv_y, pv_z);
-                // Every load issued must land before the CTA may exit.
+                // Every load issued must land before the CTA may exit (a K tile
+                // that rode on a V barrier lands with that V tile).
                 if (units > 0) mbar_wait_drain(bar(L::bQFull), (units - 1) & 1);
                 for (int i = max(0, k_it - L::kKStages); i < k_it; ++i)
                     mbar_wait_drain(bar(L::bKFull + i % L::kKStages), (i / L::kKStages) & 1);
@@ -559,7 +588,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     // Per key tile j: O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1).
                     for (int j = 0; j < nmax; ++j, ++t) {
                         const int t1 = t + 1;
-                        bool k_next = false;  // K_{j+1} seen to have landed
                         ok = mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 7);
     #pragma unroll
                         for (int x = 0; x < 2; ++x) {
@@ -585,14 +613,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                             if constexpr (kWin) {
                                 if (j + 1 < U.first[x]) continue;
                             }
-                            if (!k_next) {
-                                ok = mbar_wait(bar(L::bKFull + t1 % L::kKStages), (t1 / L::kKStages) & 1,
-                                               wc, 10);
-                                k_next = true;
-                            }
-                            // S_X(j+1) overwrites the P_X(j) that O_X += P_X V
-                            // reads; issue order keeps them apart (see the header)
-                            if (!ok) continue;
+                            // K_{j+1} landed with V_j (see the producer).  S_X(j+1)
+                            // overwrites the P_X(j) that O_X += P_X V reads; issue
+                            // order keeps them apart (see the header)
                             tc_fence_after();
                             issue_s(x, t1 % L::kKStages);
                             mma_commit(bar(L::bSFull + x));
