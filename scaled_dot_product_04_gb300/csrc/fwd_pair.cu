@@ -72,8 +72,12 @@ struct PairLayout {
     static constexpr int bQFull = 0;
     static constexpr int bQEmpty = 1;
     static constexpr int bKFull = 2;
-    static constexpr int bKEmpty = bKFull + kKStages;
-    static constexpr int bVFull = bKEmpty + kKStages;
+    // K stages have no release barrier of their own: K_i's stage is refilled
+    // only after the release of V_{i-1-kVStages} has been seen, which the MMA
+    // thread commits behind every product that reads K_{i-kKStages} as long as
+    // the K ring is at least one stage deeper than the V ring.
+    static_assert(kKStages >= kVStages + 1, "the V releases must cover the K ring");
+    static constexpr int bVFull = bKFull + kKStages;
     static constexpr int bVEmpty = bVFull + kVStages;
     // per tile X in {A, B}: index + X
     static constexpr int bSFull = bVEmpty + kVStages;
@@ -345,10 +349,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(L::bQFull), 1);
         mbar_init(bar(L::bQEmpty), 1);
-        for (int s = 0; s < L::kKStages; ++s) {
-            mbar_init(bar(L::bKFull + s), 1);
-            mbar_init(bar(L::bKEmpty + s), 1);
-        }
+        for (int s = 0; s < L::kKStages; ++s) mbar_init(bar(L::bKFull + s), 1);
         for (int s = 0; s < L::kVStages; ++s) {
             mbar_init(bar(L::bVFull + s), 1);
             mbar_init(bar(L::bVEmpty + s), 1);
@@ -401,21 +402,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 // phase of its own stage's full barrier (a plain arrive), so the
                 // K barriers keep one phase per K tile; the MMA thread waits on
                 // them only for a unit's first K, whose stage cannot be refilled
-                // before that wait (the refill waits for the tile's release).
+                // before that wait (the refill waits for a V release that the MMA
+                // thread commits only after it).
                 int k_it = 0, v_it = 0, units = 0;
                 bool ok = true;
-                // K_{j+1} of a pair: into its stage once released, landing on
-                // `full` (V_j's barrier); its own full barrier gets a plain arrive
-                auto k_stage = [&](uint32_t full, int ky, int kz) -> bool {
-                    const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
-                    if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) return false;
+                // K_{j+1} of a pair, landing on `full` (V_j's barrier); its own
+                // stage's full barrier gets a plain arrive.  The stage is free:
+                // the V stage wait just before it covers the K ring (see
+                // PairLayout).
+                auto k_stage = [&](uint32_t full, int ky, int kz) {
+                    const int ks = k_it % L::kKStages;
                     mbar_arrive(bar(L::bKFull + ks));
     #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
                         tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k, full,
                                     c * (128 / kEb), ky, kz);
                     ++k_it;
-                    return true;
                 };
                 for (int k = 0; ok; ++k) {
                     int u;
@@ -462,11 +464,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         int ky, kz;
                         kv_yz(0, ky, kz);
                         const uint32_t full = bar(L::bKFull + k_it % L::kKStages);
-                        const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
-                        if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
-                            ok = false;
-                            break;
-                        }
+                        const int ks = k_it % L::kKStages;
                         mbar_arrive_expect_tx(full, L::kTileBytes);
     #pragma unroll
                         for (int c = 0; c < L::kChunks; ++c)
@@ -493,7 +491,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         if (pair_k) {
                             int ky, kz;
                             kv_yz(j + 1, ky, kz);
-                            if (!(ok = k_stage(vfull, ky, kz))) break;
+                            k_stage(vfull, ky, kz);
                         }
                     }
                 }
@@ -583,7 +581,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         mma_commit(bar(L::bSFull + x));
                     }
                     if (!ok) break;
-                    mma_commit(bar(L::bKEmpty + t % L::kKStages));
                     if (nmax == 1) mma_commit(bar(L::bQEmpty));
                     // Per key tile j: O_A += P_A V_j, S_A(j+1), O_B += P_B V_j, S_B(j+1).
                     for (int j = 0; j < nmax; ++j, ++t) {
@@ -621,11 +618,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                             mma_commit(bar(L::bSFull + x));
                         }
                         if (!ok) break;
+                        // releases V_j, and with it the K stages (see PairLayout)
                         mma_commit(bar(L::bVEmpty + t % L::kVStages));
-                        if (j + 1 < nmax) {
-                            mma_commit(bar(L::bKEmpty + t1 % L::kKStages));
-                            if (j + 2 == nmax) mma_commit(bar(L::bQEmpty));  // last reader of Q
-                        }
+                        if (j + 2 == nmax) mma_commit(bar(L::bQEmpty));  // last reader of Q
                     }
                     if (!ok) break;
     #pragma unroll
