@@ -84,7 +84,9 @@ TRAFFIC = {("bwd_main", "sdpa_gb300 0.4 sm_103a"): 0.81430e9 + 0.49046e9,
            ("bwd_main", "sdpa_gb300 0.18 sm_103a"): 0.84556e9 + 0.51496e9,
            # 0.19 and 0.20 changed the two-tile forward's load barriers only
            ("bwd_main", "sdpa_gb300 0.19 sm_103a"): 0.84556e9 + 0.51496e9,
-           ("bwd_main", "sdpa_gb300 0.20 sm_103a"): 0.84556e9 + 0.51496e9}
+           ("bwd_main", "sdpa_gb300 0.20 sm_103a"): 0.84556e9 + 0.51496e9,
+           # 0.21 changed the one-tile forward's load barriers only
+           ("bwd_main", "sdpa_gb300 0.21 sm_103a"): 0.84556e9 + 0.51496e9}
 
 
 def fwd_flops(w) -> float:

@@ -26,7 +26,9 @@
 // memory); a unit past its sequence's end costs a few instructions.
 //
 // Roles inside a CTA:
-//   warp 0      TMA producer: Q of each unit, then K_j / V_j into two rings;
+//   warp 0      TMA producer: Q and the first K tile of each unit, then per
+//               key tile j the pair V_j, K_{j+1} on one barrier (K and V keep
+//               rings of their own);
 //   warp 1      MMA issuer (one thread): S_t = Q K_t^T into TMEM (two S
 //               buffers, alternating over the CTA's running tile count t),
 //               then O += P_t V_t with P_t read straight from TMEM;
@@ -57,10 +59,15 @@ struct FwdLayout {
     static constexpr int kChunks = D * kEb / 128;          // 128-byte swizzle columns per row
     static constexpr int kChunkBytes = kTileM * 128;      // 16 KiB: 128 rows x 128 bytes
     static constexpr int kTileBytes = kChunks * kChunkBytes;
-    // K and V have rings of their own: a K stage is released once S = Q K^T
-    // has read it, a V stage once O += P V has, so the next loads start early.
+    // K and V have rings of their own.  Per key tile t the producer issues
+    // V_t and K_{t+1} as a pair on V_t's full barrier, and a V stage is
+    // released once O += P V has read it.  That release also frees the K ring:
+    // K_{i-kKStages} is read by S products issued before the release of
+    // V_{i-1-kVStages}, which the producer waits for before it loads K_i, as
+    // long as the K ring is at least one stage deeper than the V ring.
     static constexpr int kKStages = (kTileBytes >= 32768) ? 3 : 5;
     static constexpr int kVStages = (kTileBytes >= 32768) ? 2 : 4;
+    static_assert(kKStages >= kVStages + 1, "the V releases must cover the K ring");
     // Q is double-buffered by unit parity so the next unit's Q arrives while
     // the current unit still runs.
     static constexpr int kQStages = 2;
@@ -79,8 +86,7 @@ struct FwdLayout {
     static constexpr int bQFull = 0;   // two
     static constexpr int bQEmpty = 2;  // two
     static constexpr int bKFull = 4;
-    static constexpr int bKEmpty = bKFull + kKStages;
-    static constexpr int bVFull = bKEmpty + kKStages;
+    static constexpr int bVFull = bKFull + kKStages;
     static constexpr int bVEmpty = bVFull + kVStages;
     static constexpr int bSFull = bVEmpty + kVStages;  // two
     // P_t ready / P_t V_t retired: two barriers each, indexed by t & 1, so no
@@ -332,10 +338,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(L::bQFull + b), 1);
             mbar_init(bar(L::bQEmpty + b), 1);
         }
-        for (int s = 0; s < L::kKStages; ++s) {
-            mbar_init(bar(L::bKFull + s), 1);
-            mbar_init(bar(L::bKEmpty + s), 1);
-        }
+        for (int s = 0; s < L::kKStages; ++s) mbar_init(bar(L::bKFull + s), 1);
         for (int s = 0; s < L::kVStages; ++s) {
             mbar_init(bar(L::bVFull + s), 1);
             mbar_init(bar(L::bVEmpty + s), 1);
@@ -377,22 +380,16 @@ __global__ void __launch_bounds__(192, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            // V_x is issued one tile after K_x, so a wait for a free V stage
-            // never holds back the K load that the next S product needs first.
+            // Per unit: Q, the unit's first K tile (on its K stage's full
+            // barrier), then per key tile j the pair V_j, K_{j+1}, both on V_j's
+            // full barrier, so the MMA thread waits once per key tile.  A K tile
+            // that rides on a V barrier gives its own stage's full barrier a
+            // plain arrive, so the K barriers keep one phase per K tile; the
+            // MMA thread waits on them only for a unit's first K, whose stage
+            // cannot be refilled before that wait (the refill waits for a V
+            // release that the MMA thread commits only after it).
             int k_it = 0, v_it = 0, units = 0;
-            int pv_y = 0, pv_z = 0;
-            bool v_pending = false, ok = true;
-            auto issue_v = [&](int y, int z) -> bool {
-                const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
-                if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) return false;
-                mbar_arrive_expect_tx(bar(L::bVFull + vs), L::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
-                                bar(L::bVFull + vs), c * (128 / kEb), y, z);
-                ++v_it;
-                return true;
-            };
+            bool ok = true;
             for (int k = 0; ok; ++k) {
                 int u;
                 if constexpr (kDyn) {
@@ -411,9 +408,6 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
                 if (U.n_kv == 0) continue;
-                // the previous unit's last V goes out before waiting for Q's slot
-                if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
-                v_pending = false;
                 const int qs = units & 1;
                 if (units > 1 && !mbar_wait(bar(L::bQEmpty + qs), ((units - 2) >> 1) & 1, wc, 1)) break;
                 const int qy = kPacked ? U.head : U.row0;
@@ -424,28 +418,50 @@ __global__ void __launch_bounds__(192, 1)
                     tma_load_3d(sbase + L::kQ + qs * L::kTileBytes + c * L::kChunkBytes, &tm_q,
                                 bar(L::bQFull + qs), c * (128 / kEb), qy, qz);
                 ++units;
-                for (int j = 0; j < U.n_kv; ++j) {
+                // key tile j of the unit: (y, z) coordinates of K_j and V_j
+                auto kv_yz = [&](int j, int &y, int &z) {
                     const int k0 = (U.kt0 + j) * kTileN;
-                    const int ky = kPacked ? U.kv_head : k0;
-                    const int kz = kPacked ? U.tok_kv0 + k0 : U.kv_slice;
-                    const int ks = k_it % L::kKStages, kuse = k_it / L::kKStages;
-                    if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 2)) {
+                    y = kPacked ? U.kv_head : k0;
+                    z = kPacked ? U.tok_kv0 + k0 : U.kv_slice;
+                };
+                // K tile number k_it into its stage (free: see FwdLayout), on `full`
+                auto load_k = [&](uint32_t full, int j) {
+                    int ky, kz;
+                    kv_yz(j, ky, kz);
+                    const int ks = k_it % L::kKStages;
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k, full,
+                                    c * (128 / kEb), ky, kz);
+                    ++k_it;
+                };
+                {
+                    const uint32_t kfull = bar(L::bKFull + k_it % L::kKStages);
+                    mbar_arrive_expect_tx(kfull, L::kTileBytes);
+                    load_k(kfull, 0);
+                }
+                for (int j = 0; j < U.n_kv; ++j) {
+                    const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
+                    if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(L::bKFull + ks), L::kTileBytes);
+                    const bool pair_k = j + 1 < U.n_kv;
+                    const uint32_t vfull = bar(L::bVFull + vs);
+                    int vy, vz;
+                    kv_yz(j, vy, vz);
+                    mbar_arrive_expect_tx(vfull, pair_k ? 2 * L::kTileBytes : L::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
-                                    bar(L::bKFull + ks), c * (128 / kEb), ky, kz);
-                    ++k_it;
-                    if (v_pending && !(ok = issue_v(pv_y, pv_z))) break;
-                    pv_y = ky;
-                    pv_z = kz;
-                    v_pending = true;
+                        tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v, vfull,
+                                    c * (128 / kEb), vy, vz);
+                    ++v_it;
+                    if (pair_k) {
+                        mbar_arrive(bar(L::bKFull + k_it % L::kKStages));
+                        load_k(vfull, j + 1);
+                    }
                 }
             }
-            if (ok && v_pending) issue_v(pv_y, pv_z);
             // Every load issued must land before the CTA may exit.
             for (int i = max(0, units - 2); i < units; ++i)
                 mbar_wait_drain(bar(L::bQFull + (i & 1)), (i >> 1) & 1);
@@ -500,15 +516,14 @@ __global__ void __launch_bounds__(192, 1)
             // S_x goes to S buffer x&1, which held P_{x-2}: it waits for that
             // P V product (barrier x&1 again, phase (x-2)>>1).  Every P V phase
             // is waited here in order, so the waits stay within one phase.
+            // K_x has landed when this is called: a unit's first K tile is
+            // waited for on its own barrier, every other one with V_{x-1}.
             auto issue_s_tile = [&](int x) -> bool {
-                if (!mbar_wait(bar(L::bKFull + x % L::kKStages), (x / L::kKStages) & 1, wc, 5))
-                    return false;
                 if (x >= 2 && !mbar_wait(bar(L::bPVDone + (x & 1)), ((x - 2) >> 1) & 1, wc, 6))
                     return false;
                 tc_fence_after();
                 issue_s(x % L::kKStages, (x & 1) * 128);
                 mma_commit(bar(L::bSFull + (x & 1)));
-                mma_commit(bar(L::bKEmpty + x % L::kKStages));
                 return true;
             };
             int t = 0;  // tiles processed by this CTA
@@ -527,16 +542,20 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const Unit U = decode_unit<D, kPacked>(p, u, cu_q, cu_kv, slice_major, order, first_s);
                 if (U.n_kv == 0) continue;
-                ok = mbar_wait(bar(L::bQFull + (units & 1)), (units >> 1) & 1, wc, 4) && issue_s_tile(t);
+                ok = mbar_wait(bar(L::bQFull + (units & 1)), (units >> 1) & 1, wc, 4) &&
+                     mbar_wait(bar(L::bKFull + t % L::kKStages), (t / L::kKStages) & 1, wc, 5) &&
+                     issue_s_tile(t);
                 if (!ok) break;
                 if (U.n_kv == 1) mma_commit(bar(L::bQEmpty + (units & 1)));
                 for (int j = 0; j < U.n_kv; ++j, ++t) {
+                    // V_t and, within the unit, K_{t+1} (see the producer)
+                    if (!(ok = mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 10)))
+                        break;
                     if (j + 1 < U.n_kv) {
                         if (!(ok = issue_s_tile(t + 1))) break;
                         if (j + 2 == U.n_kv) mma_commit(bar(L::bQEmpty + (units & 1)));  // last reader of Q
                     }
-                    ok = mbar_wait(bar(L::bPReady + (t & 1)), (t >> 1) & 1, wc, 9) &&
-                         mbar_wait(bar(L::bVFull + t % L::kVStages), (t / L::kVStages) & 1, wc, 10);
+                    ok = mbar_wait(bar(L::bPReady + (t & 1)), (t >> 1) & 1, wc, 9);
                     // The unit's first P V overwrites O buffer units&1: the epilogue
                     // of the unit two back must have read it out.
                     if (ok && j == 0 && units > 1)
