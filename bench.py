@@ -86,7 +86,9 @@ TRAFFIC = {("bwd_main", "sdpa_gb300 0.4 sm_103a"): 0.81430e9 + 0.49046e9,
            ("bwd_main", "sdpa_gb300 0.19 sm_103a"): 0.84556e9 + 0.51496e9,
            ("bwd_main", "sdpa_gb300 0.20 sm_103a"): 0.84556e9 + 0.51496e9,
            # 0.21 changed the one-tile forward's load barriers only
-           ("bwd_main", "sdpa_gb300 0.21 sm_103a"): 0.84556e9 + 0.51496e9}
+           ("bwd_main", "sdpa_gb300 0.21 sm_103a"): 0.84556e9 + 0.51496e9,
+           # 0.22 changed the deterministic dQ pass only
+           ("bwd_main", "sdpa_gb300 0.22 sm_103a"): 0.84556e9 + 0.51496e9}
 
 
 def fwd_flops(w) -> float:

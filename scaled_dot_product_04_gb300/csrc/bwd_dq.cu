@@ -17,9 +17,9 @@
 // pairs that sum to -LSE/scale and -D); each thread owns one query row (TMEM
 // lane), so they are plain registers here.
 //
-// Roles (192 threads): warp 0 TMA (Q and dO once, then K_j / V_j into rings
-// of three and two stages), warp 1 MMA issuer, warps 2-5 compute (thread =
-// row).
+// Roles (192 threads): warp 0 TMA (Q and dO once, then K_j and V_j, into
+// rings of three and two stages, on one barrier), warp 1 MMA issuer, warps
+// 2-5 compute (thread = row).
 // TMEM: S_j in buffer j & 1 (columns 0 and 128), dP at 256, dQ at 384.
 // dS'_j goes back packed into the first 64 columns of its S buffer and feeds
 // dQ += dS'_j K_j straight from TMEM; S_{j+1} is issued into the other buffer
@@ -38,19 +38,23 @@ struct DqLayout {
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     // K_j is read by S_j and, one tile later, by dQ += dS'_j K_j, so the K
     // ring has a third stage for the load of K_{j+2} to overlap dQ_j; V_j is
-    // read by dP_j alone.
+    // read by dP_j alone.  K_j and V_j land on one barrier (K_j's full
+    // barrier).  A V stage is released once dP has read it, and that release
+    // also frees the K ring: the pair K_j, V_j takes the stages of
+    // K_{j-kKStages} and V_{j-kVStages}, and V_{j-kVStages}'s release is
+    // committed behind dP_{j-kVStages}, which is issued after dQ_{j-kKStages},
+    // the last reader of K_{j-kKStages}, when the K ring is one stage deeper.
     static constexpr int kKStages = 3;
     static constexpr int kVStages = 2;
+    static_assert(kKStages == kVStages + 1, "the V releases must cover the K ring");
     static constexpr int kQ = 0;
     static constexpr int kDO = kQ + kTileBytes;
     static constexpr int kK = kDO + kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
     static constexpr int kBar = kV + kVStages * kTileBytes;
     static constexpr int bQFull = 0;                 // Q and dO
-    static constexpr int bKFull = 1;
-    static constexpr int bKEmpty = bKFull + kKStages;
-    static constexpr int bVFull = bKEmpty + kKStages;
-    static constexpr int bVEmpty = bVFull + kVStages;
+    static constexpr int bKFull = 1;                 // K_j and V_j
+    static constexpr int bVEmpty = bKFull + kKStages;
     static constexpr int bSFull = bVEmpty + kVStages;  // two: S buffer
     static constexpr int bDPFull = bSFull + 2;
     static constexpr int bDSReady = bDPFull + 1;      // two: S buffer holds dS'
@@ -149,14 +153,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::bQFull), 1);
-        for (int s = 0; s < L::kKStages; ++s) {
-            mbar_init(bar(L::bKFull + s), 1);
-            mbar_init(bar(L::bKEmpty + s), 1);
-        }
-        for (int s = 0; s < L::kVStages; ++s) {
-            mbar_init(bar(L::bVFull + s), 1);
-            mbar_init(bar(L::bVEmpty + s), 1);
-        }
+        for (int s = 0; s < L::kKStages; ++s) mbar_init(bar(L::bKFull + s), 1);
+        for (int s = 0; s < L::kVStages; ++s) mbar_init(bar(L::bVEmpty + s), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::bSFull + b), 1);
             mbar_init(bar(L::bDSReady + b), kTileM);
@@ -193,34 +191,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 tma_load_3d(sbase + L::kQ + c * L::kChunkBytes, &tm_q, bar(L::bQFull), c * 64, qy, qz);
                 tma_load_3d(sbase + L::kDO + c * L::kChunkBytes, &tm_do, bar(L::bQFull), c * 64, qy, qz);
             }
-            int k_issued = 0, v_issued = 0;
+            int issued = 0;
             for (int j = 0; j < n; ++j) {
                 const int k0 = (U.kt0 + j) * kTileN;
                 const int ky = kPacked ? U.kv_head : k0;
                 const int kz = kPacked ? U.tok_kv0 + k0 : U.kv_slice;
-                const int ks = j % L::kKStages, kuse = j / L::kKStages;
-                if (kuse > 0 && !mbar_wait(bar(L::bKEmpty + ks), (kuse - 1) & 1, wc, 1)) break;
-                mbar_arrive_expect_tx(bar(L::bKFull + ks), L::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k,
-                                bar(L::bKFull + ks), c * 64, ky, kz);
-                k_issued = j + 1;
-                const int vs = j % L::kVStages, vuse = j / L::kVStages;
+                // the V stage's release also frees the K stage (see DqLayout)
+                const int ks = j % L::kKStages, vs = j % L::kVStages, vuse = j / L::kVStages;
                 if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 2)) break;
-                mbar_arrive_expect_tx(bar(L::bVFull + vs), L::kTileBytes);
+                const uint32_t full = bar(L::bKFull + ks);
+                mbar_arrive_expect_tx(full, 2 * L::kTileBytes);
 #pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v,
-                                bar(L::bVFull + vs), c * 64, ky, kz);
-                v_issued = j + 1;
+                for (int c = 0; c < L::kChunks; ++c) {
+                    tma_load_3d(sbase + L::kK + ks * L::kTileBytes + c * L::kChunkBytes, &tm_k, full, c * 64,
+                                ky, kz);
+                    tma_load_3d(sbase + L::kV + vs * L::kTileBytes + c * L::kChunkBytes, &tm_v, full, c * 64,
+                                ky, kz);
+                }
+                issued = j + 1;
             }
             // every load issued must land before the CTA may exit
             mbar_wait_drain(bar(L::bQFull), 0);
-            for (int j = max(0, k_issued - L::kKStages); j < k_issued; ++j)
+            for (int j = max(0, issued - L::kKStages); j < issued; ++j)
                 mbar_wait_drain(bar(L::bKFull + j % L::kKStages), (j / L::kKStages) & 1);
-            for (int j = max(0, v_issued - L::kVStages); j < v_issued; ++j)
-                mbar_wait_drain(bar(L::bVFull + j % L::kVStages), (j / L::kVStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -249,9 +242,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 mma_commit(bar(L::bSFull + (j & 1)));
                 return true;
             };
-            auto issue_dp = [&](int j) -> bool {  // dP_j
+            auto issue_dp = [&](int j) -> bool {  // dP_j: V_j landed with K_j, waited for by S_j
                 const int st = j % L::kVStages;
-                if (!mbar_wait(bar(L::bVFull + st), (j / L::kVStages) & 1, wc, 5)) return false;
                 tc_fence_after();
                 issue_nt(dDO_k, dV_k + st * kTile16, L::kColDP);
                 mma_commit(bar(L::bDPFull));
@@ -273,7 +265,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                                (j > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(L::bDQDone + (j & 1)));
-                mma_commit(bar(L::bKEmpty + j % L::kKStages));
                 // dP_{j+1} overwrites dP_j, which the compute warps have read
                 // (they wrote dS'_j after loading it)
                 if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
