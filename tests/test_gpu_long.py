@@ -6,6 +6,8 @@ scale 1/sqrt(d):
   to 512 key tiles and the backward's units up to 512 query tiles, four times the
   16,384-token workload's (d = 64 runs the other TMEM layout: dQ has columns of
   its own and dO two stages);
+- the FP8 (E4M3) forward of the d = 128 causal head, within the bound derived for
+  E4M3 P;
 - a bottom-right band (window_left 5000) with s_q = 61,000 (a ragged last
   query tile) against s_kv = 65,536, two query heads on one key/value head,
   d = 128.
@@ -120,3 +122,40 @@ def test_long_sequence_sampled_rows(sdpa, name):
     for hk in range(c["h_kv"]):
         check_rel(dk[0, hk, ki], rdk[hk], GRAD_TOL, f"dk[{hk}]")
         check_rel(dv[0, hk, ki], rdv[hk], GRAD_TOL, f"dv[{hk}]")
+
+
+@functools.lru_cache(maxsize=None)
+def _fp8_reference(name):
+    """The E4M3 encoding of the case's inputs (codes, descales), the decoded
+    values and the oracle's rows of the forward on them (query head 0)."""
+    c = CASES[name]
+    q, k, v, _ = _inputs(name)
+    enc = [sdpa_inputs.fp8_quantize(x.float()) for x in (q, k, v)]
+    (qc, dsq), (kc, dsk), (vc, dsv) = enc
+    qd = oracle.e4m3_to_f64(qc[0, 0], dsq)
+    kd = oracle.e4m3_to_f64(kc[0, 0], dsk)
+    vd = oracle.e4m3_to_f64(vc[0, 0], dsv)
+    q_rows = _rows(c["s_q"], c["seed"] + 3)
+    ro, rl = oracle.attn_fwd_rows_ex(qd, kd, vd, q_rows, _scale(c), c["mask"], c["window"])
+    return enc, q_rows, ro, rl, float(np.abs(vd).max())
+
+
+def test_long_sequence_fp8_forward_sampled_rows(sdpa):
+    """The FP8 forward over the 65,536-token causal head: O within the bound
+    derived for E4M3 P (2^-4 max|V| + 2^-8 max|O| of the oracle on the decoded
+    inputs), LSE within 1e-3."""
+    name = "causal_s65536"
+    c = CASES[name]
+    enc, q_rows, ro, rl, vmax = _fp8_reference(name)
+    (qc, dsq), (kc, dsk), (vc, dsv) = enc
+    ds = [torch.tensor([x], dtype=torch.float32, device="cuda") for x in (dsq, dsk, dsv)]
+    o, lse, _ = sdpa.attention_fp8(qc.cuda(), kc.cuda(), vc.cuda(), *ds, scale=_scale(c),
+                                   causal=True)
+    torch.cuda.synchronize()
+    qi = torch.from_numpy(q_rows).long()
+    o, lse = o[0, 0, qi].cpu(), lse[0, 0, qi].cpu()
+    assert torch.isfinite(o.float()).all()
+    err = float(np.abs(o.double().numpy() - ro).max())
+    bound = 2.0 ** -4 * vmax + 2.0 ** -8 * float(np.abs(ro).max()) + 1e-6
+    assert err <= bound, f"max|dO| {err:.3e} > bound {bound:.3e}"
+    check_lse(lse, rl, "lse")
