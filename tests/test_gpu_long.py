@@ -8,6 +8,9 @@ scale 1/sqrt(d):
   its own and dO two stages);
 - the FP8 (E4M3) forward of the d = 128 causal head, within the bound derived for
   E4M3 P;
+- a packed list of one 40,997-token sequence among short and ragged ones (1 to 2049
+  tokens), two query heads on one key/value head, causal (sequences shorter than 8
+  tokens have their gradients checked by the whole-tensor tests only, reading 8);
 - a bottom-right band (window_left 5000) with s_q = 61,000 (a ragged last
   query tile) against s_kv = 65,536, two query heads on one key/value head,
   d = 128.
@@ -159,3 +162,64 @@ def test_long_sequence_fp8_forward_sampled_rows(sdpa):
     bound = 2.0 ** -4 * vmax + 2.0 ** -8 * float(np.abs(ro).max()) + 1e-6
     assert err <= bound, f"max|dO| {err:.3e} > bound {bound:.3e}"
     check_lse(lse, rl, "lse")
+
+
+# A packed list with one long sequence among short and ragged ones, two query
+# heads on one key/value head, causal: the packed forward takes the long
+# sequence's units first and the short ones on demand; the backward walks up
+# to 321 query tiles per unit.
+PACKED_LENS = [40997, 1, 127, 128, 129, 700, 2049, 33]
+
+
+@functools.lru_cache(maxsize=None)
+def _packed_inputs():
+    return sdpa_inputs.packed(PACKED_LENS, PACKED_LENS, 2, 128, seed=40997, h_kv=1)
+
+
+@functools.lru_cache(maxsize=None)
+def _packed_reference():
+    """Per sequence: its sampled rows, O/LSE/dQ rows per query head and dK/dV
+    rows summed over the two query heads."""
+    q, k, v, do, cu, _ = _packed_inputs()
+    scale = 1.0 / math.sqrt(128)
+    out = []
+    for n, L in enumerate(PACKED_LENS):
+        t0 = int(cu[n])
+        rows = np.arange(L, dtype=np.int32) if L <= 300 else _rows(L, 7 + n)
+        o, lse, dq = [], [], []
+        dk = np.zeros((len(rows), 128))
+        dv = np.zeros((len(rows), 128))
+        for hq in range(2):
+            args = (q[t0:t0 + L, hq], k[t0:t0 + L, 0], v[t0:t0 + L, 0])
+            ro, rl = oracle.attn_fwd_rows_ex(*args, rows, scale, "top_left", -1)
+            rdq, rdk, rdv = oracle.attn_bwd_rows_ex(*args, do[t0:t0 + L, hq], rows, rows, scale,
+                                                    "top_left", -1)
+            o.append(ro)
+            lse.append(rl)
+            dq.append(rdq)
+            dk += rdk
+            dv += rdv
+        out.append((t0, rows, o, lse, dq, dk, dv))
+    return out
+
+
+@pytest.mark.usefixtures("bwd_kernel")
+def test_long_packed_sequence_sampled_rows(sdpa):
+    q, k, v, do, cu, _ = (x.cuda() for x in _packed_inputs())
+    mx = max(PACKED_LENS)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = sdpa.attention_varlen(q, k, v, cu, cu, mx, mx, scale=scale, causal=True)
+    dq, dk, dv = sdpa.attention_varlen_bwd(q, k, v, o, do, lse, cu, cu, mx, mx, scale=scale,
+                                           causal=True)
+    torch.cuda.synchronize()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    for n, (t0, rows, ro, rl, rdq, rdk, rdv) in enumerate(_packed_reference()):
+        idx = torch.from_numpy(rows).long() + t0
+        for hq in range(2):
+            check_rel(o[idx, hq], ro[hq], O_TOL[torch.bfloat16], f"o[seq {n}, head {hq}]")
+            check_lse(lse[idx, hq], rl[hq], f"lse[seq {n}, head {hq}]")
+            if PACKED_LENS[n] >= 8:
+                check_rel(dq[idx, hq], rdq[hq], GRAD_TOL, f"dq[seq {n}, head {hq}]")
+        if PACKED_LENS[n] >= 8:
+            check_rel(dk[idx, 0], rdk, GRAD_TOL, f"dk[seq {n}]")
+            check_rel(dv[idx, 0], rdv, GRAD_TOL, f"dv[seq {n}]")
