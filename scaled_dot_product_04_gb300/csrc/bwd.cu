@@ -376,10 +376,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::bDPFull), 1);
         mbar_init(bar(L::bPReady), 256);
         mbar_init(bar(L::bDSReady), 256);
-        mbar_init(bar(L::bDVDone), 1);
         mbar_init(bar(L::bDQFull), 1);
         mbar_init(bar(L::bDQFree), 128);
-        mbar_init(bar(L::bDSFree), 1);
         mbar_init(bar(L::bMmaIdle), 1);
         misc[1] = 0u;
         fence_mbar_init();
@@ -527,13 +525,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ts(tmem + L::kColDV, tmem + L::kColS + (k >> 2) * 64 + (k & 3) * 8,
                                b + k * 128, id_mn, (i > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(L::bDVDone));
-                mma_commit(bar(L::bDOEmpty + dst));
+                mma_commit(bar(L::bDOEmpty + dst));  // also: dV_i has read P^T_i
                 // S'^T_{i+1}, once the dV product has finished reading P^T_i
                 if (i + 1 < n_it) {
                     const int st1 = (i + 1) & 1, use1 = (i + 1) >> 1;
                     ok = mbar_wait_lean(bar(L::bQFull + st1), use1 & 1, wc, 6) &&
-                         mbar_wait_lean(bar(L::bDVDone), i & 1, wc, 7);
+                         mbar_wait_lean(bar(L::bDOEmpty + dst), (i / L::kDOStages) & 1, wc, 7);
                     if (!ok) break;
                     tc_fence_after();
                     issue_kmajor(dK_k, dQ_k + st1 * kTile16, dAS, st1, L::kColS);
@@ -560,8 +557,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_ss(tmem + L::kColDK, dDS_k + kstep(k), b + k * 128, id_mn,
                                (i > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(L::bQEmpty + st));
-                mma_commit(bar(L::bDSFree));
+                mma_commit(bar(L::bQEmpty + st));  // also: dK and dQ have read dS'_i
                 // dP'^T_{i+1}
                 if (i + 1 < n_it) {
                     const int dst1 = L::kDOStages == 1 ? 0 : ((i + 1) & 1);
@@ -637,7 +633,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
             // dS'^T = P^T o dP'^T  ->  shared memory (SW128)
             ok = warp_wait_b(bar(L::bDPFull), i & 1, wc, 14);
-            if (ok && i > 0) ok = warp_wait_b(bar(L::bDSFree), (i - 1) & 1, wc, 15);
+            if (ok && i > 0) ok = warp_wait_b(bar(L::bQEmpty + ((i - 1) & 1)), ((i - 1) >> 1) & 1, wc, 15);
             if (!ok) break;
             tc_fence_after();
             uint32_t dp[64];

@@ -49,16 +49,16 @@ struct BwdLayout {
     static constexpr int bKVFull = 0;
     static constexpr int bQFull = 1;       // 2: Q and its row terms
     static constexpr int bDOFull = 3;      // 2
-    static constexpr int bQEmpty = 7;      // 2: Q (and row terms) stage, freed after dK
-    static constexpr int bDOEmpty = 18;    // kDOStages: dO stage, freed after dV
+    static constexpr int bQEmpty = 7;      // 2: Q (and row terms) stage, freed after dK;
+                                           // it also tells the compute warps that dS' is read
+    static constexpr int bDOEmpty = 18;    // kDOStages: dO stage, freed after dV; it also
+                                           // tells the MMA thread that P^T is read
     static constexpr int bSFull = 9;
     static constexpr int bDPFull = 10;
     static constexpr int bPReady = 11;
     static constexpr int bDSReady = 12;
-    static constexpr int bDVDone = 13;
     static constexpr int bDQFull = 14;
     static constexpr int bDQFree = 15;
-    static constexpr int bDSFree = 16;
     static constexpr int bMmaIdle = 17;
     static constexpr int kNumBars = 20;
     static constexpr int kMisc = kBar + kNumBars * 8;

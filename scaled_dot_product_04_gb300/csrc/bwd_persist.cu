@@ -208,10 +208,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::bDPFull), 1);
         mbar_init(bar(L::bPReady), 256);
         mbar_init(bar(L::bDSReady), 256);
-        mbar_init(bar(L::bDVDone), 1);
         mbar_init(bar(L::bDQFull), 1);
         mbar_init(bar(L::bDQFree), 128);
-        mbar_init(bar(L::bDSFree), 1);
         mbar_init(bar(L::bMmaIdle), 1);
         for (int r = 0; r < R; ++r) {
             mbar_init(pbar(PL::bUFull + r), 1);
@@ -468,12 +466,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             mma_ts(tmem + L::kColDV, tmem + L::kColS + (k >> 2) * 64 + (k & 3) * 8,
                                    b + k * 128, id_mn, (i > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(bar(L::bDVDone));
-                    mma_commit(bar(L::bDOEmpty + dst));
+                    mma_commit(bar(L::bDOEmpty + dst));  // also: dV has read P^T
                     if (i + 1 < U.n_it) {  // S'^T_{G+1}, once dV has read P^T_G
                         const int st1 = (G + 1) & 1;
                         ok = mbar_wait_lean(bar(L::bQFull + st1), ((G + 1) >> 1) & 1, wc, 6) &&
-                             mbar_wait_lean(bar(L::bDVDone), G & 1, wc, 7);
+                             mbar_wait_lean(bar(L::bDOEmpty + dst), (G / L::kDOStages) & 1, wc, 7);
                         if (!ok) break;
                         tc_fence_after();
                         issue_kmajor(dK_k, dQ_k + st1 * kTile16, dAS, st1, L::kColS);
@@ -499,8 +496,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             mma_ss(tmem + L::kColDK, dDS_k + kstep(k), b + k * 128, id_mn,
                                    (i > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(bar(L::bQEmpty + st));
-                    mma_commit(bar(L::bDSFree));
+                    mma_commit(bar(L::bQEmpty + st));  // also: dK and dQ have read dS'
                     if (i + 1 < U.n_it) {  // dP'^T_{G+1}
                         const int dst1 = (G + 1) % L::kDOStages;
                         ok = mbar_wait_lean(bar(L::bDOFull + dst1), ((G + 1) / L::kDOStages) & 1, wc, 10);
@@ -585,7 +581,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(bar(L::bPReady));
 
                 ok = warp_wait_b(bar(L::bDPFull), G & 1, wc, 14);
-                if (ok && G > 0) ok = warp_wait_b(bar(L::bDSFree), (G - 1) & 1, wc, 15);
+                if (ok && G > 0) ok = warp_wait_b(bar(L::bQEmpty + ((G - 1) & 1)), ((G - 1) >> 1) & 1, wc, 15);
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t dp[64];
