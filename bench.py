@@ -90,7 +90,9 @@ TRAFFIC = {("bwd_main", "sdpa_gb300 0.4 sm_103a"): 0.81430e9 + 0.49046e9,
            # 0.22 changed the deterministic dQ pass only
            ("bwd_main", "sdpa_gb300 0.22 sm_103a"): 0.84556e9 + 0.51496e9,
            # 0.23: two of bwd_main's barriers folded into others; captured again
-           ("bwd_main", "sdpa_gb300 0.23 sm_103a"): 0.84483e9 + 0.51597e9}
+           ("bwd_main", "sdpa_gb300 0.23 sm_103a"): 0.84483e9 + 0.51597e9,
+           # 0.24 changed the one-tile forward only
+           ("bwd_main", "sdpa_gb300 0.24 sm_103a"): 0.84483e9 + 0.51597e9}
 
 
 def fwd_flops(w) -> float:

@@ -61,7 +61,7 @@ struct FwdLayout {
     static constexpr int kTileBytes = kChunks * kChunkBytes;
     // K and V have rings of their own.  Per key tile t the producer issues
     // V_t and K_{t+1} as a pair on V_t's full barrier, and a V stage is
-    // released once O += P V has read it.  That release also frees the K ring:
+    // released once O += P V has read it (the P V retired barrier below).  That release also frees the K ring:
     // K_{i-kKStages} is read by S products issued before the release of
     // V_{i-1-kVStages}, which the producer waits for before it loads K_i, as
     // long as the K ring is at least one stage deeper than the V ring.
@@ -87,15 +87,16 @@ struct FwdLayout {
     static constexpr int bQEmpty = 2;  // two
     static constexpr int bKFull = 4;
     static constexpr int bVFull = bKFull + kKStages;
-    static constexpr int bVEmpty = bVFull + kVStages;
-    static constexpr int bSFull = bVEmpty + kVStages;  // two
-    // P_t ready / P_t V_t retired: two barriers each, indexed by t & 1, so no
-    // waiter can ever be two phases away from the barrier it polls.
+    static constexpr int bSFull = bVFull + kVStages;  // two
+    // P_t ready: two barriers, indexed by t & 1; P_t V_t retired: one per V
+    // stage, indexed by t % kVStages, which is also V_t's release (and with it
+    // the K stages', see above).  No waiter can be two phases away from the
+    // barrier it polls.
     static constexpr int bPReady = bSFull + 2;   // two
-    static constexpr int bPVDone = bPReady + 2;  // two
+    static constexpr int bPVDone = bPReady + 2;  // kVStages
     // O is double-buffered by unit parity: the epilogue of unit k overlaps
     // the products of unit k+1.
-    static constexpr int bOFull = bPVDone + 2;   // two: a unit's last P V retired
+    static constexpr int bOFull = bPVDone + kVStages;  // two: a unit's last P V retired
     static constexpr int bOFree = bOFull + 2;    // two: the epilogue has read O
     static constexpr int bMmaIdle = bOFree + 2;
     static constexpr int kNumBars = bMmaIdle + 1;
@@ -341,14 +342,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int s = 0; s < L::kKStages; ++s) mbar_init(bar(L::bKFull + s), 1);
         for (int s = 0; s < L::kVStages; ++s) {
             mbar_init(bar(L::bVFull + s), 1);
-            mbar_init(bar(L::bVEmpty + s), 1);
+            mbar_init(bar(L::bPVDone + s), 1);
         }
         mbar_init(bar(L::bSFull + 0), 1);
         mbar_init(bar(L::bSFull + 1), 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(L::bPReady + b), kTileM);
-            mbar_init(bar(L::bPVDone + b), 1);
-        }
+        for (int b = 0; b < 2; ++b) mbar_init(bar(L::bPReady + b), kTileM);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::bOFull + b), 1);
             mbar_init(bar(L::bOFree + b), kTileM);
@@ -442,7 +440,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 for (int j = 0; j < U.n_kv; ++j) {
                     const int vs = v_it % L::kVStages, vuse = v_it / L::kVStages;
-                    if (vuse > 0 && !mbar_wait(bar(L::bVEmpty + vs), (vuse - 1) & 1, wc, 3)) {
+                    if (vuse > 0 && !mbar_wait(bar(L::bPVDone + vs), (vuse - 1) & 1, wc, 3)) {
                         ok = false;
                         break;
                     }
@@ -514,12 +512,14 @@ __global__ void __launch_bounds__(192, 1)
                 }
             };
             // S_x goes to S buffer x&1, which held P_{x-2}: it waits for that
-            // P V product (barrier x&1 again, phase (x-2)>>1).  Every P V phase
-            // is waited here in order, so the waits stay within one phase.
+            // P V product (barrier (x-2) % kVStages, phase (x-2) / kVStages).
+            // Every P V phase is waited here in order, so the waits stay within
+            // one phase.
             // K_x has landed when this is called: a unit's first K tile is
             // waited for on its own barrier, every other one with V_{x-1}.
             auto issue_s_tile = [&](int x) -> bool {
-                if (x >= 2 && !mbar_wait(bar(L::bPVDone + (x & 1)), ((x - 2) >> 1) & 1, wc, 6))
+                if (x >= 2 &&
+                    !mbar_wait(bar(L::bPVDone + (x - 2) % L::kVStages), ((x - 2) / L::kVStages) & 1, wc, 6))
                     return false;
                 tc_fence_after();
                 issue_s(x % L::kKStages, (x & 1) * 128);
@@ -563,8 +563,7 @@ __global__ void __launch_bounds__(192, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(t % L::kVStages, (t & 1) * 128, L::kColO + (units & 1) * D, j > 0);
-                    mma_commit(bar(L::bPVDone + (t & 1)));
-                    mma_commit(bar(L::bVEmpty + t % L::kVStages));
+                    mma_commit(bar(L::bPVDone + t % L::kVStages));  // also V_t's release
                 }
                 if (!ok) break;
                 mma_commit(bar(L::bOFull + (units & 1)));
@@ -763,7 +762,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                     // O holds the unit's earlier P V products; it may be rescaled
                     // only once the last of them has retired.
-                    ok = warp_wait(bar(L::bPVDone + ((t - 1) & 1)), ((t - 1) >> 1) & 1, wc, 13);
+                    ok = warp_wait(bar(L::bPVDone + (t - 1) % L::kVStages), ((t - 1) / L::kVStages) & 1, wc, 13);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll 1
